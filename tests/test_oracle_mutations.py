@@ -1,0 +1,103 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that a pin catches each.
+
+Each mutant is the oracle's own source with one expression changed, compiled
+into the oracle module's namespace and patched in for the duration of a test.
+A mutant that no pin catches would mean the pins leave that part of the
+oracle unchecked.
+"""
+import inspect
+import textwrap
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kda_oracle as O
+from kda_delta_rule_gb300 import inputs as I
+
+import test_oracle_pins as pins
+
+
+def _mutant(fn, old, new):
+    src = textwrap.dedent(inspect.getsource(fn))
+    assert src.count(old) >= 1, (fn.__name__, old)
+    src = src.replace(old, new, 1)
+    ns = dict(vars(O))
+    exec(compile(src, f"<mutant {fn.__name__}>", "exec"), ns)
+    return ns[fn.__name__]
+
+
+STEP_MUTANTS = {
+    "decay_first_uses_undecayed_delta": (
+        'delta = v - np.einsum("...ij,...i->...j", S_dec, k)',
+        'delta = v - np.einsum("...ij,...i->...j", S, k)'),
+    "update_sign_flipped": (
+        "S_new = S_dec + b * k[..., :, None] * delta[..., None, :]",
+        "S_new = S_dec - b * k[..., :, None] * delta[..., None, :]"),
+    "beta_dropped": (
+        "S_new = S_dec + b * k[..., :, None] * delta[..., None, :]",
+        "S_new = S_dec + k[..., :, None] * delta[..., None, :]"),
+    "decay_on_value_axis": (
+        "decay = np.exp(g)[..., :, None]",
+        "decay = np.exp(g)[..., None, :1]"),
+    "readout_before_write": (
+        'o = np.einsum("...ij,...i->...j", S_new, q)',
+        'o = np.einsum("...ij,...i->...j", S, q)'),
+    "readout_transposed": (
+        'o = np.einsum("...ij,...i->...j", S_new, q)',
+        'o = np.einsum("...ij,...j->...i", S_new, q)'),
+    "page1_decays_before_delta": (
+        'delta = v - np.einsum("...ij,...i->...j", S, k)\n        S_new = decay * S',
+        'delta = v - np.einsum("...ij,...i->...j", decay * S, k)\n        S_new = decay * S'),
+}
+
+CHUNK_MUTANTS = {
+    "P_mask_drops_diagonal": ("EP = np.exp(np.where(lower[:, :, None]",
+                              "EP = np.exp(np.where(lower_strict[:, :, None]"),
+    "A_without_beta": ('A = np.einsum("ri,si,rsi->rs", k, k, EA) * beta[None, :]',
+                       'A = np.einsum("ri,si,rsi->rs", k, k, EA)'),
+    "page1_shift_missing": ("G = Gam if mode == DECAY_FIRST else Gam - g", "G = Gam"),
+    "output_uses_unscaled_delta": ("O = (q * np.exp(Gam)) @ S + P @ bD",
+                                   "O = (q * np.exp(Gam)) @ S + P @ Delta"),
+    "state_decay_missing": ("S_end = np.exp(GL)[:, None] * S +", "S_end = S +"),
+    "wy_sign": ("Delta = U - W @ S", "Delta = U + W @ S"),
+}
+
+
+def _step_pins():
+    for mode in (O.DECAY_FIRST, O.UNDECAYED_DELTA):
+        for T, dk, dv, seed in [(2, 4, 3, 1), (3, 5, 5, 2)]:
+            yield lambda m=mode, a=(T, dk, dv, seed): pins.test_recurrent_equals_unrolled_products(m, *a)
+    yield pins.test_scalar_step_by_hand
+    yield pins.test_two_by_two_step_by_hand
+    yield pins.test_decay_first_perfect_write_and_page1_breaks_it
+    yield pins.test_cold_start_single_token
+
+
+def _caught(pin_iter):
+    for pin in pin_iter:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            return True
+    return False
+
+
+@pytest.mark.parametrize("name", sorted(STEP_MUTANTS))
+def test_step_mutant_is_caught(name, monkeypatch):
+    old, new = STEP_MUTANTS[name]
+    monkeypatch.setattr(O, "kda_step", _mutant(O.kda_step, old, new))
+    assert _caught(_step_pins()), f"no pin catches mutant {name}"
+
+
+@pytest.mark.parametrize("name", sorted(CHUNK_MUTANTS))
+def test_chunk_mutant_is_caught(name, monkeypatch):
+    old, new = CHUNK_MUTANTS[name]
+    monkeypatch.setattr(O, "chunk_step", _mutant(O.chunk_step, old, new))
+    checks = [lambda m=m: pins.test_chunked_equals_recurrent(m, 200, 64)
+              for m in (O.DECAY_FIRST, O.UNDECAYED_DELTA)]
+    assert _caught(checks), f"no pin catches mutant {name}"
+
+
+def test_unmutated_oracle_passes_the_same_pins():
+    assert not _caught(_step_pins())

@@ -1,0 +1,321 @@
+"""Pins of the fp64 oracle to facts the pages and the mathematics fix.
+
+None of these compares the oracle with a retyped copy of itself: each check is
+a hand-derived value, a closed form, an independent formulation (explicit
+transition-matrix products), a value the pages print, or an invariant.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import kda_oracle as O
+from kda_delta_rule_gb300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_printed_values.json")
+f64 = I.to_f64_numpy
+
+
+def _rand_head(T, dk, dv, seed, g_min=-5.0, S_std=0.3):
+    S0, p, _ = I.prefill_inputs(T, 1, dk, dv, dtype=torch.float64, seed=seed,
+                                state_std=S_std, g_min=g_min)
+    a = {n: f64(t)[:, 0] for n, t in p.items()}
+    return f64(S0)[0, 0], a
+
+
+# --------------------------------------------------------------------------
+# Hand-derived scalar examples (dk = dv = 1)
+# --------------------------------------------------------------------------
+
+def test_scalar_step_by_hand():
+    # S0 = 1, k = q = 1, v = 2, e^g = 1/2, beta = 1/2.
+    # decay first: S' = 0.5, delta = 2 - 0.5 = 1.5, S = 0.5 + 0.5*1.5 = 1.25, o = 1.25
+    # undecayed delta: delta = 2 - 1 = 1, S = 0.5 + 0.5*1 = 1.0, o = 1.0
+    args = (np.array([[1.0]]), np.array([1.0]), np.array([1.0]), np.array([2.0]),
+            np.array([math.log(0.5)]), np.array(0.5))
+    o, S = O.kda_step(*args, mode=O.DECAY_FIRST)
+    assert S[0, 0] == pytest.approx(1.25, abs=1e-15) and o[0] == pytest.approx(1.25, abs=1e-15)
+    o, S = O.kda_step(*args, mode=O.UNDECAYED_DELTA)
+    assert S[0, 0] == pytest.approx(1.0, abs=1e-15) and o[0] == pytest.approx(1.0, abs=1e-15)
+
+
+def test_two_by_two_step_by_hand():
+    # dk = dv = 2, S0 = I, k = (0.6, 0.8), q = (1, 0), v = (1, -1), g = (0, ln 0.5), beta = 1.
+    # decay first: S' = diag(1, .5); S'^T k = (0.6, 0.4); delta = (0.4, -1.4)
+    #   S = S' + k delta^T = [[1.24, -0.84], [0.32, -0.62]]; o = row 0 = (1.24, -0.84)
+    # undecayed: S^T k = (0.6, 0.8); delta = (0.4, -1.8)
+    #   S = diag(1,.5) + k delta^T = [[1.24, -1.08], [0.32, -0.94]]; o = (1.24, -1.08)
+    S0 = np.eye(2)
+    k = np.array([0.6, 0.8]); q = np.array([1.0, 0.0]); v = np.array([1.0, -1.0])
+    g = np.array([0.0, math.log(0.5)]); beta = np.array(1.0)
+    o, S = O.kda_step(S0, q, k, v, g, beta, O.DECAY_FIRST)
+    np.testing.assert_allclose(S, [[1.24, -0.84], [0.32, -0.62]], atol=1e-14)
+    np.testing.assert_allclose(o, [1.24, -0.84], atol=1e-14)
+    o, S = O.kda_step(S0, q, k, v, g, beta, O.UNDECAYED_DELTA)
+    np.testing.assert_allclose(S, [[1.24, -1.08], [0.32, -0.94]], atol=1e-14)
+    np.testing.assert_allclose(o, [1.24, -1.08], atol=1e-14)
+    assert np.array_equal(S0, np.eye(2))           # the input state is not modified
+
+
+# --------------------------------------------------------------------------
+# Brute force: explicit products of the dk x dk transitions, tiny T
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", [O.DECAY_FIRST, O.UNDECAYED_DELTA])
+@pytest.mark.parametrize("T,dk,dv,seed", [(1, 3, 2, 0), (2, 4, 3, 1), (3, 5, 4, 2), (3, 2, 6, 3)])
+def test_recurrent_equals_unrolled_products(mode, T, dk, dv, seed):
+    S0, a = _rand_head(T, dk, dv, seed)
+    o_ref, S_ref = O.unrolled_products(S0, a["q"], a["k"], a["v"], a["g"], a["beta"], mode)
+    o, S = O.kda_recurrent(S0, a["q"], a["k"], a["v"], a["g"], a["beta"], mode)
+    np.testing.assert_allclose(o, o_ref, atol=1e-13, rtol=0)
+    np.testing.assert_allclose(S, S_ref, atol=1e-13, rtol=0)
+
+
+# --------------------------------------------------------------------------
+# Closed forms and special cases
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", [O.DECAY_FIRST, O.UNDECAYED_DELTA])
+def test_beta_zero_is_pure_decay(mode):
+    T, dk, dv = 7, 6, 5
+    S0, a = _rand_head(T, dk, dv, 11)
+    beta = np.zeros(T)
+    o, S, states = O.kda_recurrent(S0, a["q"], a["k"], a["v"], a["g"], beta, mode,
+                                   return_states=True)
+    cum = np.cumsum(a["g"], axis=0)
+    for t in range(T):
+        S_t = np.exp(cum[t])[:, None] * S0
+        np.testing.assert_allclose(states[t + 1], S_t, atol=1e-14)
+        np.testing.assert_allclose(o[t], S_t.T @ a["q"][t], atol=1e-14)
+
+
+def test_zero_gate_modes_coincide_and_equal_plain_delta_rule():
+    # g = 0: both orderings reduce to S_t = (I - beta k k^T) S_{t-1} + beta k v^T.
+    T, dk, dv = 9, 5, 4
+    S0, a = _rand_head(T, dk, dv, 12)
+    g0 = np.zeros_like(a["g"])
+    o0, S0_ = O.kda_recurrent(S0, a["q"], a["k"], a["v"], g0, a["beta"], O.DECAY_FIRST)
+    o1, S1_ = O.kda_recurrent(S0, a["q"], a["k"], a["v"], g0, a["beta"], O.UNDECAYED_DELTA)
+    np.testing.assert_allclose(o0, o1, atol=1e-14)
+    np.testing.assert_allclose(S0_, S1_, atol=1e-14)
+    S = S0.copy()
+    for t in range(T):
+        k = a["k"][t]
+        S = (np.eye(dk) - a["beta"][t] * np.outer(k, k)) @ S + a["beta"][t] * np.outer(k, a["v"][t])
+        np.testing.assert_allclose(o0[t], S.T @ a["q"][t], atol=1e-13)
+    np.testing.assert_allclose(S0_, S, atol=1e-13)
+
+
+def test_decay_first_perfect_write_and_page1_breaks_it():
+    # beta = 1, |k| = 1: decay first gives S_t^T k_t = v_t exactly (the write
+    # fully corrects the decayed prediction).  The undecayed-delta ordering
+    # does not when g != 0, which tells the two orderings apart.
+    T, dk, dv = 6, 8, 5
+    S0, a = _rand_head(T, dk, dv, 13)
+    ones = np.ones(T)
+    _, _, st = O.kda_recurrent(S0, a["q"], a["k"], a["v"], a["g"], ones, O.DECAY_FIRST,
+                               return_states=True)
+    for t in range(T):
+        np.testing.assert_allclose(st[t + 1].T @ a["k"][t], a["v"][t], atol=1e-13)
+    _, _, st1 = O.kda_recurrent(S0, a["q"], a["k"], a["v"], a["g"], ones, O.UNDECAYED_DELTA,
+                                return_states=True)
+    worst = max(np.abs(st1[t + 1].T @ a["k"][t] - a["v"][t]).max() for t in range(T))
+    assert worst > 1e-3
+
+
+def test_cold_start_single_token():
+    # S0 = 0, T = 1: o = beta (k . q) v in both orderings.
+    dk, dv = 7, 3
+    _, a = _rand_head(1, dk, dv, 14)
+    for mode in (O.DECAY_FIRST, O.UNDECAYED_DELTA):
+        o, S = O.kda_step(np.zeros((dk, dv)), a["q"][0], a["k"][0], a["v"][0], a["g"][0],
+                          a["beta"][0], mode)
+        np.testing.assert_allclose(o, a["beta"][0] * (a["k"][0] @ a["q"][0]) * a["v"][0],
+                                   atol=1e-15)
+        np.testing.assert_allclose(S, a["beta"][0] * np.outer(a["k"][0], a["v"][0]), atol=1e-15)
+
+
+def test_ut_inverse_is_the_inverse():
+    rng = np.random.default_rng(3)
+    A = np.tril(rng.standard_normal((12, 12)) * 0.3, -1)
+    T = O.ut_inverse(A)
+    np.testing.assert_allclose(T @ (np.eye(12) + A), np.eye(12), atol=1e-12)
+    np.testing.assert_allclose(T, np.linalg.inv(np.eye(12) + A), atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Chunked WY/UT form == token recurrence (an independent algorithm)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", [O.DECAY_FIRST, O.UNDECAYED_DELTA])
+@pytest.mark.parametrize("T,chunk", [(64, 64), (200, 64), (131, 16), (5, 64), (96, 32)])
+def test_chunked_equals_recurrent(mode, T, chunk):
+    S0, p, cu = I.prefill_inputs(T, 2, 12, 6, dtype=torch.float64, seed=T + chunk)
+    args = [f64(S0)] + [f64(p[n]) for n in ("q", "k", "v", "g", "beta")]
+    oc, Sc, cc = O.prefill_chunked(*args, cu_seqlens=cu, chunk=chunk, ckpt_stride=chunk, mode=mode)
+    orr, Sr, cr = O.prefill_recurrent(*args, cu_seqlens=cu, ckpt_stride=chunk, mode=mode)
+    scale = max(1.0, np.abs(orr).max())
+    assert np.abs(oc - orr).max() <= 1e-10 * scale
+    assert np.abs(Sc - Sr).max() <= 1e-10
+    assert [(n, t) for n, t, _ in cc] == [(n, t) for n, t, _ in cr]
+    for (_, _, a), (_, _, b) in zip(cc, cr):
+        assert np.abs(a - b).max() <= 1e-10
+
+
+def test_chunked_strong_decay_no_overflow():
+    # Cumulative log-decay over a 64-token chunk reaches about -300 here; any
+    # factorisation e^{Gamma_r} * e^{-Gamma_s} would overflow fp32 (and near fp64).
+    T = 128
+    S0, p, cu = I.prefill_inputs(T, 1, 8, 4, dtype=torch.float64, seed=5, g_min=-9.0)
+    args = [f64(S0)] + [f64(p[n]) for n in ("q", "k", "v", "g", "beta")]
+    assert np.cumsum(args[4][:64, 0], axis=0).min() < -200
+    oc, Sc, _ = O.prefill_chunked(*args, cu_seqlens=cu, chunk=64, ckpt_stride=64)
+    orr, Sr, _ = O.prefill_recurrent(*args, cu_seqlens=cu, ckpt_stride=64)
+    assert np.isfinite(oc).all() and np.isfinite(Sc).all()
+    assert np.abs(oc - orr).max() <= 1e-10 and np.abs(Sc - Sr).max() <= 1e-10
+
+
+def test_varlen_is_independent_sequences():
+    lengths = [64, 128, 37, 0, 192]
+    S0, p, cu = I.prefill_inputs(lengths, 2, 8, 4, dtype=torch.float64, seed=21)
+    args = [f64(S0)] + [f64(p[n]) for n in ("q", "k", "v", "g", "beta")]
+    o, S, ck = O.prefill_chunked(*args, cu_seqlens=cu, chunk=64, ckpt_stride=64)
+    for n, L in enumerate(lengths):
+        a, b = cu[n], cu[n + 1]
+        sl = [args[0][n:n + 1]] + [x[a:b] for x in args[1:]]
+        o1, S1, ck1 = O.prefill_recurrent(*sl, cu_seqlens=None, ckpt_stride=64)
+        np.testing.assert_allclose(o[a:b], o1, atol=1e-10)
+        np.testing.assert_allclose(S[n], S1[0], atol=1e-10)
+        mine = [(t, s) for m, t, s in ck if m == n]
+        assert [t for t, _ in mine] == [t for _, t, _ in ck1]
+    np.testing.assert_array_equal(S[3], args[0][3])    # an empty sequence keeps S0
+
+
+# --------------------------------------------------------------------------
+# Checkpoint boundaries
+# --------------------------------------------------------------------------
+
+def test_checkpoint_positions_long_prefill():
+    # T = 8192, stride 512: 16 boundaries 512..8192, the last one at T itself.
+    pos = O.checkpoint_positions(8192, 512)
+    assert pos == [512 * j for j in range(1, 17)]
+    assert O.checkpoint_positions(511, 512) == []
+    assert O.checkpoint_positions(1000, 512) == [512]
+    assert O.num_checkpoints([8192, 1000, 511, 1024], 512) == 16 + 1 + 0 + 2
+
+
+def test_last_checkpoint_is_final_state_bitwise():
+    S0, p, cu = I.prefill_inputs(256, 2, 8, 4, dtype=torch.float64, seed=9)
+    args = [f64(S0)] + [f64(p[n]) for n in ("q", "k", "v", "g", "beta")]
+    o, S, ck = O.prefill_chunked(*args, cu_seqlens=cu, chunk=64, ckpt_stride=128)
+    assert [t for _, t, _ in ck] == [128, 256]
+    assert np.array_equal(ck[-1][2], S[0])
+
+
+# --------------------------------------------------------------------------
+# Replay: the pages' three acceptance scenarios and the clone invariant
+# --------------------------------------------------------------------------
+
+def _golden():
+    with open(GOLDEN) as fh:
+        return json.load(fh)
+
+
+@pytest.mark.parametrize("mode", [O.DECAY_FIRST, O.UNDECAYED_DELTA])
+def test_replay_scenarios_match_recurrent(mode):
+    gold = _golden()
+    draft = gold["acceptance_scenarios"]["draft"]
+    B, H, dk, dv = 2, 3, 8, 8
+    S, proj, _ = I.replay_inputs(B, H, dk, dv, draft, dtype=torch.float64, seed=4)
+    S = f64(S)
+    P = {n: f64(getattr(proj, n)) for n in ("q", "k", "v", "g", "beta")}
+    o_full, _, states = O.kda_recurrent(S, P["q"], P["k"], P["v"], P["g"], P["beta"], mode,
+                                        return_states=True)
+    for n in gold["acceptance_scenarios"]["n_accepted"]:
+        S_before = S.copy()
+        S_new, out = O.verify_and_replay(S, P["q"], P["k"], P["v"], P["g"], P["beta"], n, mode)
+        assert out.shape == (B, H, n, dv)
+        assert np.array_equal(S, S_before)                      # committed state untouched
+        bound = gold["replay_vs_recurrent"]["bound_fp64"]
+        if n:
+            assert np.abs(out - np.moveaxis(o_full[:n], 0, 2)).max() < bound
+        assert np.abs(S_new - states[n]).max() < bound
+        if n == 0:
+            assert np.array_equal(S_new, S)
+
+
+def test_batched_replay_zero_pads_and_matches_per_sequence():
+    B, H, dk, dv, draft = 5, 2, 4, 3, 6
+    S, proj, n_acc = I.replay_inputs(B, H, dk, dv, draft, dtype=torch.float64, seed=8,
+                                     n_accepted=[0, 6, 3, 1, 6])
+    P = {n: f64(getattr(proj, n)) for n in ("q", "k", "v", "g", "beta")}
+    S_new, out = O.verify_and_replay_batched(f64(S), P["q"], P["k"], P["v"], P["g"], P["beta"],
+                                             n_acc.numpy())
+    for b, n in enumerate([0, 6, 3, 1, 6]):
+        o, Sb = O.kda_recurrent(f64(S)[b], P["q"][:n, b], P["k"][:n, b], P["v"][:n, b],
+                                P["g"][:n, b], P["beta"][:n, b])
+        np.testing.assert_allclose(out[b, :, :n], np.moveaxis(o, 0, 1), atol=1e-15)
+        assert np.all(out[b, :, n:] == 0.0)
+        np.testing.assert_allclose(S_new[b], Sb, atol=1e-15)
+
+
+def test_draft_window_layout():
+    # Tab 4 panel b: (draft=3, B=1, H=2, D=3), step i filled with i.
+    lay = _golden()["draft_window_layout"]
+    q = torch.stack([torch.full((lay["B"], lay["H"], lay["D"]), float(i)) for i in range(lay["draft"])])
+    proj = I.DraftProjections(q, q, q, q, q[..., 0])
+    assert tuple(proj.q.shape) == (3, 1, 2, 3) and proj.draft == 3
+    for i in range(3):
+        assert torch.all(proj.q[i] == i)
+
+
+# --------------------------------------------------------------------------
+# Page packing
+# --------------------------------------------------------------------------
+
+def test_pack_layout_and_roundtrip():
+    B, H, dk, dv = 2, 3, 4, 5
+    S = np.random.default_rng(0).standard_normal((B, H, dk, dv))
+    flat = O.pack_heads(S)
+    for b, h, i, j in [(0, 0, 0, 0), (1, 2, 3, 4), (0, 2, 1, 3), (1, 0, 3, 0)]:
+        assert flat[((b * H + h) * dk + i) * dv + j] == S[b, h, i, j]
+    back = O.unpack_heads(flat, B, H, dk, dv)
+    assert np.array_equal(back, S)
+    assert np.abs(back - S).max() < _golden()["pack_roundtrip"]["bound_fp64"]
+
+
+def test_store_load_zero_padded_page():
+    S = np.random.default_rng(1).standard_normal((1, 2, 3, 4))
+    page = O.store_kda(S, 40)
+    assert page.size == 40 and np.all(page[24:] == 0.0)
+    assert np.array_equal(O.load_kda(page, 1, 2, 3, 4), S)
+    with pytest.raises(ValueError):
+        O.store_kda(S, 23)
+
+
+# --------------------------------------------------------------------------
+# Byte accounting
+# --------------------------------------------------------------------------
+
+def test_snapshot_cost_ratio_printed_values():
+    for row in _golden()["snapshot_cost_ratio"]:
+        r = O.snapshot_cost_ratio(row["H"], row["dk"], row["dv"])
+        if row["consistent"]:
+            assert round(r, row["digits"]) == row["printed"], row
+        else:
+            # page error: the closed form gives 1024/129, not the printed 4.0
+            assert r == pytest.approx(1024 / 129) and round(r, 1) != row["printed"]
+
+
+def test_snapshot_cost_ratio_properties():
+    # > 1 and growing with the state size; independent of draft length and dtype.
+    rs = [O.snapshot_cost_ratio(4, d, d) for d in (8, 16, 32, 64, 128)]
+    assert all(r > 1 for r in rs) and all(a < b for a, b in zip(rs, rs[1:]))
+    for draft in (1, 2, 8, 32):
+        for item in (2, 4, 8):
+            snap = draft * O.snapshot_bytes_per_step(16, 32, 32, item)
+            proj = draft * O.projection_bytes_per_step(16, 32, 32, item)
+            assert snap / proj == pytest.approx(O.snapshot_cost_ratio(16, 32, 32))
