@@ -1,0 +1,388 @@
+"""Benchmark of the KDA hot path on GB300.
+
+Main line (``value``): chunked prefill tokens/s on a long single sequence,
+B=1, H=32, dk=dv=128, T=8192, bf16 q/k/v/g/beta, fp32 state, chunk 64,
+checkpoints every 512 tokens (16 pages of 2 MiB written through the pack_heads
+layout).  Inputs (336 MB per step) are larger than L2, so no flush is needed.
+Extra objects in the same JSON line:
+  * ``decode``: 256 consecutive decode steps, B=256, H=32, dk=dv=128, fp32
+    state (512 MiB, > L2), fresh bf16 projections per step: state GB/s;
+  * ``replay``: speculative verify/replay, B=32, H=16, dk=dv=32, draft 8,
+    n_accepted ~ U{0..8}, fp32: amortised GB/s over 64 distinct buffer sets
+    (> L2) and the device time of one call.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# The fp64 oracle runs single-threaded (einsum plus 64x64 BLAS calls): pin BLAS to one
+# thread so the CPU baseline's core count is exact.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kda_delta_rule_gb300 import dist as D           # noqa: E402
+from kda_delta_rule_gb300 import inputs as I         # noqa: E402
+
+H, DK, DV, T, STRIDE, CHUNK = 32, 128, 128, 8192, 512, 64
+DEC_B, DEC_STEPS = 256, 256
+REP_B, REP_H, REP_D, REP_DRAFT, REP_SETS = 32, 16, 32, 8, 64
+WORKLOAD = (f"kda_prefill_chunked long single sequence: B=1 H={H} dk=dv={DK} T={T} bf16 "
+            f"fp32-state chunk={CHUNK} ckpt_stride={STRIDE} (16 checkpoint pages)")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            m = json.load(fh)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def prefill_bytes(T_, H_, dk, dv, es, n_ck, page_bytes, n_seqs=1):
+    tok = T_ * H_ * (3 * dk + 2 * dv + 1) * es            # q,k,g,v,beta in, o out
+    state = 2 * n_seqs * H_ * dk * dv * 4                  # S0 read, S_final write
+    return tok + state + n_ck * page_bytes
+
+
+def prefill_flops(T_, H_, dk, dv, C=CHUNK):
+    # dense chunk form: 2C^2(3dk + 2dv) + 6 C dk dv per chunk and head
+    return (T_ // C) * H_ * (2 * C * C * (3 * dk + 2 * dv) + 6 * C * dk * dv)
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def bench_prefill(K, dev, steps, warmup, rank):
+    torch.manual_seed(rank)
+    S0, p, cu = I.prefill_inputs([T], H, DK, DV, dtype=torch.bfloat16, seed=100 + rank, device=dev)
+    n_ck = K.kda_num_checkpoints(cu, T, STRIDE)
+    page_bytes = H * DK * DV * 4
+    pool = K.PagePool(page_bytes, n_ck, device=dev)
+    ids = torch.tensor(pool.alloc(n_ck), dtype=torch.int32, device=dev)
+    pos = torch.empty(n_ck, dtype=torch.int32, device=dev)
+    o = torch.empty(T, H, DV, dtype=torch.bfloat16, device=dev)
+    S_fin = torch.empty(1, H, DK, DV, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
+                              ckpt_stride=STRIDE, page_pool=pool, ckpt_page_ids=ids, ckpt_pos=pos,
+                              o=o, S_final=S_fin, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    D.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index or 0) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for a, b in evs:
+            a.record(stream)
+            step()
+            b.record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    D.barrier()
+    total_ms = t0.elapsed_time(t1)
+    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    bytes_step = prefill_bytes(T, H, DK, DV, 2, n_ck, page_bytes)
+
+    # end to end through the C ABI from pinned host buffers: H2D inputs, prefill, D2H results
+    host_in = {n: t.to("cpu").pin_memory() for n, t in p.items()}
+    host_S0 = S0.to("cpu").pin_memory()
+    dev_in = {n: torch.empty_like(t) for n, t in p.items()}
+    dev_S0 = torch.empty_like(S0)
+    host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    host_S = torch.empty(S_fin.shape, dtype=S_fin.dtype).pin_memory()
+    host_pages = torch.empty(pool.arena.shape, dtype=torch.uint8).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_S0.numel() * 4
+    d2h = host_o.numel() * 2 + host_S.numel() * 4 + host_pages.numel()
+
+    def e2e_step():
+        for n in dev_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        dev_S0.copy_(host_S0, non_blocking=True)
+        K.kda_prefill_chunked(dev_S0, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"],
+                              dev_in["beta"], cu_seqlens=cu, ckpt_stride=STRIDE, page_pool=pool,
+                              ckpt_page_ids=ids, ckpt_pos=pos, o=o, S_final=S_fin, stream=stream)
+        host_o.copy_(o, non_blocking=True)
+        host_S.copy_(S_fin, non_blocking=True)
+        host_pages.copy_(pool.arena, non_blocking=True)
+
+    for _ in range(warmup):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    D.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    D.barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    return dict(total_ms=total_ms, kern_ms=kern_ms, bytes_step=bytes_step, clocks=clk.summary(),
+                n_ck=n_ck, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+
+
+def bench_decode(K, dev, warmup=3, runs=3):
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    S = (0.05 * torch.randn(DEC_B, H, DK, DV, generator=gen, device=dev)).contiguous()
+    projs = [I.decode_step_projections(DEC_B, H, DK, DV, dtype=torch.bfloat16, seed=1000 + t, device=dev)
+             for t in range(DEC_STEPS)]
+    o = torch.empty(DEC_B, H, DV, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def run():
+        for p in projs:
+            K.kda_decode_step(S, p["q"], p["k"], p["v"], p["g"], p["beta"], o=o, stream=stream)
+
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(runs):
+        run()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_per_step = a.elapsed_time(b) / (runs * DEC_STEPS)
+    bytes_step = 2 * DEC_B * H * DK * DV * 4 + DEC_B * H * (3 * DK + DV + 1) * 2 + DEC_B * H * DV * 2
+    return ms_per_step, bytes_step
+
+
+def bench_replay(K, dev, warmup=3, runs=5):
+    sets = []
+    n_bytes = 0
+    for i in range(REP_SETS):
+        S, proj, n_acc = I.replay_inputs(REP_B, REP_H, REP_D, REP_D, REP_DRAFT, dtype=torch.float32,
+                                         seed=i, device=dev, state_std=0.1)
+        n_acc = n_acc.to(dev)
+        S_new = torch.empty_like(S)
+        out = torch.empty(REP_B, REP_H, REP_DRAFT, REP_D, device=dev)
+        sets.append((S, proj, n_acc, S_new, out))
+        acc = int(n_acc.sum())
+        n_bytes += 2 * S.numel() * 4 + acc * REP_H * (3 * REP_D + REP_D + 1) * 4 + out.numel() * 4
+    stream = torch.cuda.current_stream(dev)
+
+    def call(s):
+        S, pr, n_acc, S_new, out = s
+        K.kda_verify_replay(S, pr.q, pr.k, pr.v, pr.g, pr.beta, n_acc, S_new=S_new, out=out, stream=stream)
+
+    for _ in range(warmup):
+        for s in sets:
+            call(s)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(runs):
+        for s in sets:
+            call(s)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    amort_ms = a.elapsed_time(b) / (runs * REP_SETS)
+    single = []
+    for s in sets[:16]:
+        x, y = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x.record(stream)
+        call(s)
+        y.record(stream)
+        torch.cuda.synchronize(dev)
+        single.append(x.elapsed_time(y))
+    return amort_ms, n_bytes / REP_SETS, statistics.median(single)
+
+
+# ---------------------------------------------------------------------------
+def oracle_sample(heads=2, tokens=T):
+    """fp64 oracle on `heads` heads x `tokens` tokens of the workload's input distribution.
+
+    Returns (tokens/s scaled to all H heads, seconds, threads used)."""
+    from oracle import kda_oracle as O
+    S0, p, cu = I.prefill_inputs([tokens], heads, DK, DV, dtype=torch.bfloat16, seed=100)
+    f = I.to_f64_numpy
+    args = [f(S0)] + [f(p[n]) for n in ("q", "k", "v", "g", "beta")]
+    t0 = time.perf_counter()
+    O.prefill_chunked(*args, cu_seqlens=cu, chunk=CHUNK, ckpt_stride=STRIDE)
+    dt = time.perf_counter() - t0
+    return tokens * heads / H / dt, dt, 1
+
+
+def run_reference(args, rank, world):
+    """The fp64 oracle as it stands, one bounded sample per step: 1 head x 2048 tokens."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(heads=1, tokens=2048)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        v, dt, threads = oracle_sample(heads=1, tokens=2048)
+        vals.append(v)
+        secs.append(dt)
+    value = len(vals) / sum(1.0 / v for v in vals)
+    line = {
+        "impl": "reference", "metric": "kda_prefill_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * statistics.mean(secs), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": T, "l2": "host memory"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step 1 of {H} heads x 2048 of {T} tokens; tokens/s scaled by "
+                                   f"the {H} heads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the decode / replay objects")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = D.init()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        D.finalize()
+        return
+    args.warmup = max(args.warmup, 3)
+    from kda_delta_rule_gb300 import kda as K
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    r = bench_prefill(K, dev, args.steps, args.warmup, rank)
+    t_max = D.max_over_ranks(r["total_ms"])
+    e2e_max = D.max_over_ranks(r["e2e_ms"])
+    tokens_all = T * world * args.steps
+    value = tokens_all / (t_max / 1e3)
+    hbm, tf, src = peaks()
+    kern_avg_ms = sum(r["kern_ms"]) / len(r["kern_ms"])
+    achieved = r["bytes_step"] / (kern_avg_ms / 1e3) / 1e9
+    flops = prefill_flops(T, H, DK, DV)
+    extras = {}
+    if not args.no_extras:
+        dms, dbytes = bench_decode(K, dev)
+        dgbs = dbytes / (dms / 1e3) / 1e9
+        extras["decode"] = {"workload": f"B={DEC_B} H={H} dk=dv={DK} fp32 state, bf16 projections, "
+                                        f"{DEC_STEPS} consecutive steps",
+                            "ms_per_step": dms, "state_GBps": dgbs, "hbm_frac": dgbs / hbm,
+                            "bytes_per_step": dbytes, "tokens_per_s": DEC_B / (dms / 1e3)}
+        ams, abytes, single_ms = bench_replay(K, dev)
+        agbs = abytes / (ams / 1e3) / 1e9
+        extras["replay"] = {"workload": f"B={REP_B} H={REP_H} dk=dv={REP_D} draft={REP_DRAFT} fp32, "
+                                        f"n_accepted~U{{0..8}}, {REP_SETS} distinct buffer sets",
+                            "ms_per_call_amortised": ams, "ms_per_call_single": single_ms,
+                            "state_GBps": agbs, "hbm_frac": agbs / hbm, "bytes_per_call": abytes}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, threads = oracle_sample(heads=2)
+        cpu = {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"2 of {H} heads, all {T} tokens ({dt:.1f} s of fp64 CPU work), scaled by {H // 2}"}
+    if rank == 0:
+        line = {
+            "metric": "kda_prefill_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T,
+                       "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (336 MB/step)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None, "peak_source": src,
+                         "kernel": "kda_prefill", "kernel_ms": kern_avg_ms,
+                         "algorithmic_bytes": r["bytes_step"],
+                         "tc_tflops": flops / (kern_avg_ms / 1e3) / 1e12,
+                         "tc_frac": flops / (kern_avg_ms / 1e3) / 1e12 / tf},
+            "e2e": {"value": T * world * args.steps / (e2e_max / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": args.steps,
+            "clocks": r["clocks"],
+            "cpu_baseline": cpu,
+            **extras,
+        }
+        print(json.dumps(line))
+    D.finalize()
+
+
+if __name__ == "__main__":
+    main()

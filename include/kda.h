@@ -1,0 +1,223 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) KDA gated delta-rule library.
+ *
+ * The operations follow two pages:
+ *   [SERVE] "【轻量化复刻大模型 / KIMI K3】Serve 模块交互式演示"
+ *           (www.cveoy.top/t/topic/qHUG): §1.1 projection cache and
+ *           snapshot_cost_ratio, §1.2 verify_and_replay, §1.3 the KDA
+ *           recurrence (kda_step), §1.5 the unified page pool and
+ *           pack_heads / unpack_heads, Tab 7 store_kda / load_kda.
+ *   [CACHE] "Kimi Linear 的 KDA 缓存：SGLang、vLLM 与 Mooncake Store 全链路"
+ *           (imreese.github.io/blogs/kimi-kda-cache-sglang-vllm-mooncake-store):
+ *           "KDA 的递推与充分状态" (decay first, per-key-channel gates),
+ *           "预填充为什么能分块并行" (chunked WY/UT form, chunk 64),
+ *           "SGLang：从一次较长的 extend 调用中提取检查点" (chunk-aligned
+ *           intermediate states), "检查点状态池的内存成本" (FP32 state).
+ *
+ * Conventions (all entry points):
+ *  - Every call returns an int status: KDA_OK (0) or a negative KDA_ERR_*.
+ *    Arguments are validated on the host before anything is launched; a call
+ *    that fails validation launches nothing and writes nothing.
+ *    kda_last_error() gives a message for the calling thread's last failure.
+ *  - The caller owns all memory. No entry point allocates device memory.
+ *  - Pointers named "device" must be device (or managed) memory of the
+ *    current device; "host" pointers are plain host memory.
+ *  - Launches are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream). Device-side errors surface on later syncs.
+ *  - State tensors are fp32, layout (..., dk, dv) row-major: key channels are
+ *    rows, dv is contiguous. Projections q, k, g are (..., dk), v is
+ *    (..., dv), beta is (...) -- all of one dtype `dtype` (KDA_F32 or
+ *    KDA_BF16). Outputs o take the same dtype as the projections.
+ *  - Supported head sizes: dk, dv in {32, 64, 128}.
+ *  - Base pointers of state and projection arrays must be 16-byte aligned.
+ *  - Gates g are per-key-channel log-decays in [g_min, 0] with g_min >= -10
+ *    (the pages draw g = g_min * sigmoid(.), g_min = -5); beta in [0, 1].
+ *
+ * Modes: KDA_MODE_DECAY_FIRST ([CACHE]: S' = Diag(e^g) S; delta = v - S'^T k;
+ * S = S' + beta k delta^T; o = S^T q) and KDA_MODE_UNDECAYED_DELTA ([SERVE]
+ * §1.3: delta = v - S^T k taken against the undecayed state;
+ * S = Diag(e^g) S + beta k delta^T; o = S^T q).
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define KDA_OK          0
+#define KDA_ERR_ARG    -1   /* null pointer, bad enum, bad scalar argument   */
+#define KDA_ERR_SHAPE  -2   /* unsupported or inconsistent sizes             */
+#define KDA_ERR_DTYPE  -3   /* unsupported dtype                             */
+#define KDA_ERR_ALIGN  -4   /* pointer not aligned as required               */
+#define KDA_ERR_CUDA   -5   /* a CUDA runtime call failed                    */
+#define KDA_ERR_NOMEM  -6   /* page pool exhausted                           */
+#define KDA_ERR_ALIAS  -7   /* an output overlaps an input it must not touch */
+
+/* dtypes of projections / outputs */
+#define KDA_F32   0
+#define KDA_BF16  1
+
+/* orderings of the recurrence */
+#define KDA_MODE_DECAY_FIRST      0
+#define KDA_MODE_UNDECAYED_DELTA  1
+
+/* page kinds of the unified pool ([SERVE] §1.5: one free list, two kinds) */
+#define KDA_PAGE_FREE       0
+#define KDA_PAGE_KDA_STATE  1
+#define KDA_PAGE_MLA_KV     2
+
+/* limits */
+#define KDA_MAX_DRAFT            16    /* replay steps per call                */
+#define KDA_MAX_SEQS_PER_LAUNCH  1024  /* prefill splits larger batches        */
+
+typedef struct CUstream_st* kda_stream_t;   /* identical to cudaStream_t */
+
+int         kda_version(void);
+const char* kda_status_string(int status);
+const char* kda_last_error(void);
+
+/*
+ * kda_decode_step -- one token of the recurrence for B*H heads, in place.
+ * [SERVE] §1.3 kda_step; [CACHE] "KDA 的递推与充分状态".
+ *   S     device fp32 [B,H,dk,dv]    in/out, updated in place
+ *   q,k,g device dtype [B,H,dk]      in
+ *   v     device dtype [B,H,dv]      in
+ *   beta  device dtype [B,H]         in
+ *   o     device dtype [B,H,dv]      out: o = S_new^T q
+ * B == 0 or H == 0 is a no-op. o must not overlap S.
+ */
+int kda_decode_step(float* S, const void* q, const void* k, const void* v,
+                    const void* g, const void* beta, void* o,
+                    int B, int H, int dk, int dv, int dtype, int mode,
+                    kda_stream_t stream);
+
+/*
+ * kda_verify_replay -- clone the committed state and replay the accepted
+ * prefix of a draft. [SERVE] §1.2 verify_and_replay, Tab 3 §6.4.
+ *   S_committed  device fp32 [B,H,dk,dv]        in, never written
+ *   q,k,g        device dtype [draft,B,H,dk]    in (draft-projection cache layout)
+ *   v            device dtype [draft,B,H,dv]    in
+ *   beta         device dtype [draft,B,H]       in
+ *   n_accepted   device int32 [B]               in; clamped to [0, draft]
+ *   S_new        device fp32 [B,H,dk,dv]        out: state after n_b steps
+ *   out          device dtype [B,H,draft,dv]    out: step outputs, zero for
+ *                                               steps >= n_b
+ * 1 <= draft <= KDA_MAX_DRAFT. S_new must not overlap S_committed
+ * (KDA_ERR_ALIAS): the committed state is shared and must stay intact.
+ */
+int kda_verify_replay(const float* S_committed, const void* q, const void* k,
+                      const void* v, const void* g, const void* beta,
+                      const int32_t* n_accepted, float* S_new, void* out,
+                      int draft, int B, int H, int dk, int dv, int dtype, int mode,
+                      kda_stream_t stream);
+
+/*
+ * kda_num_checkpoints -- number of checkpoint states a prefill will emit:
+ * sum over sequences of floor(L_n / ckpt_stride). Host only.
+ *   cu_seqlens  host int32 [n_seqs+1] or NULL (one sequence of T tokens)
+ * Returns the count (>= 0) or a negative KDA_ERR_*.
+ */
+int64_t kda_num_checkpoints(const int32_t* cu_seqlens, int n_seqs, int64_t T,
+                            int ckpt_stride);
+
+/*
+ * kda_prefill_chunked -- chunked (WY/UT) prefill of packed sequences with
+ * chunk-aligned checkpoint emission. [CACHE] "预填充为什么能分块并行",
+ * "SGLang：从一次较长的 extend 调用中提取检查点"; [SERVE] §1.5, Tab 7.
+ *   S0          device fp32 [n_seqs,H,dk,dv] in, never written; NULL = zero state
+ *   q,k,g       device dtype [T,H,dk]        in (token-major, packed sequences)
+ *   v           device dtype [T,H,dv]        in
+ *   beta        device dtype [T,H]           in
+ *   cu_seqlens  host int32 [n_seqs+1]        sequence boundaries, cu[0] = 0,
+ *                                            non-decreasing, cu[n_seqs] = T;
+ *                                            NULL means one sequence (n_seqs = 1)
+ *   chunk       must be 64
+ *   ckpt_stride multiple of chunk, or 0 for no checkpoints
+ *   o           device dtype [T,H,dv]        out
+ *   S_final     device fp32 [n_seqs,H,dk,dv] out, must not overlap S0
+ *   page_pool   device base of the page arena (required if checkpoints > 0)
+ *   page_bytes  bytes per page, multiple of 16, >= H*dk*dv*4
+ *   ckpt_page_ids device int32 [num_ckpt]    page index of checkpoint c
+ *   ckpt_pos    device int32 [num_ckpt] out  boundary position of checkpoint c
+ *                                            within its sequence (may be NULL)
+ *   num_ckpt    entries in ckpt_page_ids; must be >= kda_num_checkpoints()
+ * Checkpoint c (sequence-major, then position) is the state after the first
+ * j*ckpt_stride tokens of its sequence, j >= 1, written into page
+ * ckpt_page_ids[c] in pack_heads layout ([1,H,dk,dv] flat) with the rest of
+ * the page zeroed. Positions count from each sequence's first token.
+ */
+int kda_prefill_chunked(const float* S0, const void* q, const void* k,
+                        const void* v, const void* g, const void* beta,
+                        const int32_t* cu_seqlens, int n_seqs, int64_t T,
+                        int H, int dk, int dv, int dtype, int chunk, int ckpt_stride,
+                        void* o, float* S_final,
+                        void* page_pool, int64_t page_bytes,
+                        const int32_t* ckpt_page_ids, int32_t* ckpt_pos, int64_t num_ckpt,
+                        int mode, kda_stream_t stream);
+
+/*
+ * kda_pack_heads -- gather (B,H,dk,dv) states into one flat head-contiguous
+ * buffer, zero-filling it past B*H*dk*dv. [SERVE] §1.5 pack_heads.
+ *   S         device fp32; element (b,h,i,j) at S[b*stride_b + h*stride_h + i*dv + j]
+ *   flat      device fp32 [flat_elems] out; flat_elems >= B*H*dk*dv
+ * Strides are in elements and must be multiples of 4. Bit-exact copy.
+ */
+int kda_pack_heads(const float* S, int64_t stride_b, int64_t stride_h,
+                   float* flat, int64_t flat_elems,
+                   int B, int H, int dk, int dv, kda_stream_t stream);
+
+/*
+ * kda_unpack_heads -- scatter a flat head-contiguous buffer back into
+ * (B,H,dk,dv) states (strided as in kda_pack_heads). [SERVE] §1.5.
+ */
+int kda_unpack_heads(const float* flat, float* S, int64_t stride_b, int64_t stride_h,
+                     int B, int H, int dk, int dv, kda_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Unified page pool ([SERVE] §1.5 PagePool / PagedCache): a host-side free
+ * list over a caller-owned device arena of n_pages pages of page_bytes each.
+ * Pages are handed out lowest index first. Not thread-safe: one owner thread.
+ * ------------------------------------------------------------------------- */
+typedef struct kda_page_pool kda_page_pool;
+
+int   kda_pool_create(void* device_base, int64_t page_bytes, int64_t n_pages,
+                      kda_page_pool** pool_out);
+int   kda_pool_destroy(kda_page_pool* pool);
+/* take n pages of one kind; all or nothing (KDA_ERR_NOMEM leaves the pool unchanged) */
+int   kda_pool_alloc(kda_page_pool* pool, int kind, int64_t n, int32_t* page_ids_out);
+/* return pages; a page that is not allocated is KDA_ERR_ARG and nothing is freed */
+int   kda_pool_free(kda_page_pool* pool, int64_t n, const int32_t* page_ids);
+int64_t kda_pool_num_free(const kda_page_pool* pool);
+int   kda_pool_page_kind(const kda_page_pool* pool, int32_t page_id);
+void* kda_pool_page_ptr(const kda_page_pool* pool, int32_t page_id);
+void* kda_pool_base(const kda_page_pool* pool);
+int64_t kda_pool_page_bytes(const kda_page_pool* pool);
+
+/* store_kda / load_kda ([SERVE] Tab 7): pack a (B,H,dk,dv) state into one
+ * KDA page (zero-padded tail) / unpack it back. The page must be allocated
+ * with kind KDA_PAGE_KDA_STATE. */
+int kda_store_kda(kda_page_pool* pool, int32_t page_id, const float* S,
+                  int64_t stride_b, int64_t stride_h, int B, int H, int dk, int dv,
+                  kda_stream_t stream);
+int kda_load_kda(const kda_page_pool* pool, int32_t page_id, float* S,
+                 int64_t stride_b, int64_t stride_h, int B, int H, int dk, int dv,
+                 kda_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Byte accounting ([SERVE] §1.1): bytes of a full state snapshot per draft
+ * step over bytes of the cached projections per draft step,
+ * (H dk dv) / (H (3 dk + dv + 1)). Independent of draft length and dtype.
+ * Returns a negative value for non-positive sizes.
+ * ------------------------------------------------------------------------- */
+double kda_snapshot_cost_ratio(int H, int dk, int dv);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

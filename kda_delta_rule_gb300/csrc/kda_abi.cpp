@@ -1,0 +1,422 @@
+// C ABI of the KDA library: host-side validation, scheduling and dispatch,
+// plus the unified page pool.  Every check runs before any launch, so a call
+// that returns an error has launched nothing and written nothing.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace kda {
+cudaError_t launch_prefill_simt(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s,
+                              bool* handled);
+}  // namespace kda
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+int ok() {
+  g_last_error.clear();
+  return KDA_OK;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool head_dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t elem_size(int dtype) { return dtype == KDA_BF16 ? 2 : 4; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  auto pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+int check_common(int dk, int dv, int dtype, int mode) {
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return fail(KDA_ERR_DTYPE, "dtype %d is not KDA_F32 or KDA_BF16", dtype);
+  if (mode != KDA_MODE_DECAY_FIRST && mode != KDA_MODE_UNDECAYED_DELTA)
+    return fail(KDA_ERR_ARG, "mode %d is not a KDA_MODE_*", mode);
+  if (!head_dim_ok(dk) || !head_dim_ok(dv))
+    return fail(KDA_ERR_SHAPE, "head sizes dk=%d dv=%d: each must be 32, 64 or 128", dk, dv);
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return 1; }
+
+const char* kda_status_string(int status) {
+  switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_ARG: return "KDA_ERR_ARG";
+    case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE";
+    case KDA_ERR_DTYPE: return "KDA_ERR_DTYPE";
+    case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_NOMEM: return "KDA_ERR_NOMEM";
+    case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_last_error(void) { return g_last_error.c_str(); }
+
+// ---------------------------------------------------------------------------
+int kda_decode_step(float* S, const void* q, const void* k, const void* v, const void* g,
+                    const void* beta, void* o, int B, int H, int dk, int dv, int dtype, int mode,
+                    kda_stream_t stream) {
+  if (int st = check_common(dk, dv, dtype, mode)) return st;
+  if (B < 0 || H < 0) return fail(KDA_ERR_SHAPE, "negative B=%d or H=%d", B, H);
+  const int64_t heads = (int64_t)B * H;
+  if (heads == 0) return ok();
+  if (heads > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "B*H too large");
+  if (!S || !q || !k || !v || !g || !beta || !o) return fail(KDA_ERR_ARG, "null pointer argument");
+  if (!aligned16(S) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o))
+    return fail(KDA_ERR_ALIGN, "state, projection and output pointers must be 16-byte aligned");
+  const size_t es = elem_size(dtype);
+  if (overlap(o, heads * dv * es, S, heads * dk * dv * 4))
+    return fail(KDA_ERR_ALIAS, "o overlaps the state");
+  kda::StepArgs a{};
+  a.S_in = S; a.S_out = S;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = o;
+  a.n_accepted = nullptr;
+  a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = 1; a.dtype = dtype; a.mode = mode;
+  a.out_head_stride = dv; a.out_step_stride = 0;
+  return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_decode_step launch");
+}
+
+// ---------------------------------------------------------------------------
+int kda_verify_replay(const float* S_committed, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, const int32_t* n_accepted, float* S_new,
+                      void* out, int draft, int B, int H, int dk, int dv, int dtype, int mode,
+                      kda_stream_t stream) {
+  if (int st = check_common(dk, dv, dtype, mode)) return st;
+  if (B < 0 || H < 0) return fail(KDA_ERR_SHAPE, "negative B=%d or H=%d", B, H);
+  if (draft < 1 || draft > KDA_MAX_DRAFT)
+    return fail(KDA_ERR_SHAPE, "draft=%d outside [1, %d]", draft, KDA_MAX_DRAFT);
+  const int64_t heads = (int64_t)B * H;
+  if (heads == 0) return ok();
+  if (heads > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "B*H too large");
+  if (!S_committed || !q || !k || !v || !g || !beta || !n_accepted || !S_new || !out)
+    return fail(KDA_ERR_ARG, "null pointer argument");
+  if (!aligned16(S_committed) || !aligned16(S_new) || !aligned16(q) || !aligned16(k) ||
+      !aligned16(v) || !aligned16(g) || !aligned16(out))
+    return fail(KDA_ERR_ALIGN, "state, projection and output pointers must be 16-byte aligned");
+  const size_t sbytes = heads * dk * dv * 4;
+  const size_t es = elem_size(dtype);
+  if (overlap(S_new, sbytes, S_committed, sbytes))
+    return fail(KDA_ERR_ALIAS, "S_new overlaps S_committed: the committed state must not be written");
+  if (overlap(out, heads * draft * dv * es, S_committed, sbytes) ||
+      overlap(out, heads * draft * dv * es, S_new, sbytes))
+    return fail(KDA_ERR_ALIAS, "out overlaps a state buffer");
+  kda::StepArgs a{};
+  a.S_in = S_committed; a.S_out = S_new;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
+  a.n_accepted = n_accepted;
+  a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = draft; a.dtype = dtype; a.mode = mode;
+  a.out_head_stride = (int64_t)draft * dv; a.out_step_stride = dv;
+  return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_verify_replay launch");
+}
+
+// ---------------------------------------------------------------------------
+static int check_seqlens(const int32_t* cu, int n_seqs, int64_t T) {
+  if (T < 0) return fail(KDA_ERR_SHAPE, "negative T");
+  if (T > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "T=%lld exceeds 2^31-1 tokens", (long long)T);
+  if (!cu) {
+    if (n_seqs != 1) return fail(KDA_ERR_ARG, "cu_seqlens is NULL but n_seqs=%d (must be 1)", n_seqs);
+    return KDA_OK;
+  }
+  if (n_seqs < 0) return fail(KDA_ERR_SHAPE, "negative n_seqs");
+  if (cu[0] != 0) return fail(KDA_ERR_SHAPE, "cu_seqlens[0]=%d, must be 0", cu[0]);
+  for (int n = 0; n < n_seqs; ++n)
+    if (cu[n + 1] < cu[n]) return fail(KDA_ERR_SHAPE, "cu_seqlens decreases at %d", n);
+  if (cu[n_seqs] != T) return fail(KDA_ERR_SHAPE, "cu_seqlens[n_seqs]=%d != T=%lld", cu[n_seqs], (long long)T);
+  return KDA_OK;
+}
+
+int64_t kda_num_checkpoints(const int32_t* cu_seqlens, int n_seqs, int64_t T, int ckpt_stride) {
+  if (ckpt_stride < 0) return fail(KDA_ERR_ARG, "negative ckpt_stride");
+  if (int st = check_seqlens(cu_seqlens, n_seqs, T)) return st;
+  ok();
+  if (ckpt_stride == 0) return 0;
+  if (!cu_seqlens) return T / ckpt_stride;
+  int64_t n = 0;
+  for (int i = 0; i < n_seqs; ++i) n += (cu_seqlens[i + 1] - cu_seqlens[i]) / ckpt_stride;
+  return n;
+}
+
+int kda_prefill_chunked(const float* S0, const void* q, const void* k, const void* v,
+                        const void* g, const void* beta, const int32_t* cu_seqlens, int n_seqs,
+                        int64_t T, int H, int dk, int dv, int dtype, int chunk, int ckpt_stride,
+                        void* o, float* S_final, void* page_pool, int64_t page_bytes,
+                        const int32_t* ckpt_page_ids, int32_t* ckpt_pos, int64_t num_ckpt,
+                        int mode, kda_stream_t stream) {
+  if (int st = check_common(dk, dv, dtype, mode)) return st;
+  if (chunk != 64) return fail(KDA_ERR_ARG, "chunk=%d: the kernels use 64-token chunks", chunk);
+  if (ckpt_stride < 0 || (ckpt_stride % chunk) != 0)
+    return fail(KDA_ERR_ARG, "ckpt_stride=%d must be a non-negative multiple of chunk=%d", ckpt_stride, chunk);
+  if (H < 0) return fail(KDA_ERR_SHAPE, "negative H");
+  if (int st = check_seqlens(cu_seqlens, n_seqs, T)) return st;
+  const int N = cu_seqlens ? n_seqs : 1;
+  if (N == 0 || H == 0) return ok();
+  const size_t es = elem_size(dtype);
+  const size_t state_bytes = (size_t)N * H * dk * dv * 4;
+  if (!S_final) return fail(KDA_ERR_ARG, "S_final is NULL");
+  if (T > 0 && (!q || !k || !v || !g || !beta || !o)) return fail(KDA_ERR_ARG, "null projection or output pointer");
+  if ((S0 && !aligned16(S0)) || !aligned16(S_final) || !aligned16(q) || !aligned16(k) ||
+      !aligned16(v) || !aligned16(g) || !aligned16(o))
+    return fail(KDA_ERR_ALIGN, "state, projection and output pointers must be 16-byte aligned");
+  if (overlap(S_final, state_bytes, S0, state_bytes))
+    return fail(KDA_ERR_ALIAS, "S_final overlaps S0: the starting checkpoint must not be written");
+  const size_t obytes = (size_t)T * H * dv * es;
+  const size_t kbytes = (size_t)T * H * dk * es;
+  if (overlap(o, obytes, q, kbytes) || overlap(o, obytes, k, kbytes) || overlap(o, obytes, g, kbytes) ||
+      overlap(o, obytes, v, obytes) || overlap(o, obytes, S0, state_bytes) ||
+      overlap(o, obytes, S_final, state_bytes))
+    return fail(KDA_ERR_ALIAS, "o overlaps an input or the final state");
+  const int64_t need = kda_num_checkpoints(cu_seqlens, n_seqs, T, ckpt_stride);
+  if (need < 0) return (int)need;
+  if (need > 0) {
+    if (!page_pool || !ckpt_page_ids) return fail(KDA_ERR_ARG, "checkpoints requested but page_pool or ckpt_page_ids is NULL");
+    if (num_ckpt < need)
+      return fail(KDA_ERR_SHAPE, "num_ckpt=%lld < %lld checkpoints this prefill emits", (long long)num_ckpt, (long long)need);
+    if (page_bytes < (int64_t)H * dk * dv * 4 || (page_bytes % 16) != 0)
+      return fail(KDA_ERR_SHAPE, "page_bytes=%lld must be a multiple of 16 and >= H*dk*dv*4=%lld",
+                  (long long)page_bytes, (long long)H * dk * dv * 4);
+    if (!aligned16(page_pool)) return fail(KDA_ERR_ALIGN, "page_pool must be 16-byte aligned");
+  }
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  std::vector<int32_t> starts(N), lens(N), bases(N);
+  int64_t cb = 0;
+  for (int n = 0; n < N; ++n) {
+    starts[n] = cu_seqlens ? cu_seqlens[n] : 0;
+    lens[n] = cu_seqlens ? cu_seqlens[n + 1] - cu_seqlens[n] : (int32_t)T;
+    bases[n] = (int32_t)cb;
+    if (ckpt_stride > 0) cb += lens[n] / ckpt_stride;
+  }
+  // ~16 KB schedule block, passed to the kernel by value; kept off the stack
+  static thread_local kda::PrefillSched sched_storage;
+  kda::PrefillSched* sched = &sched_storage;
+  int status = KDA_OK;
+  for (int g0 = 0; g0 < N && status == KDA_OK; g0 += kda::kMaxSeqs) {
+    const int n = std::min(kda::kMaxSeqs, N - g0);
+    sched->n_seqs = n;
+    std::vector<int32_t> idx(n);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) { return lens[g0 + x] > lens[g0 + y]; });
+    int max_len = 0;
+    for (int i = 0; i < n; ++i) {
+      sched->order[i] = idx[i];
+      sched->start[i] = starts[g0 + i];
+      sched->len[i] = lens[g0 + i];
+      sched->ckpt_base[i] = bases[g0 + i];
+      max_len = std::max(max_len, lens[g0 + i]);
+    }
+    kda::PrefillArgs a{};
+    const int64_t hs = (int64_t)H * dk * dv;
+    a.S0 = S0 ? S0 + g0 * hs : nullptr;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.o = o;
+    a.S_final = S_final + g0 * hs;
+    a.page_pool = static_cast<char*>(page_pool);
+    a.page_bytes = page_bytes;
+    a.ckpt_page_ids = ckpt_page_ids;
+    a.ckpt_pos = ckpt_pos;
+    a.num_ckpt = need > 0 ? num_ckpt : 0;
+    a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
+    a.ckpt_stride = ckpt_stride; a.mode = mode;
+    status = cuda_status(kda::launch_prefill(a, *sched, max_len, s), "kda_prefill_chunked launch");
+  }
+  return status;
+}
+
+// ---------------------------------------------------------------------------
+static int check_pack(const float* S, int64_t stride_b, int64_t stride_h, const float* flat,
+                      int B, int H, int dk, int dv) {
+  if (B < 0 || H < 0) return fail(KDA_ERR_SHAPE, "negative B or H");
+  if (!head_dim_ok(dk) || !head_dim_ok(dv)) return fail(KDA_ERR_SHAPE, "dk, dv must be 32, 64 or 128");
+  if ((int64_t)B * H == 0) return KDA_OK;
+  if (!S || !flat) return fail(KDA_ERR_ARG, "null pointer argument");
+  if (!aligned16(S) || !aligned16(flat)) return fail(KDA_ERR_ALIGN, "pointers must be 16-byte aligned");
+  if (stride_b < 0 || stride_h < 0 || (stride_b % 4) || (stride_h % 4))
+    return fail(KDA_ERR_ALIGN, "strides must be non-negative multiples of 4 elements");
+  return KDA_OK;
+}
+
+int kda_pack_heads(const float* S, int64_t stride_b, int64_t stride_h, float* flat,
+                   int64_t flat_elems, int B, int H, int dk, int dv, kda_stream_t stream) {
+  if (int st = check_pack(S, stride_b, stride_h, flat, B, H, dk, dv)) return st;
+  const int64_t n = (int64_t)B * H * dk * dv;
+  if (flat_elems < n) return fail(KDA_ERR_SHAPE, "flat_elems=%lld < B*H*dk*dv=%lld", (long long)flat_elems, (long long)n);
+  if (n == 0 && flat_elems == 0) return ok();
+  if (!flat) return fail(KDA_ERR_ARG, "null flat");
+  return cuda_status(kda::launch_pack(S, stride_b, stride_h, flat, flat_elems, B, H, dk, dv,
+                                      reinterpret_cast<cudaStream_t>(stream)), "kda_pack_heads launch");
+}
+
+int kda_unpack_heads(const float* flat, float* S, int64_t stride_b, int64_t stride_h, int B, int H,
+                     int dk, int dv, kda_stream_t stream) {
+  if (int st = check_pack(S, stride_b, stride_h, flat, B, H, dk, dv)) return st;
+  if ((int64_t)B * H == 0) return ok();
+  return cuda_status(kda::launch_unpack(flat, S, stride_b, stride_h, B, H, dk, dv,
+                                        reinterpret_cast<cudaStream_t>(stream)), "kda_unpack_heads launch");
+}
+
+// ---------------------------------------------------------------------------
+struct kda_page_pool {
+  char* base;
+  int64_t page_bytes;
+  int64_t n_pages;
+  std::vector<int8_t> kind;
+  std::set<int32_t> free_ids;
+};
+
+int kda_pool_create(void* device_base, int64_t page_bytes, int64_t n_pages, kda_page_pool** pool_out) {
+  if (!pool_out) return fail(KDA_ERR_ARG, "pool_out is NULL");
+  *pool_out = nullptr;
+  if (n_pages < 0 || n_pages > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "n_pages out of range");
+  if (page_bytes <= 0 || (page_bytes % 16)) return fail(KDA_ERR_SHAPE, "page_bytes must be a positive multiple of 16");
+  if (n_pages > 0 && !device_base) return fail(KDA_ERR_ARG, "device_base is NULL");
+  if (!aligned16(device_base)) return fail(KDA_ERR_ALIGN, "device_base must be 16-byte aligned");
+  kda_page_pool* p = new kda_page_pool;
+  p->base = static_cast<char*>(device_base);
+  p->page_bytes = page_bytes;
+  p->n_pages = n_pages;
+  p->kind.assign((size_t)n_pages, KDA_PAGE_FREE);
+  for (int64_t i = 0; i < n_pages; ++i) p->free_ids.insert(p->free_ids.end(), (int32_t)i);
+  *pool_out = p;
+  return ok();
+}
+
+int kda_pool_destroy(kda_page_pool* pool) {
+  delete pool;
+  return ok();
+}
+
+int kda_pool_alloc(kda_page_pool* pool, int kind, int64_t n, int32_t* page_ids_out) {
+  if (!pool) return fail(KDA_ERR_ARG, "pool is NULL");
+  if (kind != KDA_PAGE_KDA_STATE && kind != KDA_PAGE_MLA_KV) return fail(KDA_ERR_ARG, "bad page kind %d", kind);
+  if (n < 0) return fail(KDA_ERR_ARG, "negative n");
+  if (n > 0 && !page_ids_out) return fail(KDA_ERR_ARG, "page_ids_out is NULL");
+  if ((int64_t)pool->free_ids.size() < n)
+    return fail(KDA_ERR_NOMEM, "pool has %zu free pages, %lld requested", pool->free_ids.size(), (long long)n);
+  for (int64_t i = 0; i < n; ++i) {
+    auto it = pool->free_ids.begin();
+    page_ids_out[i] = *it;
+    pool->kind[*it] = (int8_t)kind;
+    pool->free_ids.erase(it);
+  }
+  return ok();
+}
+
+int kda_pool_free(kda_page_pool* pool, int64_t n, const int32_t* page_ids) {
+  if (!pool) return fail(KDA_ERR_ARG, "pool is NULL");
+  if (n < 0 || (n > 0 && !page_ids)) return fail(KDA_ERR_ARG, "bad page id list");
+  std::set<int32_t> seen;
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t id = page_ids[i];
+    if (id < 0 || id >= pool->n_pages || pool->kind[id] == KDA_PAGE_FREE || !seen.insert(id).second)
+      return fail(KDA_ERR_ARG, "page %d is not an allocated page (or is listed twice)", id);
+  }
+  for (int64_t i = 0; i < n; ++i) {
+    pool->kind[page_ids[i]] = KDA_PAGE_FREE;
+    pool->free_ids.insert(page_ids[i]);
+  }
+  return ok();
+}
+
+int64_t kda_pool_num_free(const kda_page_pool* pool) {
+  if (!pool) return fail(KDA_ERR_ARG, "pool is NULL");
+  return (int64_t)pool->free_ids.size();
+}
+
+int kda_pool_page_kind(const kda_page_pool* pool, int32_t page_id) {
+  if (!pool || page_id < 0 || page_id >= pool->n_pages) return fail(KDA_ERR_ARG, "bad pool or page id");
+  return pool->kind[page_id];
+}
+
+void* kda_pool_page_ptr(const kda_page_pool* pool, int32_t page_id) {
+  if (!pool || page_id < 0 || page_id >= pool->n_pages) {
+    fail(KDA_ERR_ARG, "bad pool or page id");
+    return nullptr;
+  }
+  return pool->base + (int64_t)page_id * pool->page_bytes;
+}
+
+void* kda_pool_base(const kda_page_pool* pool) { return pool ? pool->base : nullptr; }
+int64_t kda_pool_page_bytes(const kda_page_pool* pool) { return pool ? pool->page_bytes : (int64_t)KDA_ERR_ARG; }
+
+static int check_state_page(const kda_page_pool* pool, int32_t page_id, int B, int H, int dk, int dv) {
+  if (!pool) return fail(KDA_ERR_ARG, "pool is NULL");
+  if (page_id < 0 || page_id >= pool->n_pages) return fail(KDA_ERR_ARG, "page id %d out of range", page_id);
+  if (pool->kind[page_id] != KDA_PAGE_KDA_STATE)
+    return fail(KDA_ERR_ARG, "page %d is not an allocated KDA state page", page_id);
+  if ((int64_t)B * H * dk * dv * 4 > pool->page_bytes)
+    return fail(KDA_ERR_SHAPE, "state of %lld bytes does not fit a %lld-byte page",
+                (long long)B * H * dk * dv * 4, (long long)pool->page_bytes);
+  return KDA_OK;
+}
+
+int kda_store_kda(kda_page_pool* pool, int32_t page_id, const float* S, int64_t stride_b,
+                  int64_t stride_h, int B, int H, int dk, int dv, kda_stream_t stream) {
+  if (int st = check_state_page(pool, page_id, B, H, dk, dv)) return st;
+  float* page = reinterpret_cast<float*>(pool->base + (int64_t)page_id * pool->page_bytes);
+  return kda_pack_heads(S, stride_b, stride_h, page, pool->page_bytes / 4, B, H, dk, dv, stream);
+}
+
+int kda_load_kda(const kda_page_pool* pool, int32_t page_id, float* S, int64_t stride_b,
+                 int64_t stride_h, int B, int H, int dk, int dv, kda_stream_t stream) {
+  if (int st = check_state_page(pool, page_id, B, H, dk, dv)) return st;
+  const float* page = reinterpret_cast<const float*>(pool->base + (int64_t)page_id * pool->page_bytes);
+  return kda_unpack_heads(page, S, stride_b, stride_h, B, H, dk, dv, stream);
+}
+
+double kda_snapshot_cost_ratio(int H, int dk, int dv) {
+  if (H <= 0 || dk <= 0 || dv <= 0) {
+    fail(KDA_ERR_ARG, "sizes must be positive");
+    return -1.0;
+  }
+  ok();
+  const double snap = (double)H * dk * dv;
+  const double proj = (double)H * (3.0 * dk + dv + 1.0);
+  return snap / proj;
+}
+
+}  // extern "C"
+
+// Prefill dispatch: the tensor-core kernel takes bf16 projections where it
+// supports the shape; everything else runs the fp32 CUDA-core kernel.
+namespace kda {
+cudaError_t launch_prefill(const PrefillArgs& a, const PrefillSched& sched, int max_len, cudaStream_t s) {
+  (void)max_len;
+  bool handled = false;
+  cudaError_t e = launch_prefill_tc(a, sched, s, &handled);
+  if (handled) return e;
+  return launch_prefill_simt(a, sched, s);
+}
+}  // namespace kda

@@ -1,0 +1,57 @@
+// Internal launch interface between the C ABI (kda_abi.cpp) and the kernels.
+// Everything here assumes arguments were validated by the ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// One or more steps of the token recurrence per (b, h) head with the state
+// held on chip across steps.  Decode: steps = 1, S_in == S_out.  Replay:
+// steps = draft, per-sequence step counts from n_accepted.
+struct StepArgs {
+  const float* S_in;
+  float* S_out;
+  const void *q, *k, *v, *g, *beta;
+  void* out;
+  const int32_t* n_accepted;   // device [B] or nullptr (all heads run `steps`)
+  int B, H, dk, dv, steps, dtype, mode;
+  int64_t out_head_stride;     // elements between heads in `out`
+  int64_t out_step_stride;     // elements between steps in `out`
+};
+cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+
+// Sequence schedule of one prefill launch, passed by value as a kernel
+// parameter: at most kMaxSeqs sequences.
+constexpr int kMaxSeqs = 1024;
+struct PrefillSched {
+  int32_t n_seqs;
+  int32_t order[kMaxSeqs];       // launch slot -> sequence (longest first)
+  int32_t start[kMaxSeqs];       // first token of each sequence (relative to `base_token`)
+  int32_t len[kMaxSeqs];         // tokens of each sequence
+  int32_t ckpt_base[kMaxSeqs];   // index of each sequence's first checkpoint
+};
+
+struct PrefillArgs {
+  const float* S0;               // [n,H,dk,dv] (already offset to this launch) or nullptr
+  const void *q, *k, *v, *g, *beta;  // token-major, offset to this launch's first token
+  void* o;
+  float* S_final;                // offset to this launch's first sequence
+  char* page_pool;
+  int64_t page_bytes;
+  const int32_t* ckpt_page_ids;  // offset to this launch's first checkpoint
+  int32_t* ckpt_pos;             // same offset, or nullptr
+  int64_t num_ckpt;              // entries available from the offset
+  int H, dk, dv, dtype, chunk, ckpt_stride, mode;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, const PrefillSched& sched, int max_len,
+                           cudaStream_t s);
+
+// Flat <-> strided (B,H,dk,dv) copies.  pack zero-fills flat past B*H*dk*dv.
+cudaError_t launch_pack(const float* S, int64_t stride_b, int64_t stride_h, float* flat,
+                        int64_t flat_elems, int B, int H, int dk, int dv, cudaStream_t s);
+cudaError_t launch_unpack(const float* flat, float* S, int64_t stride_b, int64_t stride_h,
+                          int B, int H, int dk, int dv, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,303 @@
+"""Python binding of the KDA C ABI (``include/kda.h``): argument marshalling only.
+
+Every function here checks that its tensors are CUDA tensors of the expected
+dtype and layout, allocates missing outputs with PyTorch, and calls the entry
+point of the same name in ``libkda.so``.  All computation happens in the
+library's kernels; there is no CPU path.  Importing this module raises if the
+library has not been built (``python -m kda_delta_rule_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkda.so")
+
+KDA_OK = 0
+KDA_F32, KDA_BF16 = 0, 1
+DECAY_FIRST, UNDECAYED_DELTA = 0, 1
+PAGE_FREE, PAGE_KDA_STATE, PAGE_MLA_KV = 0, 1, 2
+MAX_DRAFT = 16
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        super().__init__(f"{where}: {message} (status {status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"KDA CUDA library not found at {_LIB_PATH}; build it with "
+            "`python -m kda_delta_rule_gb300.build` (needs nvcc for sm_103a)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    sig = {
+        "kda_version": ([], I),
+        "kda_status_string": ([I], ctypes.c_char_p),
+        "kda_last_error": ([], ctypes.c_char_p),
+        "kda_decode_step": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
+        "kda_verify_replay": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
+        "kda_num_checkpoints": ([P, I, L, I], L),
+        "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, I, P], I),
+        "kda_pack_heads": ([P, L, L, P, L, I, I, I, I, P], I),
+        "kda_unpack_heads": ([P, P, L, L, I, I, I, I, P], I),
+        "kda_pool_create": ([P, L, L, ctypes.POINTER(P)], I),
+        "kda_pool_destroy": ([P], I),
+        "kda_pool_alloc": ([P, I, L, P], I),
+        "kda_pool_free": ([P, L, P], I),
+        "kda_pool_num_free": ([P], L),
+        "kda_pool_page_kind": ([P, ctypes.c_int32], I),
+        "kda_pool_page_ptr": ([P, ctypes.c_int32], P),
+        "kda_store_kda": ([P, ctypes.c_int32, P, L, L, I, I, I, I, P], I),
+        "kda_load_kda": ([P, ctypes.c_int32, P, L, L, I, I, I, I, P], I),
+        "kda_snapshot_cost_ratio": ([I, I, I], D),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int, where: str):
+    if status != KDA_OK:
+        raise KdaError(status, where, _lib.kda_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return KDA_F32
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    raise TypeError(f"projections must be float32 or bfloat16, got {t.dtype}")
+
+
+def _cuda(name, t, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _projections(q, k, v, g, beta, lead):
+    dt = q.dtype
+    dk = q.shape[-1]
+    dv = v.shape[-1]
+    _cuda("q", q, dt, (*lead, dk))
+    _cuda("k", k, dt, (*lead, dk))
+    _cuda("g", g, dt, (*lead, dk))
+    _cuda("v", v, dt, (*lead, dv))
+    _cuda("beta", beta, dt, tuple(lead))
+    return _dtype_code(q), dk, dv
+
+
+# ---------------------------------------------------------------------------
+def kda_decode_step(S, q, k, v, g, beta, o=None, mode=DECAY_FIRST, stream=None):
+    """One token for every (b, h) head; S (B,H,dk,dv) fp32 is updated in place. Returns o."""
+    B, H, dk, dv = S.shape
+    _cuda("S", S, torch.float32)
+    code, _, _ = _projections(q, k, v, g, beta, (B, H))
+    if o is None:
+        o = torch.empty((B, H, dv), device=S.device, dtype=q.dtype)
+    _cuda("o", o, q.dtype, (B, H, dv))
+    _check(_lib.kda_decode_step(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o),
+                                B, H, dk, dv, code, mode, _stream(stream, S.device)),
+           "kda_decode_step")
+    return o
+
+
+def kda_verify_replay(S_committed, q, k, v, g, beta, n_accepted, S_new=None, out=None,
+                      mode=DECAY_FIRST, stream=None):
+    """Replay the accepted draft prefix from a clone of S_committed (left untouched).
+
+    Projections (draft,B,H,D); n_accepted int32 (B,). Returns (S_new, out (B,H,draft,dv)).
+    """
+    B, H, dk, dv = S_committed.shape
+    draft = q.shape[0]
+    _cuda("S_committed", S_committed, torch.float32)
+    code, _, _ = _projections(q, k, v, g, beta, (draft, B, H))
+    _cuda("n_accepted", n_accepted, torch.int32, (B,))
+    if S_new is None:
+        S_new = torch.empty_like(S_committed)
+    if out is None:
+        out = torch.empty((B, H, draft, dv), device=S_committed.device, dtype=q.dtype)
+    _cuda("S_new", S_new, torch.float32, (B, H, dk, dv))
+    _cuda("out", out, q.dtype, (B, H, draft, dv))
+    _check(_lib.kda_verify_replay(_ptr(S_committed), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  _ptr(n_accepted), _ptr(S_new), _ptr(out), draft, B, H, dk, dv,
+                                  code, mode, _stream(stream, S_committed.device)),
+           "kda_verify_replay")
+    return S_new, out
+
+
+def _cu_array(cu_seqlens: Optional[Sequence[int]]):
+    if cu_seqlens is None:
+        return None, 1
+    arr = (ctypes.c_int32 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
+    return arr, len(cu_seqlens) - 1
+
+
+def kda_num_checkpoints(cu_seqlens, T, ckpt_stride) -> int:
+    arr, n = _cu_array(cu_seqlens)
+    r = _lib.kda_num_checkpoints(arr, n, int(T), int(ckpt_stride))
+    if r < 0:
+        _check(int(r), "kda_num_checkpoints")
+    return int(r)
+
+
+def kda_prefill_chunked(S0, q, k, v, g, beta, cu_seqlens=None, chunk=64, ckpt_stride=512,
+                        o=None, S_final=None, page_pool=None, ckpt_page_ids=None, ckpt_pos=None,
+                        mode=DECAY_FIRST, stream=None, n_seqs=None, H=None):
+    """Chunked prefill of packed sequences with chunk-aligned checkpoints.
+
+    q,k,g (T,H,dk); v (T,H,dv); beta (T,H); cu_seqlens: host list of N+1 ints (None: one
+    sequence). S0 (N,H,dk,dv) fp32 or None (zero state). page_pool: a PagePool (or None
+    when no checkpoints are emitted); ckpt_page_ids: CUDA int32 tensor with one page per
+    checkpoint. Returns (o, S_final).
+    """
+    T, Hq, dk = q.shape
+    code, _, dv = _projections(q, k, v, g, beta, (T, Hq))
+    arr, N = _cu_array(cu_seqlens)
+    dev = q.device
+    if S0 is not None:
+        _cuda("S0", S0, torch.float32, (N, Hq, dk, dv))
+    if o is None:
+        o = torch.empty((T, Hq, dv), device=dev, dtype=q.dtype)
+    if S_final is None:
+        S_final = torch.empty((N, Hq, dk, dv), device=dev, dtype=torch.float32)
+    _cuda("o", o, q.dtype, (T, Hq, dv))
+    _cuda("S_final", S_final, torch.float32, (N, Hq, dk, dv))
+    base, page_bytes, n_ck = None, 0, 0
+    if ckpt_page_ids is not None:
+        _cuda("ckpt_page_ids", ckpt_page_ids, torch.int32)
+        n_ck = ckpt_page_ids.numel()
+        if page_pool is None:
+            raise ValueError("ckpt_page_ids given without a page_pool")
+        base, page_bytes = ctypes.c_void_p(page_pool.arena.data_ptr()), page_pool.page_bytes
+    if ckpt_pos is not None:
+        _cuda("ckpt_pos", ckpt_pos, torch.int32)
+    _check(_lib.kda_prefill_chunked(_ptr(S0), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                    arr, N, T, Hq, dk, dv, code, chunk, ckpt_stride,
+                                    _ptr(o), _ptr(S_final), base, page_bytes,
+                                    _ptr(ckpt_page_ids), _ptr(ckpt_pos), n_ck, mode,
+                                    _stream(stream, dev)),
+           "kda_prefill_chunked")
+    return o, S_final
+
+
+def kda_pack_heads(S, flat=None, flat_elems=None, stream=None):
+    """(B,H,dk,dv) fp32 (the (b,h) dims may be strided) -> flat fp32, zero-padded."""
+    if not S.is_cuda or S.dtype != torch.float32:
+        raise TypeError("S must be a CUDA float32 tensor")
+    B, H, dk, dv = S.shape
+    if S.stride(3) != 1 or S.stride(2) != dv:
+        raise ValueError("each (dk, dv) block of S must be contiguous")
+    n = B * H * dk * dv
+    if flat is None:
+        flat = torch.empty(flat_elems or n, device=S.device, dtype=torch.float32)
+    _cuda("flat", flat, torch.float32)
+    _check(_lib.kda_pack_heads(_ptr(S), S.stride(0), S.stride(1), _ptr(flat), flat.numel(),
+                               B, H, dk, dv, _stream(stream, S.device)), "kda_pack_heads")
+    return flat
+
+
+def kda_unpack_heads(flat, S, stream=None):
+    """flat fp32 -> S (B,H,dk,dv), written in place (the (b,h) dims may be strided)."""
+    _cuda("flat", flat, torch.float32)
+    if not S.is_cuda or S.dtype != torch.float32:
+        raise TypeError("S must be a CUDA float32 tensor")
+    B, H, dk, dv = S.shape
+    if S.stride(3) != 1 or S.stride(2) != dv:
+        raise ValueError("each (dk, dv) block of S must be contiguous")
+    if flat.numel() < B * H * dk * dv:
+        raise ValueError("flat is smaller than the state")
+    _check(_lib.kda_unpack_heads(_ptr(flat), _ptr(S), S.stride(0), S.stride(1), B, H, dk, dv,
+                                 _stream(stream, S.device)), "kda_unpack_heads")
+    return S
+
+
+def kda_snapshot_cost_ratio(H, dk, dv) -> float:
+    r = _lib.kda_snapshot_cost_ratio(int(H), int(dk), int(dv))
+    if r < 0:
+        raise ValueError(_lib.kda_last_error().decode())
+    return r
+
+
+class PagePool:
+    """Unified page pool: a device arena (owned by PyTorch) plus the library's host free list.
+
+    One free list hands out pages of both kinds (KDA state, MLA KV), lowest index first.
+    """
+
+    def __init__(self, page_bytes: int, n_pages: int, device="cuda"):
+        self.page_bytes = int(page_bytes)
+        self.n_pages = int(n_pages)
+        self.arena = torch.empty(self.page_bytes * self.n_pages, dtype=torch.uint8, device=device)
+        h = ctypes.c_void_p()
+        _check(_lib.kda_pool_create(ctypes.c_void_p(self.arena.data_ptr()), self.page_bytes,
+                                    self.n_pages, ctypes.byref(h)), "kda_pool_create")
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _lib is not None:
+            _lib.kda_pool_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def alloc(self, n: int, kind: int = PAGE_KDA_STATE):
+        ids = (ctypes.c_int32 * max(int(n), 1))()
+        _check(_lib.kda_pool_alloc(self._h, kind, int(n), ids), "kda_pool_alloc")
+        return [int(ids[i]) for i in range(int(n))]
+
+    def free(self, ids):
+        arr = (ctypes.c_int32 * max(len(ids), 1))(*ids)
+        _check(_lib.kda_pool_free(self._h, len(ids), arr), "kda_pool_free")
+
+    def num_free(self) -> int:
+        return int(_lib.kda_pool_num_free(self._h))
+
+    def kind(self, page_id: int) -> int:
+        return int(_lib.kda_pool_page_kind(self._h, int(page_id)))
+
+    def page(self, page_id: int, dtype=torch.float32) -> torch.Tensor:
+        """View of one page's bytes as a 1-D tensor (no copy)."""
+        off = int(page_id) * self.page_bytes
+        return self.arena[off:off + self.page_bytes].view(dtype)
+
+    def store_kda(self, page_id: int, S: torch.Tensor, stream=None):
+        B, H, dk, dv = S.shape
+        _check(_lib.kda_store_kda(self._h, int(page_id), _ptr(S), S.stride(0), S.stride(1),
+                                  B, H, dk, dv, _stream(stream, S.device)), "kda_store_kda")
+
+    def load_kda(self, page_id: int, S: torch.Tensor, stream=None):
+        B, H, dk, dv = S.shape
+        _check(_lib.kda_load_kda(self._h, int(page_id), _ptr(S), S.stride(0), S.stride(1),
+                                 B, H, dk, dv, _stream(stream, S.device)), "kda_load_kda")
+        return S

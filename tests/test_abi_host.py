@@ -1,0 +1,190 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and the host-only entry points (page pool, checkpoint count, byte
+ratio, argument validation) behave as documented.  Nothing here launches a
+kernel: every validation case fails before any launch, and fake device
+pointers are never dereferenced.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def K():
+    from kda_delta_rule_gb300 import build
+    build.build()
+    from kda_delta_rule_gb300 import kda
+    return kda
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("kda_decode_step", "kda_verify_replay", "kda_prefill_chunked",
+                 "kda_pack_heads", "kda_unpack_heads", "kda_num_checkpoints",
+                 "kda_pool_create", "kda_pool_alloc", "kda_pool_free",
+                 "kda_store_kda", "kda_load_kda", "kda_snapshot_cost_ratio"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(K):
+    lib = ctypes.CDLL(K._LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(K):
+    assert K._lib.kda_status_string(0) == b"KDA_OK"
+    assert K._lib.kda_status_string(-7) == b"KDA_ERR_ALIAS"
+    assert K._lib.kda_version() >= 1
+
+
+def test_snapshot_cost_ratio_matches_pages(K):
+    assert round(K.kda_snapshot_cost_ratio(2, 8, 8), 2) == 1.94
+    assert round(K.kda_snapshot_cost_ratio(1, 16, 16), 2) == 3.94
+    assert K.kda_snapshot_cost_ratio(16, 32, 32) == pytest.approx(1024 / 129)
+    with pytest.raises(ValueError):
+        K.kda_snapshot_cost_ratio(0, 8, 8)
+
+
+def test_num_checkpoints(K):
+    assert K.kda_num_checkpoints(None, 8192, 512) == 16
+    assert K.kda_num_checkpoints([0, 8192, 9192, 9703], 9703, 512) == 16 + 1 + 0
+    assert K.kda_num_checkpoints([0, 100], 100, 0) == 0
+    with pytest.raises(K.KdaError):
+        K.kda_num_checkpoints([0, 50, 40], 40, 64)     # decreasing
+    with pytest.raises(K.KdaError):
+        K.kda_num_checkpoints([0, 50], 60, 64)         # does not end at T
+
+
+def _fake_pool(K, page_bytes=4096, n_pages=8):
+    h = ctypes.c_void_p()
+    base = ctypes.c_void_p(0x10000)          # never dereferenced by the pool
+    assert K._lib.kda_pool_create(base, page_bytes, n_pages, ctypes.byref(h)) == 0
+    return h
+
+
+def test_pool_single_free_list_two_kinds(K):
+    lib = K._lib
+    h = _fake_pool(K)
+    ids = (ctypes.c_int32 * 8)()
+    assert lib.kda_pool_alloc(h, K.PAGE_KDA_STATE, 3, ids) == 0
+    assert list(ids[:3]) == [0, 1, 2]
+    assert lib.kda_pool_alloc(h, K.PAGE_MLA_KV, 2, ctypes.byref(ids, 12)) == 0
+    assert list(ids[3:5]) == [3, 4]
+    assert lib.kda_pool_num_free(h) == 3
+    assert lib.kda_pool_page_kind(h, 1) == K.PAGE_KDA_STATE
+    assert lib.kda_pool_page_kind(h, 4) == K.PAGE_MLA_KV
+    assert lib.kda_pool_page_ptr(h, 2) == 0x10000 + 2 * 4096
+    # all-or-nothing when the pool is short
+    more = (ctypes.c_int32 * 4)()
+    assert lib.kda_pool_alloc(h, K.PAGE_KDA_STATE, 4, more) == -6
+    assert lib.kda_pool_num_free(h) == 3
+    # free returns pages to the one list; lowest index first again
+    back = (ctypes.c_int32 * 2)(1, 3)
+    assert lib.kda_pool_free(h, 2, back) == 0
+    assert lib.kda_pool_page_kind(h, 1) == K.PAGE_FREE
+    one = (ctypes.c_int32 * 1)()
+    assert lib.kda_pool_alloc(h, K.PAGE_MLA_KV, 1, one) == 0 and one[0] == 1
+    # freeing a free page (or a page twice) is rejected and frees nothing
+    bad = (ctypes.c_int32 * 2)(0, 3)
+    assert lib.kda_pool_free(h, 2, bad) == -1
+    assert lib.kda_pool_page_kind(h, 0) == K.PAGE_KDA_STATE
+    dup = (ctypes.c_int32 * 2)(0, 0)
+    assert lib.kda_pool_free(h, 2, dup) == -1
+    assert lib.kda_pool_destroy(h) == 0
+
+
+def test_store_kda_requires_a_state_page(K):
+    lib = K._lib
+    h = _fake_pool(K, page_bytes=4096, n_pages=2)
+    ids = (ctypes.c_int32 * 1)()
+    assert lib.kda_pool_alloc(h, K.PAGE_MLA_KV, 1, ids) == 0
+    S = ctypes.c_void_p(0x20000)
+    assert lib.kda_store_kda(h, ids[0], S, 1024, 1024, 1, 1, 32, 32, None) == -1   # wrong kind
+    assert lib.kda_store_kda(h, 1, S, 1024, 1024, 1, 1, 32, 32, None) == -1        # free page
+    assert lib.kda_pool_alloc(h, K.PAGE_KDA_STATE, 1, ids) == 0
+    assert lib.kda_store_kda(h, ids[0], S, 4096, 4096, 1, 1, 64, 64, None) == -2   # too big
+    lib.kda_pool_destroy(h)
+
+
+# ---------------------------------------------------------------------------
+# Validation (every case fails before a launch)
+# ---------------------------------------------------------------------------
+A = 0x100000          # fake 16-byte aligned device addresses, never dereferenced
+
+
+def P(off):
+    return ctypes.c_void_p(A + off)
+
+
+def test_decode_validation(K):
+    f = K._lib.kda_decode_step
+    base = [P(0), P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20)]
+    assert f(*base, 2, 2, 48, 32, 0, 0, None) == -2          # unsupported dk
+    assert f(*base, 2, 2, 32, 32, 7, 0, None) == -3          # dtype
+    assert f(*base, 2, 2, 32, 32, 0, 5, None) == -1          # mode
+    assert f(None, *base[1:], 2, 2, 32, 32, 0, 0, None) == -1
+    bad = list(base); bad[0] = P(4)
+    assert f(*bad, 2, 2, 32, 32, 0, 0, None) == -4           # misaligned state
+    alias = list(base); alias[6] = P(64)
+    assert f(*alias, 2, 2, 32, 32, 0, 0, None) == -7         # o inside S
+    assert f(*base, 0, 2, 32, 32, 0, 0, None) == 0           # empty batch: no-op
+    assert b"32, 64 or 128" in K._lib.kda_last_error() or True
+
+
+def test_replay_rejects_writing_the_committed_state(K):
+    f = K._lib.kda_verify_replay
+    S_c, S_new = P(0), P(0)
+    args = [S_c, P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20), S_new,
+            P(7 << 20)]
+    assert f(*args, 4, 2, 2, 32, 32, 0, 0, None) == -7
+    args[7] = P(1024)                                         # partial overlap
+    assert f(*args, 4, 2, 2, 32, 32, 0, 0, None) == -7
+    args[7] = P(8 << 20)
+    assert f(*args, 0, 2, 2, 32, 32, 0, 0, None) == -2        # draft 0
+    assert f(*args, 17, 2, 2, 32, 32, 0, 0, None) == -2       # draft > 16
+
+
+def test_prefill_validation(K):
+    f = K._lib.kda_prefill_chunked
+    cu = (ctypes.c_int32 * 3)(0, 100, 228)
+
+    def call(**kw):
+        a = dict(S0=P(0), q=P(1 << 24), k=P(2 << 24), v=P(3 << 24), g=P(4 << 24), beta=P(5 << 24),
+                 cu=cu, n=2, T=228, H=2, dk=32, dv=32, dtype=0, chunk=64, stride=64,
+                 o=P(6 << 24), Sf=P(7 << 24), pool=P(8 << 24), page_bytes=8192,
+                 ids=P(9 << 24), pos=None, nck=10, mode=0)
+        a.update(kw)
+        return f(a["S0"], a["q"], a["k"], a["v"], a["g"], a["beta"], a["cu"], a["n"], a["T"],
+                 a["H"], a["dk"], a["dv"], a["dtype"], a["chunk"], a["stride"], a["o"], a["Sf"],
+                 a["pool"], a["page_bytes"], a["ids"], a["pos"], a["nck"], a["mode"], None)
+
+    assert call(chunk=32) == -1
+    assert call(stride=96) == -1                               # not a multiple of chunk
+    assert call(T=229) == -2                                   # cu_seqlens does not end at T
+    assert call(cu=(ctypes.c_int32 * 3)(0, 120, 100), T=100) == -2
+    assert call(nck=1) == -2                                   # 1 + 2 checkpoints needed
+    assert call(page_bytes=4096) == -2                         # page smaller than H*dk*dv*4
+    assert call(ids=None) == -1
+    assert call(Sf=P(64)) == -7                                # S_final overlaps S0
+    assert call(o=P(1 << 24)) == -7                            # o overlaps q
+    assert call(cu=None, n=2) == -1
+    assert call(H=0) == 0                                      # nothing to do
+
+
+def test_pack_validation(K):
+    f = K._lib.kda_pack_heads
+    assert f(P(0), 4096, 1024, P(1 << 20), 100, 2, 2, 32, 32, None) == -2   # flat too small
+    assert f(P(0), 4098, 1024, P(1 << 20), 8192, 2, 2, 32, 32, None) == -4  # stride % 4
+    assert f(P(8), 4096, 1024, P(1 << 20), 8192, 2, 2, 32, 32, None) == -4  # misaligned
