@@ -135,12 +135,14 @@ def bench_prefill(K, dev, steps, warmup, rank):
     pos = torch.empty(n_ck, dtype=torch.int32, device=dev)
     o = torch.empty(T, H, DV, dtype=torch.bfloat16, device=dev)
     S_fin = torch.empty(1, H, DK, DV, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(K.kda_prefill_workspace_bytes(cu, T, H, DK, DV, torch.bfloat16), 16),
+                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
         K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
                               ckpt_stride=STRIDE, page_pool=pool, ckpt_page_ids=ids, ckpt_pos=pos,
-                              o=o, S_final=S_fin, stream=stream)
+                              o=o, S_final=S_fin, stream=stream, workspace=ws)
 
     for _ in range(warmup):
         step()
@@ -181,7 +183,8 @@ def bench_prefill(K, dev, steps, warmup, rank):
         dev_S0.copy_(host_S0, non_blocking=True)
         K.kda_prefill_chunked(dev_S0, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"],
                               dev_in["beta"], cu_seqlens=cu, ckpt_stride=STRIDE, page_pool=pool,
-                              ckpt_page_ids=ids, ckpt_pos=pos, o=o, S_final=S_fin, stream=stream)
+                              ckpt_page_ids=ids, ckpt_pos=pos, o=o, S_final=S_fin, stream=stream,
+                              workspace=ws)
         host_o.copy_(o, non_blocking=True)
         host_S.copy_(S_fin, non_blocking=True)
         host_pages.copy_(pool.arena, non_blocking=True)

@@ -146,10 +146,18 @@ int64_t kda_num_checkpoints(const int32_t* cu_seqlens, int n_seqs, int64_t T,
  *   ckpt_pos    device int32 [num_ckpt] out  boundary position of checkpoint c
  *                                            within its sequence (may be NULL)
  *   num_ckpt    entries in ckpt_page_ids; must be >= kda_num_checkpoints()
+ *   workspace   device scratch for the tensor-core kernels, or NULL;
+ *   workspace_bytes  its size, >= kda_prefill_workspace_bytes() when used
  * Checkpoint c (sequence-major, then position) is the state after the first
  * j*ckpt_stride tokens of its sequence, j >= 1, written into page
  * ckpt_page_ids[c] in pack_heads layout ([1,H,dk,dv] flat) with the rest of
  * the page zeroed. Positions count from each sequence's first token.
+ * Page ids must index pages inside the arena (not checked: device memory).
+ * Kernels: bf16 projections with dk = 128 and dv in {64, 128} run on tcgen05
+ * tensor cores (bf16 operands, fp32 accumulation and state) when a workspace
+ * is given; every other case, and a NULL workspace, runs the fp32 CUDA-core
+ * kernel. The workspace is only touched during the call's kernels (stream
+ * order); calls sharing one workspace must be ordered on one stream.
  */
 int kda_prefill_chunked(const float* S0, const void* q, const void* k,
                         const void* v, const void* g, const void* beta,
@@ -158,7 +166,26 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k,
                         void* o, float* S_final,
                         void* page_pool, int64_t page_bytes,
                         const int32_t* ckpt_page_ids, int32_t* ckpt_pos, int64_t num_ckpt,
+                        void* workspace, int64_t workspace_bytes,
                         int mode, kda_stream_t stream);
+
+/*
+ * kda_prefill_workspace_bytes -- device scratch the tensor-core prefill needs
+ * for these sequences (0 when the shape runs on the CUDA-core kernel). The
+ * scratch holds, per 64-token chunk and head, the chunk's WY/UT operands in
+ * tensor-core layout. Host only; same sequence arguments as the prefill.
+ * Returns the byte count (>= 0) or a negative KDA_ERR_*.
+ */
+int64_t kda_prefill_workspace_bytes(const int32_t* cu_seqlens, int n_seqs, int64_t T,
+                                    int H, int dk, int dv, int dtype);
+
+/*
+ * kda_device_errors -- read and clear the library's device error word.
+ * Bit 0: a kernel gave up waiting on an mbarrier (about one second) and
+ * returned early, so that call's outputs are invalid. Synchronises the
+ * device. *flags receives the word; returns KDA_OK or KDA_ERR_CUDA.
+ */
+int kda_device_errors(int* flags);
 
 /*
  * kda_pack_heads -- gather (B,H,dk,dv) states into one flat head-contiguous

@@ -1,0 +1,97 @@
+"""Run one KDA workload a few times on cuda:0 (for profilers and quick timing).
+
+    python -m kda_delta_rule_gb300.cases decode   [--reps N]   # B=256 H=32 d=128, bf16 projections
+    python -m kda_delta_rule_gb300.cases replay   [--reps N]   # B=32 H=16 d=32 draft 8, fp32
+    python -m kda_delta_rule_gb300.cases prefill  [--reps N]   # T=8192 H=32 d=128 bf16, 16 checkpoints
+    python -m kda_delta_rule_gb300.cases varlen   [--reps N]   # 64 seqs, ~0.5M tokens, H=32 d=128 bf16
+    python -m kda_delta_rule_gb300.cases pack     [--reps N]   # pack+unpack of a (256,32,128,128) state
+
+Each case prints the mean device time per call measured with CUDA events.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import inputs as I
+from . import kda as K
+
+
+def _time(fn, reps):
+    fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def case_decode(reps, H=32, d=128, B=256):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    S = (0.05 * torch.randn(B, H, d, d, generator=gen, device="cuda")).contiguous()
+    p = I.decode_step_projections(B, H, d, d, dtype=torch.bfloat16, seed=1, device="cuda")
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+    return _time(lambda: K.kda_decode_step(S, p["q"], p["k"], p["v"], p["g"], p["beta"], o=o), reps)
+
+
+def case_replay(reps):
+    S, pr, n = I.replay_inputs(32, 16, 32, 32, 8, dtype=torch.float32, seed=0, device="cuda")
+    S_new = torch.empty_like(S)
+    out = torch.empty(32, 16, 8, 32, device="cuda")
+    return _time(lambda: K.kda_verify_replay(S, pr.q, pr.k, pr.v, pr.g, pr.beta, n, S_new=S_new, out=out),
+                 reps)
+
+
+def _prefill(lengths, reps, H=32, d=128, stride=512):
+    S0, p, cu = I.prefill_inputs(lengths, H, d, d, dtype=torch.bfloat16, seed=0, device="cuda")
+    n_ck = K.kda_num_checkpoints(cu, cu[-1], stride)
+    pool = K.PagePool(H * d * d * 4, n_ck)
+    ids = torch.tensor(pool.alloc(n_ck), dtype=torch.int32, device="cuda")
+    o = torch.empty(cu[-1], H, d, dtype=torch.bfloat16, device="cuda")
+    Sf = torch.empty_like(S0)
+    ws = torch.empty(max(K.kda_prefill_workspace_bytes(cu, cu[-1], H, d, d, torch.bfloat16), 16),
+                     dtype=torch.uint8, device="cuda")
+    return _time(lambda: K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
+                                               ckpt_stride=stride, page_pool=pool, ckpt_page_ids=ids,
+                                               o=o, S_final=Sf, workspace=ws), reps)
+
+
+def case_prefill(reps):
+    return _prefill([8192], reps)
+
+
+def case_varlen(reps):
+    return _prefill(I.varlen_lengths(64, seed=0), reps)
+
+
+def case_pack(reps):
+    S = torch.randn(256, 32, 128, 128, device="cuda")
+    flat = torch.empty(S.numel(), device="cuda")
+    back = torch.empty_like(S)
+
+    def run():
+        K.kda_pack_heads(S, flat=flat)
+        K.kda_unpack_heads(flat, back)
+    return _time(run, reps)
+
+
+CASES = {"decode": case_decode, "replay": case_replay, "prefill": case_prefill,
+         "varlen": case_varlen, "pack": case_pack}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--reps", type=int, default=3)
+    args = ap.parse_args()
+    ms = CASES[args.case](args.reps)
+    print(f"{args.case}: {ms:.4f} ms per call (mean of {args.reps})")
+
+
+if __name__ == "__main__":
+    main()

@@ -170,11 +170,43 @@ int64_t kda_num_checkpoints(const int32_t* cu_seqlens, int n_seqs, int64_t T, in
   return n;
 }
 
+// Per launch group of at most kMaxSeqs sequences: chunks of the group.
+static int64_t group_chunks(const int32_t* cu, int N, int64_t T, int g0) {
+  const int n = std::min(kda::kMaxSeqs, N - g0);
+  int64_t c = 0;
+  for (int i = g0; i < g0 + n; ++i) {
+    const int64_t L = cu ? (int64_t)cu[i + 1] - cu[i] : T;
+    c += (L + 63) / 64;
+  }
+  return c;
+}
+
+int64_t kda_prefill_workspace_bytes(const int32_t* cu_seqlens, int n_seqs, int64_t T, int H,
+                                    int dk, int dv, int dtype) {
+  if (int st = check_seqlens(cu_seqlens, n_seqs, T)) return st;
+  if (H < 0) return fail(KDA_ERR_SHAPE, "negative H");
+  ok();
+  if (!kda::prefill_tc_supported(dk, dv, dtype)) return 0;
+  const int N = cu_seqlens ? n_seqs : 1;
+  int64_t worst = 0;
+  for (int g0 = 0; g0 < N; g0 += kda::kMaxSeqs)
+    worst = std::max(worst, group_chunks(cu_seqlens, N, T, g0));
+  return worst * H * kda::prefill_tc_image_bytes(dv);
+}
+
+int kda_device_errors(int* flags) {
+  if (!flags) return fail(KDA_ERR_ARG, "flags is NULL");
+  int e = kda::read_and_clear_device_errors(flags);
+  if (e != 0) return cuda_status((cudaError_t)e, "kda_device_errors");
+  return ok();
+}
+
 int kda_prefill_chunked(const float* S0, const void* q, const void* k, const void* v,
                         const void* g, const void* beta, const int32_t* cu_seqlens, int n_seqs,
                         int64_t T, int H, int dk, int dv, int dtype, int chunk, int ckpt_stride,
                         void* o, float* S_final, void* page_pool, int64_t page_bytes,
                         const int32_t* ckpt_page_ids, int32_t* ckpt_pos, int64_t num_ckpt,
+                        void* workspace, int64_t workspace_bytes,
                         int mode, kda_stream_t stream) {
   if (int st = check_common(dk, dv, dtype, mode)) return st;
   if (chunk != 64) return fail(KDA_ERR_ARG, "chunk=%d: the kernels use 64-token chunks", chunk);
@@ -210,6 +242,15 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
                   (long long)page_bytes, (long long)H * dk * dv * 4);
     if (!aligned16(page_pool)) return fail(KDA_ERR_ALIGN, "page_pool must be 16-byte aligned");
   }
+  if (workspace) {
+    const int64_t ws_need = kda_prefill_workspace_bytes(cu_seqlens, n_seqs, T, H, dk, dv, dtype);
+    if (ws_need < 0) return (int)ws_need;
+    if (workspace_bytes < ws_need)
+      return fail(KDA_ERR_SHAPE, "workspace_bytes=%lld < %lld needed", (long long)workspace_bytes,
+                  (long long)ws_need);
+    if (!aligned16(workspace)) return fail(KDA_ERR_ALIGN, "workspace must be 16-byte aligned");
+    if (ws_need == 0) workspace = nullptr;
+  }
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   std::vector<int32_t> starts(N), lens(N), bases(N);
@@ -231,13 +272,17 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
     std::iota(idx.begin(), idx.end(), 0);
     std::stable_sort(idx.begin(), idx.end(), [&](int x, int y) { return lens[g0 + x] > lens[g0 + y]; });
     int max_len = 0;
+    int32_t cbase = 0;
     for (int i = 0; i < n; ++i) {
       sched->order[i] = idx[i];
       sched->start[i] = starts[g0 + i];
       sched->len[i] = lens[g0 + i];
       sched->ckpt_base[i] = bases[g0 + i];
+      sched->chunk_base[i] = cbase;
+      cbase += (lens[g0 + i] + 63) / 64;
       max_len = std::max(max_len, lens[g0 + i]);
     }
+    sched->chunk_base[n] = cbase;
     kda::PrefillArgs a{};
     const int64_t hs = (int64_t)H * dk * dv;
     a.S0 = S0 ? S0 + g0 * hs : nullptr;
@@ -250,6 +295,7 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
     a.num_ckpt = need > 0 ? num_ckpt : 0;
     a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
     a.ckpt_stride = ckpt_stride; a.mode = mode;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     status = cuda_status(kda::launch_prefill(a, *sched, max_len, s), "kda_prefill_chunked launch");
   }
   return status;

@@ -31,6 +31,7 @@ struct PrefillSched {
   int32_t start[kMaxSeqs];       // first token of each sequence (relative to `base_token`)
   int32_t len[kMaxSeqs];         // tokens of each sequence
   int32_t ckpt_base[kMaxSeqs];   // index of each sequence's first checkpoint
+  int32_t chunk_base[kMaxSeqs + 1];  // index of each sequence's first 64-token chunk; [n_seqs] = total
 };
 
 struct PrefillArgs {
@@ -43,10 +44,19 @@ struct PrefillArgs {
   const int32_t* ckpt_page_ids;  // offset to this launch's first checkpoint
   int32_t* ckpt_pos;             // same offset, or nullptr
   int64_t num_ckpt;              // entries available from the offset
+  void* workspace;               // chunk images of the tensor-core path, or nullptr
+  int64_t workspace_bytes;
   int H, dk, dv, dtype, chunk, ckpt_stride, mode;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, const PrefillSched& sched, int max_len,
                            cudaStream_t s);
+
+// Tensor-core path (kda_prefill_tc.cu): shapes it takes and workspace bytes per
+// (64-token chunk, head).
+bool prefill_tc_supported(int dk, int dv, int dtype);
+int64_t prefill_tc_image_bytes(int dv);
+// Copy the device error word to *flags and clear it (synchronises the device).
+int read_and_clear_device_errors(int* flags);
 
 // Flat <-> strided (B,H,dk,dv) copies.  pack zero-fills flat past B*H*dk*dv.
 cudaError_t launch_pack(const float* S, int64_t stride_b, int64_t stride_h, float* flat,

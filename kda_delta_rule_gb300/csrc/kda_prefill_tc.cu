@@ -1,10 +1,590 @@
-// Tensor-core (tcgen05) chunked prefill: not built yet; every call falls
-// through to the fp32 CUDA-core kernel.
+// Chunked prefill of the KDA gated delta rule on tcgen05 tensor cores (bf16
+// operands, fp32 accumulation and state), dk = 128, dv in {64, 128}.
+//
+// Math ("Kimi Linear 的 KDA 缓存", section "预填充为什么能分块并行": every
+// token's transition is a diagonal minus a rank-one matrix; a 64-token chunk
+// compresses into WY/UT form with a small lower-triangular solve).  Per chunk
+// and head, with Gamma_r the inclusive per-channel cumsum of g inside the chunk
+// and G_r = Gamma_r (decay first) or Gamma_{r-1} (undecayed delta):
+//   A[r,s] = beta_s <k_r, k_s e^{G_r - Gamma_s}>   (s < r),  T = (I + A)^{-1}
+//   P[r,s] = <q_r, k_s e^{Gamma_r - Gamma_s}>       (s <= r)
+//   W = T (k e^{G}),  U = T V                        (WY representation)
+//   Delta' = beta (U - W S)                          (needs the state)
+//   O = (q e^{Gamma}) S + P Delta'
+//   S <- e^{Gamma_C} S + (k e^{Gamma_C - Gamma})^T Delta'
+// Two kernels:
+//  * chunk prep, one CTA per (chunk, head), all chunks in parallel: gates,
+//    A and P on tcgen05, the UT solve in shared memory, W and U on tcgen05.
+//    It writes, per chunk and head, a pre-swizzled image of every operand the
+//    state recurrence needs (the "chunk image") into the caller's workspace.
+//  * chain, one CTA per (sequence, head, 64-column slice of dv), walking the
+//    chunks in order: bulk-async (TMA) copies of the chunk images into a
+//    two-stage ring, three tcgen05 contractions per chunk with the fp32 state
+//    in registers, outputs and chunk-aligned checkpoints straight to memory
+//    ("SGLang：从一次较长的 extend 调用中提取检查点"; pages in pack_heads layout,
+//    KIMI K3 Serve demo page §1.5).
+// Pairwise decays are split at a reference token per 16-token column block
+// (its 8th token), so every exponential factor stays below e^{8 |g_min|}:
+// finite in bf16/fp32 for g >= -10.
+#include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_tc.cuh"
+#include "../../include/kda.h"
 
 namespace kda {
-cudaError_t launch_prefill_tc(const PrefillArgs&, const PrefillSched&, cudaStream_t, bool* handled) {
-  *handled = false;
-  return cudaSuccess;
+namespace {
+using namespace tc;
+
+constexpr int C = 64;
+constexpr int DKT = 128;
+constexpr int NT = 128;
+
+// ---- chunk image: byte offsets inside the image of one (chunk, head) -------
+// WQ: K-major [128 rows][128]: rows 0-63 = -beta W, rows 64-127 = q e^{Gamma}
+// KB: MN-major (mn = dk, K = 64 tokens): k e^{Gamma_C - Gamma}
+// P : K-major [64 rows][64]: P (masked)
+// U : [dv/64][64 rows][64] row-major bf16: beta U
+// EG: fp32[128]: e^{Gamma_C}
+constexpr uint32_t IMG_WQ = 0, IMG_KB = 32768, IMG_P = 49152, IMG_U = 57344;
+__host__ __device__ constexpr uint32_t img_eg(int dv) { return IMG_U + 64u * dv * 2u; }
+__host__ __device__ constexpr uint32_t img_bytes(int dv) { return img_eg(dv) + 512u; }
+
+// ---- prep kernel shared memory ---------------------------------------------
+constexpr uint32_t P_KHAT = 0;          // 16 KB  Khat K-major [64][128]; later V (MN-major, K=64)
+constexpr uint32_t P_APB = 16384;       // 33 KB  [Ktil_S; Qtil_S] K-major [128][128]; later A, T fp32 [64][65]
+constexpr uint32_t P_KTIL = 50176;      // 16 KB  k e^{G} MN-major (mn = dk, K = 64)
+constexpr uint32_t P_R1 = 66560;        // 32 KB  X, Y bf16 [64][128]; later XT scratch + TOP
+constexpr uint32_t P_TOP = P_R1 + 16384;  // 16 KB [T; 0] K-major [128][64]
+constexpr uint32_t P_MISC = 99328;      // beta fp32[64] | mbar | tmem slot
+constexpr uint32_t P_SMEM = P_MISC + 512 + 1024;
+
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  uint4 u;
+  __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 c = __floats2bfloat162_rn(v[4], v[5]), d = __floats2bfloat162_rn(v[6], v[7]);
+  u.x = *reinterpret_cast<uint32_t*>(&a); u.y = *reinterpret_cast<uint32_t*>(&b);
+  u.z = *reinterpret_cast<uint32_t*>(&c); u.w = *reinterpret_cast<uint32_t*>(&d);
+  return u;
 }
+
+__device__ __forceinline__ int find_seq(const PrefillSched& s, int chunk) {
+  int lo = 0, hi = s.n_seqs - 1;
+  while (lo < hi) {                     // last n with chunk_base[n] <= chunk
+    const int mid = (lo + hi + 1) >> 1;
+    if (s.chunk_base[mid] <= chunk) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// All threads wait on an mbarrier; the outcome is made uniform across the CTA.
+__device__ __forceinline__ bool cta_wait(uint32_t mbar, uint32_t parity) {
+  const bool ok = mbar_wait(mbar, parity);
+  return __syncthreads_and(ok) != 0;
+}
+
+template <int DV>
+__global__ void __launch_bounds__(NT, 2)
+kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned char* __restrict__ ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  float* s_beta = reinterpret_cast<float*>(sm + P_MISC);
+  const uint32_t mbar = smem_u32(sm + P_MISC + 256);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_MISC + 264);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int chunk = blockIdx.x, h = blockIdx.y, H = a.H;
+  const int n = find_seq(sched, chunk);
+  const int c = chunk - sched.chunk_base[n];
+  const int64_t t0 = (int64_t)sched.start[n] + (int64_t)c * C;
+  const int L = min(C, sched.len[n] - c * C);
+  const bool decay_first = a.mode == KDA_MODE_DECAY_FIRST;
+  unsigned char* img = ws + ((int64_t)chunk * H + h) * img_bytes(DV);
+  const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* gg = reinterpret_cast<const __nv_bfloat16*>(a.g);
+  const __nv_bfloat16* vg = reinterpret_cast<const __nv_bfloat16*>(a.v);
+  const __nv_bfloat16* bg = reinterpret_cast<const __nv_bfloat16*>(a.beta);
+
+  if (tid == 0) { mbar_init(mbar, 1); mbar_init_fence(); }
+  if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
+  if (tid < C) s_beta[tid] = tid < L ? ldf(bg + (t0 + tid) * H + h) : 0.f;
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tslot;
+  uint32_t phase = 0;
+  bool ok = true;
+
+  // ---- gates: thread i owns key channel i ----------------------------------
+  const int i = tid;
+  const int64_t rowq = (int64_t)H * DKT;          // token stride of q, k, g
+  const int64_t base_qk = t0 * rowq + (int64_t)h * DKT + i;
+  float Gam[C];
+  {
+    float acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      acc += r < L ? ldf(gg + base_qk + r * rowq) : 0.f;
+      Gam[r] = acc;
+    }
+  }
+  const float GC = Gam[C - 1];
+  float gm[4], egm[4], egcm[4];
+#pragma unroll
+  for (int R = 0; R < 4; ++R) {
+    gm[R] = Gam[16 * R + 7];
+    egm[R] = __expf(gm[R]);
+    egcm[R] = __expf(GC - gm[R]);
+  }
+
+  __nv_bfloat16* X = reinterpret_cast<__nv_bfloat16*>(sm + P_R1);          // [64][128]
+  __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(sm + P_R1 + 16384);  // [64][128]
+#pragma unroll
+  for (int r = 0; r < C; ++r) {
+    const int R = r >> 4;
+    const float kr = r < L ? ldf(kg + base_qk + r * rowq) : 0.f;
+    const float qr = r < L ? ldf(qg + base_qk + r * rowq) : 0.f;
+    const float d = Gam[r] - gm[R];
+    const float E = __expf(d), Einv = __expf(-d);
+    const float EG = decay_first ? E : __expf((r ? Gam[r - 1] : 0.f) - gm[R]);
+    st_bf16(sm + P_KHAT, off_k(r, i, 64), kr * Einv);
+    st_bf16(sm + P_KTIL, off_mn(i, r, 64), kr * EG * egm[R]);
+    st_bf16(img + IMG_WQ, off_k(64 + r, i, 128), qr * E * egm[R]);
+    st_bf16(img + IMG_KB, off_mn(i, r, 64), kr * Einv * egcm[R]);
+    X[r * DKT + i] = __float2bfloat16_rn(kr * EG);
+    Y[r * DKT + i] = __float2bfloat16_rn(qr * E);
+  }
+  reinterpret_cast<float*>(img + img_eg(DV))[i] = __expf(GC);
+
+  // ---- A and P: one tcgen05 MMA chain per 16-token column block ------------
+  const uint32_t apb = smem_u32(sm + P_APB);
+  const uint32_t khat = smem_u32(sm + P_KHAT);
+  constexpr uint32_t ID_AP = idesc_bf16(128, 16, false, false);
+  for (int S = 0; S < 4 && ok; ++S) {
+    if (S > 0) {                                   // previous MMA must finish reading APB
+      ok = cta_wait(mbar, phase);
+      phase ^= 1;
+      fence_after();
+      if (!ok) break;
+    }
+    // block-to-block factors e^{Gamma_m(R) - Gamma_m(S)} <= 1 for R >= S
+    const float gmS = S == 0 ? gm[0] : (S == 1 ? gm[1] : (S == 2 ? gm[2] : gm[3]));
+    float fR[4];
+#pragma unroll
+    for (int R = 0; R < 4; ++R) fR[R] = R >= S ? __expf(gm[R] - gmS) : 0.f;
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      const int R = r >> 4;
+      float xs = 0.f, ys = 0.f;
+      if (R >= S) {
+        const float f = fR[R];
+        xs = __bfloat162float(X[r * DKT + i]) * f;
+        ys = __bfloat162float(Y[r * DKT + i]) * f;
+      }
+      st_bf16(sm + P_APB, off_k(r, i, 128), xs);
+      st_bf16(sm + P_APB, off_k(64 + r, i, 128), ys);
+    }
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (tid == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mma(tmem + 16 * S, desc_k(apb, 128, j), desc_k(khat + 2048 * S, 64, j), ID_AP, j > 0);
+      mma_commit(mbar);
+    }
+  }
+  if (ok) { ok = cta_wait(mbar, phase); phase ^= 1; fence_after(); }
+
+  // ---- read A (lanes 0-63) and P (lanes 64-127) ----------------------------
+  float* AF = reinterpret_cast<float*>(sm + P_APB);            // [64][65]
+  float* TF = AF + 64 * 65;                                     // [64][65]
+  if (ok) {
+    const int r = tid & 63;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+      float v[16];
+      tmem_ld16(lane_addr + 16 * cb, v);
+      tmem_wait_ld();
+      if (warp < 2) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int s = 16 * cb + e;
+          AF[r * 65 + s] = s < r ? s_beta[s] * v[e] : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          float p8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s = 16 * cb + 8 * hlf + e;
+            p8[e] = s <= r ? v[8 * hlf + e] : 0.f;
+          }
+          *reinterpret_cast<uint4*>(img + IMG_P + off_k(r, 16 * cb + 8 * hlf, 64)) = pack8(p8);
+        }
+      }
+    }
+  }
+  for (int e = tid; e < 64 * 65; e += NT) TF[e] = 0.f;
+  fence_before();
+  __syncthreads();
+  fence_after();
+
+  // ---- UT solve T = (I + A)^{-1}: 16x16 diagonal blocks, then block levels --
+  if (tid < 64) {
+    const int J = tid >> 4, cc = tid & 15, b0 = 16 * J;
+    float x[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < j; ++s) acc = fmaf(AF[(b0 + j) * 65 + b0 + s], x[s], acc);
+      x[j] = j == cc ? 1.f : (j < cc ? 0.f : -acc);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) TF[(b0 + j) * 65 + b0 + cc] = x[j];
+  }
+  __syncthreads();
+  float* XT = reinterpret_cast<float*>(sm + P_R1);               // [3][16][16]
+  for (int d = 1; d < 4; ++d) {
+    const int nb = 4 - d;
+    for (int e = tid; e < nb * 256; e += NT) {
+      const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
+      float acc = 0.f;
+      for (int K = J; K < I; ++K)
+#pragma unroll
+        for (int s = 0; s < 16; ++s)
+          acc = fmaf(AF[(16 * I + ar) * 65 + 16 * K + s], TF[(16 * K + s) * 65 + 16 * J + bc], acc);
+      XT[e] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < nb * 256; e += NT) {
+      const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
+      float acc = 0.f;
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+        if (s <= ar) acc = fmaf(TF[(16 * I + ar) * 65 + 16 * I + s], XT[(J << 8) + s * 16 + bc], acc);
+      TF[(16 * I + ar) * 65 + 16 * J + bc] = -acc;
+    }
+    __syncthreads();
+  }
+
+  // ---- [T; 0] as bf16 A operand, V as MN-major B operand --------------------
+  {
+    const int r = tid;
+#pragma unroll
+    for (int cch = 0; cch < 8; ++cch) {
+      float t8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) t8[e] = r < 64 ? TF[r * 65 + 8 * cch + e] : 0.f;
+      *reinterpret_cast<uint4*>(sm + P_TOP + off_k(r, 8 * cch, 128)) = pack8(t8);
+    }
+  }
+  if (tid < DV) {
+    const int j = tid;
+    const int64_t rowv = (int64_t)H * DV;
+    const int64_t base_v = t0 * rowv + (int64_t)h * DV + j;
+#pragma unroll 8
+    for (int r = 0; r < C; ++r)
+      st_bf16(sm + P_KHAT, off_mn(j, r, 64), r < L ? ldf(vg + base_v + r * rowv) : 0.f);
+  }
+  fence_async_smem();
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (ok && tid == 0) {
+    const uint32_t top = smem_u32(sm + P_TOP);
+    constexpr uint32_t ID_W = idesc_bf16(128, 128, false, true);
+    constexpr uint32_t ID_U = idesc_bf16(128, DV, false, true);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mma(tmem, desc_k(top, 128, j), desc_mn(smem_u32(sm + P_KTIL), 64, j), ID_W, j > 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mma(tmem + 128, desc_k(top, 128, j), desc_mn(khat, 64, j), ID_U, j > 0);
+    mma_commit(mbar);
+  }
+  if (ok) { ok = cta_wait(mbar, phase); phase ^= 1; fence_after(); }
+
+  // ---- -beta W and beta U rows to the chunk image ----------------------------
+  if (ok && warp < 2) {
+    const int r = tid;
+    const float br = s_beta[r];
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll
+    for (int cb = 0; cb < 8; ++cb) {
+      float v[16];
+      tmem_ld16(lane_addr + 16 * cb, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] *= -br;
+      *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, 16 * cb, 128)) = pack8(v);
+      *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, 16 * cb + 8, 128)) = pack8(v + 8);
+    }
+#pragma unroll
+    for (int cb = 0; cb < DV / 16; ++cb) {
+      float v[16];
+      tmem_ld16(lane_addr + 128 + 16 * cb, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] *= br;
+      const int j = 16 * cb;
+      unsigned char* dst = img + IMG_U + (j >> 6) * 8192 + r * 128 + (j & 63) * 2;
+      *reinterpret_cast<uint4*>(dst) = pack8(v);
+      *reinterpret_cast<uint4*>(dst + 16) = pack8(v + 8);
+    }
+  } else if (ok && warp >= 2) {
+    // lanes 64-127 hold the zero rows of [T; 0]: nothing to read, but the
+    // warp-collective loads are not needed either.
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ---- chain kernel -------------------------------------------------------------
+constexpr int DVS = 64;
+constexpr uint32_t S_WQ = 0, S_KB = 32768, S_PB = 49152, S_U = 65536, S_EG = 73728;
+constexpr uint32_t STAGE = 75776;                 // 74 KB, keeps every stage 1024-aligned
+constexpr uint32_t C_DELTA = 2 * STAGE;           // 8 KB  Delta' MN-major (mn = 64 cols, K = 64 tokens)
+constexpr uint32_t C_SB = C_DELTA + 8192;         // 16 KB S bf16 MN-major (mn = 64 cols, K = 128)
+constexpr uint32_t C_MISC = C_SB + 16384;
+constexpr uint32_t C_SMEM = C_MISC + 128 + 1024;
+constexpr uint32_t CHUNK_TX = 32768 + 16384 + 8192 + 8192 + 512;
+
+template <int DV>
+__global__ void __launch_bounds__(NT, 1)
+kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned char* __restrict__ ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t full0 = smem_u32(sm + C_MISC), mma_bar = smem_u32(sm + C_MISC + 16);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C_MISC + 32);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int sl = blockIdx.x, h = blockIdx.y, H = a.H;
+  const int n = sched.order[blockIdx.z];
+  const int64_t start = sched.start[n];
+  const int len = sched.len[n];
+  const int nch = (len + C - 1) / C;
+  const int64_t ib = img_bytes(DV);
+  const unsigned char* img0 = ws + ((int64_t)sched.chunk_base[n] * H + h) * ib;
+  const int col0 = sl * DVS;
+
+  if (tid == 0) {
+    mbar_init(full0, 1);
+    mbar_init(full0 + 8, 1);
+    mbar_init(mma_bar, 1);
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tslot), 128);
+  // zero rows 0-63 of both [0; P] buffers (never written by the copies)
+  for (int e = tid; e < 2 * 512; e += NT) {
+    const int s = e >> 9, o = e & 511;
+    reinterpret_cast<uint4*>(sm + s * STAGE + S_PB)[o] = make_uint4(0, 0, 0, 0);
+  }
+  // state row i = tid, columns col0..col0+63
+  const int i = tid;
+  float S[DVS];
+  const int64_t srow = (((int64_t)n * H + h) * DKT + i) * DV + col0;
+#pragma unroll
+  for (int j = 0; j < DVS; j += 4) {
+    float4 x = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + srow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+  }
+#pragma unroll
+  for (int cch = 0; cch < DVS / 8; ++cch)
+    *reinterpret_cast<uint4*>(sm + C_SB + off_mn(8 * cch, i, 128)) = pack8(S + 8 * cch);
+  fence_async_smem();
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t d1 = tmem, d2 = tmem + 64;
+
+  auto issue = [&](int cidx) {
+    const int s = cidx & 1;
+    const unsigned char* src = img0 + (int64_t)cidx * H * ib;
+    const uint32_t dst = smem_u32(sm + s * STAGE);
+    const uint32_t fb = full0 + 8 * s;
+    mbar_expect_tx(fb, CHUNK_TX);
+    bulk_g2s(dst + S_WQ, src + IMG_WQ, 32768, fb);
+    bulk_g2s(dst + S_KB, src + IMG_KB, 16384, fb);
+    bulk_g2s(dst + S_PB + 8192, src + IMG_P, 8192, fb);
+    bulk_g2s(dst + S_U, src + IMG_U + sl * 8192, 8192, fb);
+    bulk_g2s(dst + S_EG, src + img_eg(DV), 512, fb);
+  };
+  if (tid == 0) {
+    if (nch > 0) issue(0);
+    if (nch > 1) issue(1);
+  }
+
+  constexpr uint32_t ID_1 = idesc_bf16(128, DVS, false, true);   // [-bW; Qt] (K-major) x S (MN-major)
+  constexpr uint32_t ID_3 = idesc_bf16(128, DVS, true, true);    // Kbar^T (MN-major) x Delta' (MN-major)
+  const uint32_t delta = smem_u32(sm + C_DELTA), sb = smem_u32(sm + C_SB);
+  uint32_t mph = 0;
+  bool ok = true;
+  int issued = nch < 2 ? nch : 2, waited = 0;
+  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
+  const uint32_t lane_addr_off = (uint32_t)(32 * warp) << 16;
+
+  for (int c = 0; c < nch && ok; ++c) {
+    const int s = c & 1;
+    unsigned char* st = sm + s * STAGE;
+    ok = cta_wait(full0 + 8 * s, (c >> 1) & 1);
+    ++waited;
+    if (!ok) break;
+    if (tid == 0) {
+      const uint32_t wq = smem_u32(st + S_WQ);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mma(d1, desc_k(wq, 128, j), desc_mn(sb, 128, j), ID_1, j > 0);
+      mma_commit(mma_bar);
+    }
+    ok = cta_wait(mma_bar, mph);
+    mph ^= 1;
+    fence_after();
+    if (!ok) break;
+    if (warp < 2) {                         // Delta' = beta U - beta W S, row r = tid
+      const int r = tid;
+      const __nv_bfloat16* urow = reinterpret_cast<const __nv_bfloat16*>(st + S_U + r * 128);
+#pragma unroll
+      for (int cb = 0; cb < DVS / 16; ++cb) {
+        float v[16];
+        tmem_ld16(d1 + lane_addr_off + 16 * cb, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] += __bfloat162float(urow[16 * cb + e]);
+        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(16 * cb, r, 64)) = pack8(v);
+        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(16 * cb + 8, r, 64)) = pack8(v + 8);
+      }
+    }
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (tid == 0) {
+      const uint32_t pb = smem_u32(st + S_PB), kb = smem_u32(st + S_KB);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma(d1, desc_k(pb, 128, j), desc_mn(delta, 64, j), ID_1, 1);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma(d2, desc_mn(kb, 64, j), desc_mn(delta, 64, j), ID_3, j > 0);
+      mma_commit(mma_bar);
+    }
+    ok = cta_wait(mma_bar, mph);
+    mph ^= 1;
+    fence_after();
+    if (!ok) break;
+    // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
+    {
+      const float eg = reinterpret_cast<const float*>(st + S_EG)[i];
+#pragma unroll
+      for (int cb = 0; cb < DVS / 16; ++cb) {
+        float v[16];
+        tmem_ld16(d2 + lane_addr_off + 16 * cb, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) S[16 * cb + e] = fmaf(eg, S[16 * cb + e], v[e]);
+      }
+#pragma unroll
+      for (int cch = 0; cch < DVS / 8; ++cch)
+        *reinterpret_cast<uint4*>(sm + C_SB + off_mn(8 * cch, i, 128)) = pack8(S + 8 * cch);
+    }
+    const int L = min(C, len - c * C);
+    if (warp >= 2) {                        // outputs: rows 64-127 of d1
+      const int r = tid - 64;
+      __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0;
+#pragma unroll
+      for (int cb = 0; cb < DVS / 16; ++cb) {
+        float v[16];
+        tmem_ld16(d1 + lane_addr_off + 16 * cb, v);
+        tmem_wait_ld();
+        if (r < L) {
+          *reinterpret_cast<uint4*>(orow + 16 * cb) = pack8(v);
+          *reinterpret_cast<uint4*>(orow + 16 * cb + 8) = pack8(v + 8);
+        }
+      }
+    }
+    const int pos = c * C + L;
+    if (a.ckpt_stride > 0 && pos % a.ckpt_stride == 0) {
+      const int64_t idx = (int64_t)sched.ckpt_base[n] + pos / a.ckpt_stride - 1;
+      if (idx < a.num_ckpt) {
+        float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
+        float* prow = page + ((int64_t)h * DKT + i) * DV + col0;
+#pragma unroll
+        for (int j = 0; j < DVS; j += 4) *reinterpret_cast<float4*>(prow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        if (h == 0 && sl == 0) {
+          const int64_t used = (int64_t)H * DKT * DV, total = a.page_bytes / 4;
+          for (int64_t e = used + tid; e < total; e += NT) page[e] = 0.f;
+          if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = pos;
+        }
+      }
+    }
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (tid == 0 && c + 2 < nch) { issue(c + 2); ++issued; }
+  }
+  if (!ok && tid == 0) {
+    // drain copies still in flight before leaving (bounded)
+    for (int c = waited; c < issued; ++c) mbar_wait(full0 + 8 * (c & 1), (c >> 1) & 1);
+  }
+  if (ok) {
+    float* dst = a.S_final + (((int64_t)n * H + h) * DKT + i) * DV + col0;
+#pragma unroll
+    for (int j = 0; j < DVS; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+template <int DV>
+cudaError_t launch_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned char* ws, int total_chunks,
+                      cudaStream_t s) {
+  cudaError_t e;
+  if (total_chunks > 0) {
+    auto prep = kda_chunk_prep_kernel<DV>;
+    e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+    if (e != cudaSuccess) return e;
+    prep<<<dim3(total_chunks, a.H), NT, P_SMEM, s>>>(a, sched, ws);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  auto chain = kda_chain_kernel<DV>;
+  e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
+  if (e != cudaSuccess) return e;
+  chain<<<dim3(DV / DVS, a.H, sched.n_seqs), NT, C_SMEM, s>>>(a, sched, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int dk, int dv, int dtype) {
+  return dtype == KDA_BF16 && dk == 128 && (dv == 64 || dv == 128);
+}
+
+int64_t prefill_tc_image_bytes(int dv) { return img_bytes(dv); }
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s, bool* handled) {
+  *handled = prefill_tc_supported(a.dk, a.dv, a.dtype) && a.workspace != nullptr;
+  if (!*handled) return cudaSuccess;
+  if (sched.n_seqs == 0 || a.H == 0) return cudaSuccess;
+  const int total_chunks = sched.chunk_base[sched.n_seqs];
+  unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+  return a.dv == 128 ? launch_dv<128>(a, sched, ws, total_chunks, s)
+                     : launch_dv<64>(a, sched, ws, total_chunks, s);
+}
+
+int read_and_clear_device_errors(int* flags) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(flags, tc::g_kda_device_error, sizeof(int));
+  if (e != cudaSuccess) return (int)e;
+  e = cudaMemcpyToSymbol(tc::g_kda_device_error, &zero, sizeof(int));
+  return (int)e;
+}
+
 }  // namespace kda

@@ -43,7 +43,9 @@ def _load():
         "kda_decode_step": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
         "kda_verify_replay": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
         "kda_num_checkpoints": ([P, I, L, I], L),
-        "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, I, P], I),
+        "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, I, P], I),
+        "kda_prefill_workspace_bytes": ([P, I, L, I, I, I, I], L),
+        "kda_device_errors": ([ctypes.POINTER(ctypes.c_int)], I),
         "kda_pack_heads": ([P, L, L, P, L, I, I, I, I, P], I),
         "kda_unpack_heads": ([P, P, L, L, I, I, I, I, P], I),
         "kda_pool_create": ([P, L, L, ctypes.POINTER(P)], I),
@@ -168,15 +170,32 @@ def kda_num_checkpoints(cu_seqlens, T, ckpt_stride) -> int:
     return int(r)
 
 
+def kda_prefill_workspace_bytes(cu_seqlens, T, H, dk, dv, dtype) -> int:
+    arr, n = _cu_array(cu_seqlens)
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    r = _lib.kda_prefill_workspace_bytes(arr, n, int(T), int(H), int(dk), int(dv), code)
+    if r < 0:
+        _check(int(r), "kda_prefill_workspace_bytes")
+    return int(r)
+
+
+def kda_device_errors() -> int:
+    """Read and clear the device error word (bit 0: an mbarrier wait timed out)."""
+    flags = ctypes.c_int(0)
+    _check(_lib.kda_device_errors(ctypes.byref(flags)), "kda_device_errors")
+    return int(flags.value)
+
+
 def kda_prefill_chunked(S0, q, k, v, g, beta, cu_seqlens=None, chunk=64, ckpt_stride=512,
                         o=None, S_final=None, page_pool=None, ckpt_page_ids=None, ckpt_pos=None,
-                        mode=DECAY_FIRST, stream=None, n_seqs=None, H=None):
+                        mode=DECAY_FIRST, stream=None, workspace="auto"):
     """Chunked prefill of packed sequences with chunk-aligned checkpoints.
 
     q,k,g (T,H,dk); v (T,H,dv); beta (T,H); cu_seqlens: host list of N+1 ints (None: one
     sequence). S0 (N,H,dk,dv) fp32 or None (zero state). page_pool: a PagePool (or None
     when no checkpoints are emitted); ckpt_page_ids: CUDA int32 tensor with one page per
-    checkpoint. Returns (o, S_final).
+    checkpoint. workspace: "auto" (allocate what the tensor-core kernels need), None (no
+    workspace: the fp32 CUDA-core kernel runs) or a CUDA uint8 tensor. Returns (o, S_final).
     """
     T, Hq, dk = q.shape
     code, _, dv = _projections(q, k, v, g, beta, (T, Hq))
@@ -199,11 +218,18 @@ def kda_prefill_chunked(S0, q, k, v, g, beta, cu_seqlens=None, chunk=64, ckpt_st
         base, page_bytes = ctypes.c_void_p(page_pool.arena.data_ptr()), page_pool.page_bytes
     if ckpt_pos is not None:
         _cuda("ckpt_pos", ckpt_pos, torch.int32)
+    if isinstance(workspace, str):
+        need = kda_prefill_workspace_bytes(cu_seqlens, T, Hq, dk, dv, q.dtype)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
+    ws_bytes = 0
+    if workspace is not None:
+        _cuda("workspace", workspace, torch.uint8)
+        ws_bytes = workspace.numel()
     _check(_lib.kda_prefill_chunked(_ptr(S0), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                     arr, N, T, Hq, dk, dv, code, chunk, ckpt_stride,
                                     _ptr(o), _ptr(S_final), base, page_bytes,
-                                    _ptr(ckpt_page_ids), _ptr(ckpt_pos), n_ck, mode,
-                                    _stream(stream, dev)),
+                                    _ptr(ckpt_page_ids), _ptr(ckpt_pos), n_ck,
+                                    _ptr(workspace), ws_bytes, mode, _stream(stream, dev)),
            "kda_prefill_chunked")
     return o, S_final
 

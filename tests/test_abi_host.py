@@ -164,11 +164,12 @@ def test_prefill_validation(K):
         a = dict(S0=P(0), q=P(1 << 24), k=P(2 << 24), v=P(3 << 24), g=P(4 << 24), beta=P(5 << 24),
                  cu=cu, n=2, T=228, H=2, dk=32, dv=32, dtype=0, chunk=64, stride=64,
                  o=P(6 << 24), Sf=P(7 << 24), pool=P(8 << 24), page_bytes=8192,
-                 ids=P(9 << 24), pos=None, nck=10, mode=0)
+                 ids=P(9 << 24), pos=None, nck=10, ws=None, ws_bytes=0, mode=0)
         a.update(kw)
         return f(a["S0"], a["q"], a["k"], a["v"], a["g"], a["beta"], a["cu"], a["n"], a["T"],
                  a["H"], a["dk"], a["dv"], a["dtype"], a["chunk"], a["stride"], a["o"], a["Sf"],
-                 a["pool"], a["page_bytes"], a["ids"], a["pos"], a["nck"], a["mode"], None)
+                 a["pool"], a["page_bytes"], a["ids"], a["pos"], a["nck"], a["ws"], a["ws_bytes"],
+                 a["mode"], None)
 
     assert call(chunk=32) == -1
     assert call(stride=96) == -1                               # not a multiple of chunk
@@ -181,6 +182,15 @@ def test_prefill_validation(K):
     assert call(o=P(1 << 24)) == -7                            # o overlaps q
     assert call(cu=None, n=2) == -1
     assert call(H=0) == 0                                      # nothing to do
+    # tensor-core shapes need the workspace that kda_prefill_workspace_bytes reports
+    need = K._lib.kda_prefill_workspace_bytes(cu, 2, 228, 2, 128, 128, 1)
+    assert need == (2 + 2) * 2 * 74240                         # ceil(100/64)+ceil(128/64) chunks x H
+    assert K._lib.kda_prefill_workspace_bytes(cu, 2, 228, 2, 32, 32, 1) == 0
+    assert K._lib.kda_prefill_workspace_bytes(cu, 2, 228, 2, 128, 128, 0) == 0
+    assert call(dk=128, dv=128, dtype=1, page_bytes=2 * 128 * 128 * 4, ws=P(10 << 24),
+                ws_bytes=need - 16) == -2
+    assert call(dk=128, dv=128, dtype=1, page_bytes=2 * 128 * 128 * 4, ws=P(10 << 24) if False else
+                ctypes.c_void_p(A + (10 << 24) + 8), ws_bytes=need) == -4
 
 
 def test_pack_validation(K):

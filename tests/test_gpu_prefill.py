@@ -169,3 +169,73 @@ def test_varlen_resume_sampled(K):
         for j in sorted({0, len(ck_ref) - 1}):
             page = pool.page(int(ids[base[n] + j])).reshape(H, d, d)
             assert rel(page[h], ck_ref[j][2][0]) < TOL_BF16_STATE
+
+
+# ---------------------------------------------------------------------------
+# Tensor-core path (bf16, dk = 128, dv in {64, 128}) against the oracle
+# ---------------------------------------------------------------------------
+def _tc_case(K, lengths, dv, mode=0, seed=0, stride=128, g_min=-5.0, pad_bytes=0, state_std=0.05):
+    H, dk = 2, 128
+    S0, p, cu = I.prefill_inputs(lengths, H, dk, dv, dtype=torch.bfloat16, seed=seed,
+                                 g_min=g_min, state_std=state_std)
+    assert K.kda_prefill_workspace_bytes(cu, cu[-1], H, dk, dv, torch.bfloat16) > 0 or cu[-1] == 0
+    o, S_fin, pool, ids, pos = run_prefill(K, S0, p, cu, H, dk, dv, stride, mode, pad_bytes)
+    assert K.kda_device_errors() == 0
+    args = [f(S0)] + [f(p[n]) for n in ("q", "k", "v", "g", "beta")]
+    o_ref, S_ref, ck_ref = O.prefill_chunked(*args, cu_seqlens=cu, chunk=64, ckpt_stride=stride,
+                                             mode=mode)
+    assert rel(o, o_ref) < TOL_BF16_OUT
+    assert rel(S_fin, S_ref) < TOL_BF16_STATE
+    assert pos.tolist() == [t for _, t, _ in ck_ref]
+    n_state = H * dk * dv
+    for c, (n, t, st) in enumerate(ck_ref):
+        page = pool.page(int(ids[c]))
+        assert rel(page[:n_state].reshape(H, dk, dv), st) < TOL_BF16_STATE
+        if pad_bytes:
+            assert torch.all(page[n_state:] == 0)
+        if t == lengths[n]:
+            assert torch.equal(page[:n_state].reshape(H, dk, dv), S_fin[n])
+    return o, S_fin, o_ref, S_ref
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("dv", [64, 128])
+def test_tc_single_sequence(K, dv, mode):
+    _tc_case(K, [512], dv, mode=mode, seed=dv + mode)
+
+
+@pytest.mark.parametrize("dv", [64, 128])
+def test_tc_ragged_varlen(K, dv):
+    _tc_case(K, [1, 63, 65, 130, 0, 200, 128, 320], dv, seed=3, pad_bytes=64)
+
+
+def test_tc_strong_decay(K):
+    _tc_case(K, [256, 100], 128, seed=4, g_min=-10.0)
+
+
+def test_tc_cold_start_and_single_chunk(K):
+    _tc_case(K, [64], 128, seed=5, state_std=0.0)
+    _tc_case(K, [7], 64, seed=6)
+
+
+def test_tc_matches_fp32_kernel(K):
+    """bf16 inputs: tensor-core kernels vs the fp32 CUDA-core kernel on the same call."""
+    H, d = 4, 128
+    S0, p, cu = I.prefill_inputs([700, 300], H, d, d, dtype=torch.bfloat16, seed=8, device="cuda")
+    o_tc, S_tc = K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
+                                       ckpt_stride=0)
+    o_ref, S_ref = K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
+                                         ckpt_stride=0, workspace=None)
+    torch.cuda.synchronize()
+    assert rel(o_tc, o_ref) < TOL_BF16_OUT and rel(S_tc, S_ref) < TOL_BF16_STATE
+
+
+def test_tc_workspace_too_small_is_rejected(K):
+    H, d = 2, 128
+    S0, p, cu = I.prefill_inputs([128], H, d, d, dtype=torch.bfloat16, seed=1, device="cuda")
+    need = K.kda_prefill_workspace_bytes(cu, 128, H, d, d, torch.bfloat16)
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(K.KdaError) as e:
+        K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
+                              ckpt_stride=0, workspace=ws)
+    assert e.value.status == -2
