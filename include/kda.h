@@ -188,6 +188,37 @@ int64_t kda_prefill_workspace_bytes(const int32_t* cu_seqlens, int n_seqs, int64
 int kda_device_errors(int* flags);
 
 /*
+ * kda_prefill_chunked_noalloc -- kda_prefill_chunked without a caller
+ * workspace. It allocates no device memory, for callers that cannot call
+ * cudaMalloc/cudaFree at call time: serving loops that forbid them because
+ * they synchronise the whole device and stall every stream, and code embedded
+ * in a host framework that owns all device memory through its own allocator.
+ * (The pages have no counterpart: this is an interface for such callers.)
+ * Same arguments, layouts and results as kda_prefill_chunked. The
+ * tensor-core scratch comes from one fixed array of
+ * KDA_NOALLOC_SCRATCH_BYTES in device memory, which every GPU that loads the
+ * library holds until the process exits; a call whose shape needs more
+ * (kda_prefill_workspace_bytes() larger than that) fails with KDA_ERR_SHAPE
+ * and launches nothing. Shapes that need no scratch run the fp32 CUDA-core
+ * kernel as kda_prefill_chunked does with a NULL workspace.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array: calls whose kernels overlap on the GPU (on
+ * different streams, or from different threads) race on it and must be
+ * ordered by the caller. Nothing in it needs clearing between calls: every
+ * byte a call reads was written earlier in the same call.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64ull << 20)   /* 64 MiB */
+int kda_prefill_chunked_noalloc(const float* S0, const void* q, const void* k,
+                                const void* v, const void* g, const void* beta,
+                                const int32_t* cu_seqlens, int n_seqs, int64_t T,
+                                int H, int dk, int dv, int dtype, int chunk, int ckpt_stride,
+                                void* o, float* S_final,
+                                void* page_pool, int64_t page_bytes,
+                                const int32_t* ckpt_page_ids, int32_t* ckpt_pos, int64_t num_ckpt,
+                                int mode, kda_stream_t stream);
+
+/*
  * kda_pack_heads -- gather (B,H,dk,dv) states into one flat head-contiguous
  * buffer, zero-filling it past B*H*dk*dv. [SERVE] §1.5 pack_heads.
  *   S         device fp32; element (b,h,i,j) at S[b*stride_b + h*stride_h + i*dv + j]

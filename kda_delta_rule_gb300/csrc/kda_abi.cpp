@@ -455,6 +455,10 @@ double kda_snapshot_cost_ratio(int H, int dk, int dv) {
 
 }  // extern "C"
 
+namespace kda {
+int set_error(int status, const char* msg) { return fail(status, "%s", msg); }
+}  // namespace kda
+
 // Prefill dispatch: the tensor-core kernel takes bf16 projections where it
 // supports the shape; everything else runs the fp32 CUDA-core kernel.
 namespace kda {

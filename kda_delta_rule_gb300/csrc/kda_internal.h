@@ -57,6 +57,8 @@ bool prefill_tc_supported(int dk, int dv, int dtype);
 int64_t prefill_tc_image_bytes(int dv);
 // Copy the device error word to *flags and clear it (synchronises the device).
 int read_and_clear_device_errors(int* flags);
+// Record a failure message for kda_last_error() and return `status`.
+int set_error(int status, const char* msg);
 
 // Flat <-> strided (B,H,dk,dv) copies.  pack zero-fills flat past B*H*dk*dv.
 cudaError_t launch_pack(const float* S, int64_t stride_b, int64_t stride_h, float* flat,

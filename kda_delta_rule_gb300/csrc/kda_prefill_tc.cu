@@ -31,6 +31,9 @@
 #include "kda_tc.cuh"
 #include "../../include/kda.h"
 
+#include <cstdio>
+#include <mutex>
+
 namespace kda {
 namespace {
 using namespace tc;
@@ -588,3 +591,75 @@ int read_and_clear_device_errors(int* flags) {
 }
 
 }  // namespace kda
+
+// ---------------------------------------------------------------------------
+// Fixed device scratch for kda_prefill_chunked_noalloc: callers that cannot
+// allocate device memory at call time get the chunk images from this array.
+// Device code could name it directly; host code needs its device address,
+// which is looked up once per device (with that device current) and kept.
+// ---------------------------------------------------------------------------
+namespace kda {
+namespace {
+constexpr unsigned long long kNoallocBytes = KDA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (nullptr on error).
+void* noalloc_scratch(int* cuda_err) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *cuda_err = e != cudaSuccess ? (int)e : (int)cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      *cuda_err = e != cudaSuccess ? (int)e : (int)cudaErrorInvalidSymbol;
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *cuda_err = 0;
+  return g_noalloc_ptr[dev];
+}
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_prefill_chunked_noalloc(const float* S0, const void* q, const void* k, const void* v,
+                                           const void* g, const void* beta, const int32_t* cu_seqlens,
+                                           int n_seqs, int64_t T, int H, int dk, int dv, int dtype,
+                                           int chunk, int ckpt_stride, void* o, float* S_final,
+                                           void* page_pool, int64_t page_bytes,
+                                           const int32_t* ckpt_page_ids, int32_t* ckpt_pos,
+                                           int64_t num_ckpt, int mode, kda_stream_t stream) {
+  const int64_t need = kda_prefill_workspace_bytes(cu_seqlens, n_seqs, T, H, dk, dv, dtype);
+  if (need < 0) return (int)need;
+  void* ws = nullptr;
+  if (need > 0) {
+    if ((unsigned long long)need > kda::kNoallocBytes) {
+      char msg[256];
+      snprintf(msg, sizeof(msg),
+               "kda_prefill_chunked_noalloc: this call needs %lld bytes of scratch but the built-in "
+               "scratch holds %llu bytes; split the batch or use kda_prefill_chunked with a workspace",
+               (long long)need, kda::kNoallocBytes);
+      return kda::set_error(KDA_ERR_SHAPE, msg);
+    }
+    int cerr = 0;
+    ws = kda::noalloc_scratch(&cerr);
+    if (ws == nullptr) {
+      char msg[256];
+      snprintf(msg, sizeof(msg), "kda_prefill_chunked_noalloc: scratch address lookup failed: %s",
+               cudaGetErrorString((cudaError_t)cerr));
+      return kda::set_error(KDA_ERR_CUDA, msg);
+    }
+  }
+  return kda_prefill_chunked(S0, q, k, v, g, beta, cu_seqlens, n_seqs, T, H, dk, dv, dtype, chunk,
+                             ckpt_stride, o, S_final, page_pool, page_bytes, ckpt_page_ids, ckpt_pos,
+                             num_ckpt, ws, ws ? (int64_t)kda::kNoallocBytes : 0, mode, stream);
+}

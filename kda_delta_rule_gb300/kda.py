@@ -45,6 +45,7 @@ def _load():
         "kda_num_checkpoints": ([P, I, L, I], L),
         "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, I, P], I),
         "kda_prefill_workspace_bytes": ([P, I, L, I, I, I, I], L),
+        "kda_prefill_chunked_noalloc": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, I, P], I),
         "kda_device_errors": ([ctypes.POINTER(ctypes.c_int)], I),
         "kda_pack_heads": ([P, L, L, P, L, I, I, I, I, P], I),
         "kda_unpack_heads": ([P, P, L, L, I, I, I, I, P], I),
@@ -231,6 +232,36 @@ def kda_prefill_chunked(S0, q, k, v, g, beta, cu_seqlens=None, chunk=64, ckpt_st
                                     _ptr(ckpt_page_ids), _ptr(ckpt_pos), n_ck,
                                     _ptr(workspace), ws_bytes, mode, _stream(stream, dev)),
            "kda_prefill_chunked")
+    return o, S_final
+
+
+def kda_prefill_chunked_noalloc(S0, q, k, v, g, beta, o, S_final, cu_seqlens=None, chunk=64,
+                                ckpt_stride=512, page_pool=None, ckpt_page_ids=None, ckpt_pos=None,
+                                mode=DECAY_FIRST, stream=None):
+    """kda_prefill_chunked for callers that cannot allocate device memory at call time.
+
+    The outputs o and S_final must be passed in (nothing is allocated here, on the
+    host side of the binding either); the tensor-core scratch is the library's
+    fixed built-in device array, so a call needing more than it holds is refused.
+    """
+    T, Hq, dk = q.shape
+    code, _, dv = _projections(q, k, v, g, beta, (T, Hq))
+    arr, N = _cu_array(cu_seqlens)
+    if S0 is not None:
+        _cuda("S0", S0, torch.float32, (N, Hq, dk, dv))
+    _cuda("o", o, q.dtype, (T, Hq, dv))
+    _cuda("S_final", S_final, torch.float32, (N, Hq, dk, dv))
+    base, page_bytes, n_ck = None, 0, 0
+    if ckpt_page_ids is not None:
+        _cuda("ckpt_page_ids", ckpt_page_ids, torch.int32)
+        n_ck = ckpt_page_ids.numel()
+        base, page_bytes = ctypes.c_void_p(page_pool.arena.data_ptr()), page_pool.page_bytes
+    _check(_lib.kda_prefill_chunked_noalloc(_ptr(S0), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                            arr, N, T, Hq, dk, dv, code, chunk, ckpt_stride,
+                                            _ptr(o), _ptr(S_final), base, page_bytes,
+                                            _ptr(ckpt_page_ids), _ptr(ckpt_pos), n_ck, mode,
+                                            _stream(stream, q.device)),
+           "kda_prefill_chunked_noalloc")
     return o, S_final
 
 
