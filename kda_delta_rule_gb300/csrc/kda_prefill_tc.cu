@@ -72,6 +72,10 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
   return u;
 }
 
+__device__ __forceinline__ float sel4(const float (&a)[4], int i) {
+  return i == 0 ? a[0] : (i == 1 ? a[1] : (i == 2 ? a[2] : a[3]));
+}
+
 __device__ __forceinline__ int find_seq(const PrefillSched& s, int chunk) {
   int lo = 0, hi = s.n_seqs - 1;
   while (lo < hi) {                     // last n with chunk_base[n] <= chunk
@@ -124,42 +128,82 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   const int i = tid;
   const int64_t rowq = (int64_t)H * DKT;          // token stride of q, k, g
   const int64_t base_qk = t0 * rowq + (int64_t)h * DKT + i;
-  float Gam[C];
+  // Loads are issued in batches of 16 rows ahead of any store: a store through
+  // one pointer may alias a later load through another, so interleaving them
+  // would serialise one HBM round trip per row.
+  // Pass 1: the block reference values Gamma_m(R) (8th token of each 16-token
+  // block) and Gamma_C (last token).
+  float gm[4], GC;
   {
     float acc = 0.f;
 #pragma unroll
-    for (int r = 0; r < C; ++r) {
-      acc += r < L ? ldf(gg + base_qk + r * rowq) : 0.f;
-      Gam[r] = acc;
+    for (int r0 = 0; r0 < C; r0 += 16) {
+      float gv[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) gv[e] = r0 + e < L ? ldf(gg + base_qk + (r0 + e) * rowq) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        acc += gv[e];
+        if (e == 7) gm[r0 >> 4] = acc;
+      }
     }
+    GC = acc;
   }
-  const float GC = Gam[C - 1];
-  float gm[4], egm[4], egcm[4];
+  float egm[4], egcm[4];
 #pragma unroll
   for (int R = 0; R < 4; ++R) {
-    gm[R] = Gam[16 * R + 7];
     egm[R] = __expf(gm[R]);
     egcm[R] = __expf(GC - gm[R]);
   }
 
+  // Pass 2: the running cumsum again, with every gated operand of the chunk.
   __nv_bfloat16* X = reinterpret_cast<__nv_bfloat16*>(sm + P_R1);          // [64][128]
   __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(sm + P_R1 + 16384);  // [64][128]
+  // swizzle of this thread's column inside a 128-byte row: depends on r % 8 only
+  uint32_t xo[8];
 #pragma unroll
-  for (int r = 0; r < C; ++r) {
-    const int R = r >> 4;
-    const float kr = r < L ? ldf(kg + base_qk + r * rowq) : 0.f;
-    const float qr = r < L ? ldf(qg + base_qk + r * rowq) : 0.f;
-    const float d = Gam[r] - gm[R];
-    const float E = __expf(d), Einv = __expf(-d);
-    const float EG = decay_first ? E : __expf((r ? Gam[r - 1] : 0.f) - gm[R]);
-    st_bf16(sm + P_KHAT, off_k(r, i, 64), kr * Einv);
-    st_bf16(sm + P_KTIL, off_mn(i, r, 64), kr * EG * egm[R]);
-    st_bf16(img + IMG_WQ, off_k(64 + r, i, 128), qr * E * egm[R]);
-    st_bf16(img + IMG_KB, off_mn(i, r, 64), kr * Einv * egcm[R]);
-    X[r * DKT + i] = __float2bfloat16_rn(kr * EG);
-    Y[r * DKT + i] = __float2bfloat16_rn(qr * E);
+  for (int rr = 0; rr < 8; ++rr) xo[rr] = (uint32_t)(rr * 128 + ((((i & 63) >> 3) ^ rr) << 4) + (i & 7) * 2);
+  const uint32_t kblk64 = (uint32_t)(i >> 6) * 64 * 128, kblk128 = (uint32_t)(i >> 6) * 128 * 128;
+  {
+    float acc = 0.f;
+#pragma unroll 1
+    for (int r0 = 0; r0 < C; r0 += 16) {
+      const int R = r0 >> 4;
+      const float gmR = sel4(gm, R), egmR = sel4(egm, R), egcmR = sel4(egcm, R);
+      float gb[16], kb[16], qb[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const bool in = r0 + e < L;
+        const int64_t off = base_qk + (r0 + e) * rowq;
+        gb[e] = in ? ldf(gg + off) : 0.f;
+        kb[e] = in ? ldf(kg + off) : 0.f;
+        qb[e] = in ? ldf(qg + off) : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int r = r0 + e;
+        const float prev = acc;               // Gamma_{r-1}
+        acc += gb[e];                         // Gamma_r
+        const float kr = kb[e], qr = qb[e];
+        const float d = acc - gmR;
+        const float E = __expf(d), Einv = __expf(-d);
+        const float EG = decay_first ? E : __expf(prev - gmR);
+        // K-major offsets of (row r, column i) and MN-major offsets of (mn i, row r)
+        const uint32_t rg = (uint32_t)(r >> 3) * 1024 + xo[r & 7];
+        const uint32_t mn = (uint32_t)(i >> 6) * 64 * 128 + (uint32_t)(r >> 3) * 1024 +
+                            (uint32_t)(r & 7) * 128 + ((((i & 63) >> 3) ^ (r & 7)) << 4) + (i & 7) * 2;
+        st_bf16(sm + P_KHAT, kblk64 + rg, kr * Einv);
+        st_bf16(sm + P_KTIL, mn, kr * EG * egmR);
+        st_bf16(img + IMG_WQ, kblk128 + 8192 + rg, qr * E * egmR);      // row 64 + r
+        st_bf16(img + IMG_KB, mn, kr * Einv * egcmR);
+        X[r * DKT + i] = __float2bfloat16_rn(kr * EG);
+        Y[r * DKT + i] = __float2bfloat16_rn(qr * E);
+      }
+    }
   }
   reinterpret_cast<float*>(img + img_eg(DV))[i] = __expf(GC);
+
+  __syncthreads();            // X and Y rows are read by other threads below
 
   // ---- A and P: one tcgen05 MMA chain per 16-token column block ------------
   const uint32_t apb = smem_u32(sm + P_APB);
@@ -173,7 +217,7 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       if (!ok) break;
     }
     // block-to-block factors e^{Gamma_m(R) - Gamma_m(S)} <= 1 for R >= S
-    const float gmS = S == 0 ? gm[0] : (S == 1 ? gm[1] : (S == 2 ? gm[2] : gm[3]));
+    const float gmS = sel4(gm, S);
     float fR[4];
 #pragma unroll
     for (int R = 0; R < 4; ++R) fR[R] = R >= S ? __expf(gm[R] - gmS) : 0.f;
@@ -212,7 +256,6 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     for (int cb = 0; cb < 4; ++cb) {
       float v[16];
       tmem_ld16(lane_addr + 16 * cb, v);
-      tmem_wait_ld();
       if (warp < 2) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -292,9 +335,14 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     const int j = tid;
     const int64_t rowv = (int64_t)H * DV;
     const int64_t base_v = t0 * rowv + (int64_t)h * DV + j;
-#pragma unroll 8
-    for (int r = 0; r < C; ++r)
-      st_bf16(sm + P_KHAT, off_mn(j, r, 64), r < L ? ldf(vg + base_v + r * rowv) : 0.f);
+#pragma unroll
+    for (int r0 = 0; r0 < C; r0 += 16) {
+      float vb[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) vb[e] = r0 + e < L ? ldf(vg + base_v + (r0 + e) * rowv) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) st_bf16(sm + P_KHAT, off_mn(j, r0 + e, 64), vb[e]);
+    }
   }
   fence_async_smem();
   fence_before();
@@ -321,7 +369,6 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     for (int cb = 0; cb < 8; ++cb) {
       float v[16];
       tmem_ld16(lane_addr + 16 * cb, v);
-      tmem_wait_ld();
 #pragma unroll
       for (int e = 0; e < 16; ++e) v[e] *= -br;
       *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, 16 * cb, 128)) = pack8(v);
@@ -331,7 +378,6 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     for (int cb = 0; cb < DV / 16; ++cb) {
       float v[16];
       tmem_ld16(lane_addr + 128 + 16 * cb, v);
-      tmem_wait_ld();
 #pragma unroll
       for (int e = 0; e < 16; ++e) v[e] *= br;
       const int j = 16 * cb;
@@ -453,15 +499,15 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     if (warp < 2) {                         // Delta' = beta U - beta W S, row r = tid
       const int r = tid;
       const __nv_bfloat16* urow = reinterpret_cast<const __nv_bfloat16*>(st + S_U + r * 128);
+      float v[DVS / 16][16];
+#pragma unroll
+      for (int cb = 0; cb < DVS / 16; ++cb) tmem_ld16(d1 + lane_addr_off + 16 * cb, v[cb]);
 #pragma unroll
       for (int cb = 0; cb < DVS / 16; ++cb) {
-        float v[16];
-        tmem_ld16(d1 + lane_addr_off + 16 * cb, v);
-        tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] += __bfloat162float(urow[16 * cb + e]);
-        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(16 * cb, r, 64)) = pack8(v);
-        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(16 * cb + 8, r, 64)) = pack8(v + 8);
+        for (int e = 0; e < 16; ++e) v[cb][e] += __bfloat162float(urow[16 * cb + e]);
+        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(16 * cb, r, 64)) = pack8(v[cb]);
+        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(16 * cb + 8, r, 64)) = pack8(v[cb] + 8);
       }
     }
     fence_async_smem();
@@ -483,14 +529,13 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
     {
       const float eg = reinterpret_cast<const float*>(st + S_EG)[i];
+      float v[DVS / 16][16];
 #pragma unroll
-      for (int cb = 0; cb < DVS / 16; ++cb) {
-        float v[16];
-        tmem_ld16(d2 + lane_addr_off + 16 * cb, v);
-        tmem_wait_ld();
+      for (int cb = 0; cb < DVS / 16; ++cb) tmem_ld16(d2 + lane_addr_off + 16 * cb, v[cb]);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) S[16 * cb + e] = fmaf(eg, S[16 * cb + e], v[e]);
-      }
+      for (int cb = 0; cb < DVS / 16; ++cb)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) S[16 * cb + e] = fmaf(eg, S[16 * cb + e], v[cb][e]);
 #pragma unroll
       for (int cch = 0; cch < DVS / 8; ++cch)
         *reinterpret_cast<uint4*>(sm + C_SB + off_mn(8 * cch, i, 128)) = pack8(S + 8 * cch);
@@ -499,14 +544,14 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     if (warp >= 2) {                        // outputs: rows 64-127 of d1
       const int r = tid - 64;
       __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0;
+      float v[DVS / 16][16];
 #pragma unroll
-      for (int cb = 0; cb < DVS / 16; ++cb) {
-        float v[16];
-        tmem_ld16(d1 + lane_addr_off + 16 * cb, v);
-        tmem_wait_ld();
-        if (r < L) {
-          *reinterpret_cast<uint4*>(orow + 16 * cb) = pack8(v);
-          *reinterpret_cast<uint4*>(orow + 16 * cb + 8) = pack8(v + 8);
+      for (int cb = 0; cb < DVS / 16; ++cb) tmem_ld16(d1 + lane_addr_off + 16 * cb, v[cb]);
+      if (r < L) {
+#pragma unroll
+        for (int cb = 0; cb < DVS / 16; ++cb) {
+          *reinterpret_cast<uint4*>(orow + 16 * cb) = pack8(v[cb]);
+          *reinterpret_cast<uint4*>(orow + 16 * cb + 8) = pack8(v[cb] + 8);
         }
       }
     }
