@@ -296,6 +296,7 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
     a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
     a.ckpt_stride = ckpt_stride; a.mode = mode;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.T = T;
     status = cuda_status(kda::launch_prefill(a, *sched, max_len, s), "kda_prefill_chunked launch");
   }
   return status;

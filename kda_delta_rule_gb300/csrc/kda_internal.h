@@ -46,6 +46,7 @@ struct PrefillArgs {
   int64_t num_ckpt;              // entries available from the offset
   void* workspace;               // chunk images of the tensor-core path, or nullptr
   int64_t workspace_bytes;
+  int64_t T;                     // tokens in q/k/v/g/beta (all launch groups)
   int H, dk, dv, dtype, chunk, ckpt_stride, mode;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, const PrefillSched& sched, int max_len,

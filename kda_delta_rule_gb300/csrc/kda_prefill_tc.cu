@@ -26,6 +26,8 @@
 // Pairwise decays are split at a reference token per 16-token column block
 // (its 8th token), so every exponential factor stays below e^{8 |g_min|}:
 // finite in bf16/fp32 for g >= -10.
+#include <cuda.h>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_tc.cuh"
@@ -59,7 +61,8 @@ constexpr uint32_t P_KTIL = 50176;      // 16 KB  k e^{G} MN-major (mn = dk, K =
 constexpr uint32_t P_R1 = 66560;        // 32 KB  X, Y bf16 [64][128]; later XT scratch + TOP
 constexpr uint32_t P_TOP = P_R1 + 16384;  // 16 KB [T; 0] K-major [128][64]
 constexpr uint32_t P_MISC = 99328;      // beta fp32[64] | mbar | tmem slot
-constexpr uint32_t P_SMEM = P_MISC + 512 + 1024;
+constexpr uint32_t P_FAC = P_MISC + 512;  // fp32 [4][128]: block-to-block factors of one build
+constexpr uint32_t P_SMEM = P_FAC + 2048 + 1024;
 
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
@@ -91,30 +94,57 @@ __device__ __forceinline__ bool cta_wait(uint32_t mbar, uint32_t parity) {
   return __syncthreads_and(ok) != 0;
 }
 
+// 2-D tiled TMA load (tile mode) into shared memory, completion on mbar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(mbar) : "memory");
+}
+
+// Tensor maps of one prefill launch: k and q as [T][H*128] with a plain
+// 128 x 64 box (a chunk's rows of one head, row-major in shared memory); v as
+// [T][H*DV] with a 64 x 64 box and 128-byte swizzle, which lands exactly in the
+// MN-major operand layout the U = T V contraction reads.
+struct PrepMaps {
+  CUtensorMap k, q, v;
+};
+
 template <int DV>
 __global__ void __launch_bounds__(NT, 2)
-kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned char* __restrict__ ws) {
+kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned char* __restrict__ ws,
+                      const __grid_constant__ PrepMaps maps) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   float* s_beta = reinterpret_cast<float*>(sm + P_MISC);
-  const uint32_t mbar = smem_u32(sm + P_MISC + 256);
+  float* s_fac = reinterpret_cast<float*>(sm + P_FAC);
+  const uint32_t mbar = smem_u32(sm + P_MISC + 256);       // tensor-core commits
+  const uint32_t mbar_in = smem_u32(sm + P_MISC + 272);    // k and q tiles
+  const uint32_t mbar_v = smem_u32(sm + P_MISC + 280);     // v tile
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_MISC + 264);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int chunk = blockIdx.x, h = blockIdx.y, H = a.H;
+  // heads vary fastest across the grid: CTAs running together read whole token rows
+  const int H = a.H;
+  const int h = (int)(blockIdx.x % (unsigned)H), chunk = (int)(blockIdx.x / (unsigned)H);
   const int n = find_seq(sched, chunk);
   const int c = chunk - sched.chunk_base[n];
   const int64_t t0 = (int64_t)sched.start[n] + (int64_t)c * C;
   const int L = min(C, sched.len[n] - c * C);
   const bool decay_first = a.mode == KDA_MODE_DECAY_FIRST;
   unsigned char* img = ws + ((int64_t)chunk * H + h) * img_bytes(DV);
-  const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* kg = reinterpret_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* gg = reinterpret_cast<const __nv_bfloat16*>(a.g);
-  const __nv_bfloat16* vg = reinterpret_cast<const __nv_bfloat16*>(a.v);
   const __nv_bfloat16* bg = reinterpret_cast<const __nv_bfloat16*>(a.beta);
 
-  if (tid == 0) { mbar_init(mbar, 1); mbar_init_fence(); }
+  if (tid == 0) {
+    mbar_init(mbar, 1);
+    mbar_init(mbar_in, 1);
+    mbar_init(mbar_v, 1);
+    mbar_init_fence();
+    // raw k and q tiles of this (chunk, head) into the A/P buffer, idle until the first build
+    mbar_expect_tx(mbar_in, 2 * 16384);
+    tma_load_2d(smem_u32(sm + P_APB), &maps.k, h * DKT, (int)t0, mbar_in);
+    tma_load_2d(smem_u32(sm + P_APB + 16384), &maps.q, h * DKT, (int)t0, mbar_in);
+  }
   if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
   if (tid < C) s_beta[tid] = tid < L ? ldf(bg + (t0 + tid) * H + h) : 0.f;
   fence_before();
@@ -131,21 +161,18 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   // Loads are issued in batches of 16 rows ahead of any store: a store through
   // one pointer may alias a later load through another, so interleaving them
   // would serialise one HBM round trip per row.
-  // Pass 1: the block reference values Gamma_m(R) (8th token of each 16-token
-  // block) and Gamma_C (last token).
+  // Pass 1: all 64 gates of this channel in one batch of loads; the block
+  // reference values Gamma_m(R) (8th token of each 16-token block) and Gamma_C.
+  float gall[C];
+#pragma unroll
+  for (int r = 0; r < C; ++r) gall[r] = r < L ? ldf(gg + base_qk + r * rowq) : 0.f;
   float gm[4], GC;
   {
     float acc = 0.f;
 #pragma unroll
-    for (int r0 = 0; r0 < C; r0 += 16) {
-      float gv[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) gv[e] = r0 + e < L ? ldf(gg + base_qk + (r0 + e) * rowq) : 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        acc += gv[e];
-        if (e == 7) gm[r0 >> 4] = acc;
-      }
+    for (int r = 0; r < C; ++r) {
+      acc += gall[r];
+      if ((r & 15) == 7) gm[r >> 4] = acc;
     }
     GC = acc;
   }
@@ -156,35 +183,31 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     egcm[R] = __expf(GC - gm[R]);
   }
 
-  // Pass 2: the running cumsum again, with every gated operand of the chunk.
+  // Pass 2: the running cumsum again, with every gated operand of the chunk;
+  // k and q of the next 16 rows are loaded while the current 16 are processed.
   __nv_bfloat16* X = reinterpret_cast<__nv_bfloat16*>(sm + P_R1);          // [64][128]
   __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(sm + P_R1 + 16384);  // [64][128]
-  // swizzle of this thread's column inside a 128-byte row: depends on r % 8 only
   uint32_t xo[8];
 #pragma unroll
   for (int rr = 0; rr < 8; ++rr) xo[rr] = (uint32_t)(rr * 128 + ((((i & 63) >> 3) ^ rr) << 4) + (i & 7) * 2);
   const uint32_t kblk64 = (uint32_t)(i >> 6) * 64 * 128, kblk128 = (uint32_t)(i >> 6) * 128 * 128;
+  ok = cta_wait(mbar_in, 0);
+  const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_APB);           // [64][128]
+  const __nv_bfloat16* qraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_APB + 16384);   // [64][128]
   {
     float acc = 0.f;
-#pragma unroll 1
-    for (int r0 = 0; r0 < C; r0 += 16) {
-      const int R = r0 >> 4;
-      const float gmR = sel4(gm, R), egmR = sel4(egm, R), egcmR = sel4(egcm, R);
-      float gb[16], kb[16], qb[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const bool in = r0 + e < L;
-        const int64_t off = base_qk + (r0 + e) * rowq;
-        gb[e] = in ? ldf(gg + off) : 0.f;
-        kb[e] = in ? ldf(kg + off) : 0.f;
-        qb[e] = in ? ldf(qg + off) : 0.f;
-      }
+    for (int R = 0; R < 4; ++R) {
+      const int r0 = 16 * R;
+      const float gmR = gm[R], egmR = egm[R], egcmR = egcm[R];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int r = r0 + e;
         const float prev = acc;               // Gamma_{r-1}
-        acc += gb[e];                         // Gamma_r
-        const float kr = kb[e], qr = qb[e];
+        acc += gall[r];                       // Gamma_r
+        // rows past the sequence end come from the next sequence (or fill): masked
+        const float kr = r < L ? __bfloat162float(kraw[r * DKT + i]) : 0.f;
+        const float qr = r < L ? __bfloat162float(qraw[r * DKT + i]) : 0.f;
         const float d = acc - gmR;
         const float E = __expf(d), Einv = __expf(-d);
         const float EG = decay_first ? E : __expf(prev - gmR);
@@ -221,17 +244,30 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     float fR[4];
 #pragma unroll
     for (int R = 0; R < 4; ++R) fR[R] = R >= S ? __expf(gm[R] - gmS) : 0.f;
+    // The factors are per key channel: publish them so that the 16-byte chunks
+    // below (8 channels of one row each) scale every channel by its own factor.
 #pragma unroll
-    for (int r = 0; r < C; ++r) {
-      const int R = r >> 4;
-      float xs = 0.f, ys = 0.f;
-      if (R >= S) {
-        const float f = fR[R];
-        xs = __bfloat162float(X[r * DKT + i]) * f;
-        ys = __bfloat162float(Y[r * DKT + i]) * f;
+    for (int R = 0; R < 4; ++R) s_fac[R * DKT + i] = fR[R];
+    __syncthreads();
+    // 16-byte chunks: (row r, channels 8cc..8cc+7) of X (rows 0-63) and Y (rows 64-127)
+#pragma unroll 4
+    for (int e = tid; e < 2 * C * 16; e += NT) {
+      const int half = e >> 10, r = (e >> 4) & 63, cc = e & 15;
+      const float* fc = s_fac + (r >> 4) * DKT + 8 * cc;
+      const float4 f0 = *reinterpret_cast<const float4*>(fc);
+      const float4 f1 = *reinterpret_cast<const float4*>(fc + 4);
+      const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+      const __nv_bfloat16* src = (half ? Y : X) + r * DKT + 8 * cc;
+      const uint4 raw = *reinterpret_cast<const uint4*>(src);
+      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      float v8[8];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 x = __bfloat1622float2(pr[t]);
+        v8[2 * t] = x.x * f[2 * t];
+        v8[2 * t + 1] = x.y * f[2 * t + 1];
       }
-      st_bf16(sm + P_APB, off_k(r, i, 128), xs);
-      st_bf16(sm + P_APB, off_k(64 + r, i, 128), ys);
+      *reinterpret_cast<uint4*>(sm + P_APB + off_k(64 * half + r, 8 * cc, 128)) = pack8(v8);
     }
     fence_async_smem();
     fence_before();
@@ -245,6 +281,14 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     }
   }
   if (ok) { ok = cta_wait(mbar, phase); phase ^= 1; fence_after(); }
+  // the A/P products are done with Khat: bring v into its place (MN-major, swizzled)
+  const bool v_issued = ok;
+  if (ok && tid == 0) {
+    mbar_expect_tx(mbar_v, 64 * DV * 2);
+#pragma unroll
+    for (int b = 0; b < DV / 64; ++b)
+      tma_load_2d(smem_u32(sm + P_KHAT + b * 8192), &maps.v, h * DV + 64 * b, (int)t0, mbar_v);
+  }
 
   // ---- read A (lanes 0-63) and P (lanes 64-127) ----------------------------
   float* AF = reinterpret_cast<float*>(sm + P_APB);            // [64][65]
@@ -253,25 +297,25 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     const int r = tid & 63;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
-      float v[16];
-      tmem_ld16(lane_addr + 16 * cb, v);
+    for (int hb = 0; hb < 2; ++hb) {
+      float v[32];
+      tmem_ld32(lane_addr + 32 * hb, v);
       if (warp < 2) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int s = 16 * cb + e;
+        for (int e = 0; e < 32; ++e) {
+          const int s = 32 * hb + e;
           AF[r * 65 + s] = s < r ? s_beta[s] * v[e] : 0.f;
         }
       } else {
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
+        for (int q8 = 0; q8 < 4; ++q8) {
           float p8[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int s = 16 * cb + 8 * hlf + e;
-            p8[e] = s <= r ? v[8 * hlf + e] : 0.f;
+            const int s = 32 * hb + 8 * q8 + e;
+            p8[e] = s <= r ? v[8 * q8 + e] : 0.f;
           }
-          *reinterpret_cast<uint4*>(img + IMG_P + off_k(r, 16 * cb + 8 * hlf, 64)) = pack8(p8);
+          *reinterpret_cast<uint4*>(img + IMG_P + off_k(r, 32 * hb + 8 * q8, 64)) = pack8(p8);
         }
       }
     }
@@ -331,23 +375,11 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       *reinterpret_cast<uint4*>(sm + P_TOP + off_k(r, 8 * cch, 128)) = pack8(t8);
     }
   }
-  if (tid < DV) {
-    const int j = tid;
-    const int64_t rowv = (int64_t)H * DV;
-    const int64_t base_v = t0 * rowv + (int64_t)h * DV + j;
-#pragma unroll
-    for (int r0 = 0; r0 < C; r0 += 16) {
-      float vb[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) vb[e] = r0 + e < L ? ldf(vg + base_v + (r0 + e) * rowv) : 0.f;
-#pragma unroll
-      for (int e = 0; e < 16; ++e) st_bf16(sm + P_KHAT, off_mn(j, r0 + e, 64), vb[e]);
-    }
-  }
   fence_async_smem();
   fence_before();
   __syncthreads();
   fence_after();
+  if (ok) ok = cta_wait(mbar_v, 0);     // v rows past the sequence end meet beta = 0
   if (ok && tid == 0) {
     const uint32_t top = smem_u32(sm + P_TOP);
     constexpr uint32_t ID_W = idesc_bf16(128, 128, false, true);
@@ -385,9 +417,11 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       *reinterpret_cast<uint4*>(dst) = pack8(v);
       *reinterpret_cast<uint4*>(dst + 16) = pack8(v + 8);
     }
-  } else if (ok && warp >= 2) {
-    // lanes 64-127 hold the zero rows of [T; 0]: nothing to read, but the
-    // warp-collective loads are not needed either.
+  }
+  if (!ok && tid == 0) {
+    // leave no bulk copy in flight into this CTA's shared memory (bounded waits)
+    mbar_wait(mbar_in, 0);
+    if (v_issued) mbar_wait(mbar_v, 0);
   }
   fence_before();
   __syncthreads();
@@ -591,15 +625,49 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// [T][cols] bf16 tensor map with a box of box_x columns x 64 rows
+bool make_map(CUtensorMap* m, const void* base, int64_t T, int64_t cols, int box_x, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)T};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_x, 64};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DV>
 cudaError_t launch_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned char* ws, int total_chunks,
                       cudaStream_t s) {
   cudaError_t e;
   if (total_chunks > 0) {
+    PrepMaps maps;
+    if (!make_map(&maps.k, a.k, a.T, (int64_t)a.H * DKT, DKT, false) ||
+        !make_map(&maps.q, a.q, a.T, (int64_t)a.H * DKT, DKT, false) ||
+        !make_map(&maps.v, a.v, a.T, (int64_t)a.H * DV, 64, true))
+      return cudaErrorInvalidValue;
     auto prep = kda_chunk_prep_kernel<DV>;
     e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
     if (e != cudaSuccess) return e;
-    prep<<<dim3(total_chunks, a.H), NT, P_SMEM, s>>>(a, sched, ws);
+    prep<<<(unsigned)((int64_t)a.H * total_chunks), NT, P_SMEM, s>>>(a, sched, ws, maps);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   auto chain = kda_chain_kernel<DV>;
