@@ -19,6 +19,8 @@ bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
+import hashlib
 import json
 import os
 import statistics
@@ -47,6 +49,21 @@ WORKLOAD = (f"kda_prefill_chunked long single sequence: B=1 H={H} dk=dv={DK} T={
             f"fp32-state chunk={CHUNK} ckpt_stride={STRIDE} (16 checkpoint pages)")
 
 
+# DRAM bytes (read + write) of one prefill call measured by ncu on the T=8192 H=32 d=128
+# case (profiles/prefill_long_T8192_H32_d128_bf16.md), valid only for the kernel source it
+# was taken on: reported as null once kda_prefill_tc.cu changes.
+PREFILL_TRAFFIC = {"3d7764903a733fbe": 907_673_600}
+
+
+def prefill_traffic():
+    path = os.path.join(ROOT, "kda_delta_rule_gb300", "csrc", "kda_prefill_tc.cu")
+    try:
+        digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return PREFILL_TRAFFIC.get(digest)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -70,58 +87,99 @@ def prefill_flops(T_, H_, dk, dv, C=CHUNK):
 
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during a region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clocks and clock-event reasons sampled during a region (reads only).
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
+    NVML through ctypes, every 2 ms, on the GPU with the same PCI bus id as the
+    CUDA device; nvidia-smi every 200 ms if NVML cannot be loaded.
+    """
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, dev: torch.device, interval=0.002):
+        self.dev = dev
+        self.interval = interval
+        self.samples = []          # (sm_mhz, max_mhz, reasons bitmask)
+        self.stop = threading.Event()
+        self.thread = None
         self.proc = None
         self.lines = []
 
+    def _nvml_handle(self):
+        nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if nvml.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.dev)
+        bus = getattr(props, "pci_bus_id", None)
+        if bus is not None:
+            busid = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), bus,
+                                         getattr(props, "pci_device_id", 0))
+            if nvml.nvmlDeviceGetHandleByPciBusId_v2(busid.encode(), ctypes.byref(h)) == 0:
+                return nvml, h
+        if nvml.nvmlDeviceGetHandleByIndex_v2(self.dev.index or 0, ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        return nvml, h
+
+    def _run_nvml(self, nvml, h):
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_rs = getattr(nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop.is_set():
+            if nvml.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and \
+                    get_rs(h, ctypes.byref(rs)) == 0:
+                self.samples.append((clk.value, mx.value, rs.value))
+            time.sleep(self.interval)
+
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
+            nvml, h = self._nvml_handle()
+            self.thread = threading.Thread(target=self._run_nvml, args=(nvml, h), daemon=True)
+            self.thread.start()
         except Exception:
-            self.proc = None
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev.index or 0}", f"--query-gpu={q}",
+                                              "--format=csv,noheader,nounits", "-lms", "200"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.thread = threading.Thread(target=self._read_smi, daemon=True)
+                self.thread.start()
+            except Exception:
+                self.proc = None
+        time.sleep(3 * self.interval)     # first samples before the region starts
         return self
 
-    def _read(self):
+    def _read_smi(self):
+        bits = [0x8, 0x40, 0x20, 0x4]
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                mask = sum(b for b, v in zip(bits, parts[2:6]) if v.lower().startswith("active"))
+                self.samples.append((float(parts[0]), float(parts[1]), mask))
+            except (ValueError, IndexError):
+                continue
 
     def __exit__(self, *exc):
+        time.sleep(2 * self.interval)
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set()
+        for _, _, m in self.samples:
+            for bit, name in self.REASONS.items():
+                if m & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "reasons": sorted(reasons),
+                "samples": len(self.samples)}
 
 
 # ---------------------------------------------------------------------------
@@ -151,7 +209,7 @@ def bench_prefill(K, dev, steps, warmup, rank):
            for _ in range(steps)]
     D.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index or 0) as clk:
+    with ClockSampler(dev) as clk:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
@@ -371,8 +429,9 @@ def main():
             "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T,
                        "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (336 MB/step)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": None, "peak_source": src,
-                         "kernel": "kda_prefill", "kernel_ms": kern_avg_ms,
+                         "frac": achieved / hbm, "traffic": prefill_traffic(), "peak_source": src,
+                         "kernel": "kda_prefill (chunk prep + chain kernels of one call)",
+                         "kernel_ms": kern_avg_ms,
                          "algorithmic_bytes": r["bytes_step"],
                          "tc_tflops": flops / (kern_avg_ms / 1e3) / 1e12,
                          "tc_frac": flops / (kern_avg_ms / 1e3) / 1e12 / tf},
