@@ -48,7 +48,7 @@ constexpr int NT = 128;
 // WQ: K-major [128 rows][128]: rows 0-63 = -beta W, rows 64-127 = q e^{Gamma}
 // KB: MN-major (mn = dk, K = 64 tokens): k e^{Gamma_C - Gamma}
 // P : K-major [64 rows][64]: P (masked)
-// U : [dv/64][64 rows][64] row-major bf16: beta U
+// U : [dv/64][64 rows][64] bf16: beta U, 16-byte chunk c of row r at c ^ (r % 8)
 // EG: fp32[128]: e^{Gamma_C}
 constexpr uint32_t IMG_WQ = 0, IMG_KB = 32768, IMG_P = 49152, IMG_U = 57344;
 __host__ __device__ constexpr uint32_t img_eg(int dv) { return IMG_U + 64u * dv * 2u; }
@@ -101,12 +101,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(mbar) : "memory");
 }
 
-// Tensor maps of one prefill launch: k and q as [T][H*128] with a plain
+// Tensor maps of one prefill launch: k, q and g as [T][H*128] with a plain
 // 128 x 64 box (a chunk's rows of one head, row-major in shared memory); v as
 // [T][H*DV] with a 64 x 64 box and 128-byte swizzle, which lands exactly in the
 // MN-major operand layout the U = T V contraction reads.
 struct PrepMaps {
-  CUtensorMap k, q, v;
+  CUtensorMap k, q, g, v;
 };
 
 template <int DV>
@@ -132,7 +132,6 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   const int L = min(C, sched.len[n] - c * C);
   const bool decay_first = a.mode == KDA_MODE_DECAY_FIRST;
   unsigned char* img = ws + ((int64_t)chunk * H + h) * img_bytes(DV);
-  const __nv_bfloat16* gg = reinterpret_cast<const __nv_bfloat16*>(a.g);
   const __nv_bfloat16* bg = reinterpret_cast<const __nv_bfloat16*>(a.beta);
 
   if (tid == 0) {
@@ -140,10 +139,14 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     mbar_init(mbar_in, 1);
     mbar_init(mbar_v, 1);
     mbar_init_fence();
-    // raw k and q tiles of this (chunk, head) into the A/P buffer, idle until the first build
-    mbar_expect_tx(mbar_in, 2 * 16384);
+    // raw k and q tiles of this (chunk, head) into the A/P buffer, idle until the
+    // first build; the g tile into the Y buffer: thread i reads g[r][i] into a
+    // register before it writes Y[r][i] at the same address, and no other thread
+    // touches either.
+    mbar_expect_tx(mbar_in, 3 * 16384);
     tma_load_2d(smem_u32(sm + P_APB), &maps.k, h * DKT, (int)t0, mbar_in);
     tma_load_2d(smem_u32(sm + P_APB + 16384), &maps.q, h * DKT, (int)t0, mbar_in);
+    tma_load_2d(smem_u32(sm + P_R1 + 16384), &maps.g, h * DKT, (int)t0, mbar_in);
   }
   if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
   if (tid < C) s_beta[tid] = tid < L ? ldf(bg + (t0 + tid) * H + h) : 0.f;
@@ -156,16 +159,13 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 
   // ---- gates: thread i owns key channel i ----------------------------------
   const int i = tid;
-  const int64_t rowq = (int64_t)H * DKT;          // token stride of q, k, g
-  const int64_t base_qk = t0 * rowq + (int64_t)h * DKT + i;
-  // Loads are issued in batches of 16 rows ahead of any store: a store through
-  // one pointer may alias a later load through another, so interleaving them
-  // would serialise one HBM round trip per row.
-  // Pass 1: all 64 gates of this channel in one batch of loads; the block
-  // reference values Gamma_m(R) (8th token of each 16-token block) and Gamma_C.
+  // Pass 1: the block reference values Gamma_m(R) (8th token of each 16-token
+  // block) and Gamma_C (last token), from the g tile the TMA brought in.
+  ok = cta_wait(mbar_in, 0);
+  const __nv_bfloat16* graw = reinterpret_cast<const __nv_bfloat16*>(sm + P_R1 + 16384);   // [64][128]
   float gall[C];
 #pragma unroll
-  for (int r = 0; r < C; ++r) gall[r] = r < L ? ldf(gg + base_qk + r * rowq) : 0.f;
+  for (int r = 0; r < C; ++r) gall[r] = r < L ? __bfloat162float(graw[r * DKT + i]) : 0.f;
   float gm[4], GC;
   {
     float acc = 0.f;
@@ -191,7 +191,6 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 #pragma unroll
   for (int rr = 0; rr < 8; ++rr) xo[rr] = (uint32_t)(rr * 128 + ((((i & 63) >> 3) ^ rr) << 4) + (i & 7) * 2);
   const uint32_t kblk64 = (uint32_t)(i >> 6) * 64 * 128, kblk128 = (uint32_t)(i >> 6) * 128 * 128;
-  ok = cta_wait(mbar_in, 0);
   const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_APB);           // [64][128]
   const __nv_bfloat16* qraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_APB + 16384);   // [64][128]
   {
@@ -412,10 +411,13 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       tmem_ld16(lane_addr + 128 + 16 * cb, v);
 #pragma unroll
       for (int e = 0; e < 16; ++e) v[e] *= br;
+      // row r of each 64-column block: 16-byte chunk c at position c ^ (r % 8), so the
+      // chain's row-per-thread reads hit distinct banks
       const int j = 16 * cb;
-      unsigned char* dst = img + IMG_U + (j >> 6) * 8192 + r * 128 + (j & 63) * 2;
-      *reinterpret_cast<uint4*>(dst) = pack8(v);
-      *reinterpret_cast<uint4*>(dst + 16) = pack8(v + 8);
+      unsigned char* blk = img + IMG_U + (j >> 6) * 8192 + r * 128;
+      const int c0 = (j & 63) >> 3;
+      *reinterpret_cast<uint4*>(blk + (((c0) ^ (r & 7)) << 4)) = pack8(v);
+      *reinterpret_cast<uint4*>(blk + (((c0 + 1) ^ (r & 7)) << 4)) = pack8(v + 8);
     }
   }
   if (!ok && tid == 0) {
@@ -463,7 +465,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     mbar_init(mma_bar, 1);
     mbar_init_fence();
   }
-  if (warp == 0) tmem_alloc(smem_u32(tslot), 128);
+  if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
   // zero rows 0-63 of both [0; P] buffers (never written by the copies)
   for (int e = tid; e < 2 * 512; e += NT) {
     const int s = e >> 9, o = e & 511;
@@ -486,7 +488,8 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t d1 = tmem, d2 = tmem + 64;
+  // TMEM: two output/WS accumulators (one per chunk parity) and the state update
+  const uint32_t d2 = tmem + 128;          // d1 of chunk c: tmem + 64 * (c & 1)
 
   auto issue = [&](int cidx) {
     const int s = cidx & 1;
@@ -500,48 +503,64 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     bulk_g2s(dst + S_U, src + IMG_U + sl * 8192, 8192, fb);
     bulk_g2s(dst + S_EG, src + img_eg(DV), 512, fb);
   };
-  if (tid == 0) {
-    if (nch > 0) issue(0);
-    if (nch > 1) issue(1);
-  }
-
   constexpr uint32_t ID_1 = idesc_bf16(128, DVS, false, true);   // [-bW; Qt] (K-major) x S (MN-major)
   constexpr uint32_t ID_3 = idesc_bf16(128, DVS, true, true);    // Kbar^T (MN-major) x Delta' (MN-major)
   const uint32_t delta = smem_u32(sm + C_DELTA), sb = smem_u32(sm + C_SB);
-  uint32_t mph = 0;
+  auto issue_mma1 = [&](int cidx) {                                // thread 0 only
+    const uint32_t wq = smem_u32(sm + (cidx & 1) * STAGE + S_WQ);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mma(tmem + 64u * (cidx & 1), desc_k(wq, 128, j), desc_mn(sb, 128, j), ID_1, j > 0);
+    mma_commit(mma_bar);
+  };
   bool ok = true;
-  int issued = nch < 2 ? nch : 2, waited = 0;
+  bool tok = true;                          // thread 0's own waits; joined in block votes
+  bool mma_pending = false;                 // thread 0: a commit not yet waited for
+  if (tid == 0 && nch > 0) {
+    issue(0);
+    if (nch > 1) issue(1);
+    tok = mbar_wait(full0, 0);            // chunk 0's images, then its first product
+    if (tok) { issue_mma1(0); mma_pending = true; }
+  }
+  uint32_t mph = 0;
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
-  const uint32_t lane_addr_off = (uint32_t)(32 * warp) << 16;
+  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
 
-  for (int c = 0; c < nch && ok; ++c) {
+  // Per chunk c: MMA1(c) was issued at the end of chunk c-1 (or above).
+  //   Delta' = bU + (-bW S)             (warps 0-1, rows 0-63 of d1[c&1])
+  //   MMA2: d1[c&1] rows 64-127 += P Delta';  MMA3: d2 = Kbar^T Delta'
+  //   S <- e^{Gamma_C} S + d2; S as bf16 for the next MMA1; checkpoints
+  //   issue MMA1(c+1) into d1[(c+1)&1], then write the outputs of chunk c
+  //   from d1[c&1] rows 64-127 (warps 2-3) while it runs.
+  int c = 0;
+  for (; c < nch && ok; ++c) {
     const int s = c & 1;
     unsigned char* st = sm + s * STAGE;
-    ok = cta_wait(full0 + 8 * s, (c >> 1) & 1);
-    ++waited;
+    const uint32_t d1 = tmem + 64u * s;
+    ok = __syncthreads_and(tok) != 0;               // MMA1(c) was issued
     if (!ok) break;
-    if (tid == 0) {
-      const uint32_t wq = smem_u32(st + S_WQ);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) mma(d1, desc_k(wq, 128, j), desc_mn(sb, 128, j), ID_1, j > 0);
-      mma_commit(mma_bar);
-    }
-    ok = cta_wait(mma_bar, mph);
+    bool w = mbar_wait(full0 + 8 * s, (c >> 1) & 1);  // already complete: acquires the images
+    w = mbar_wait(mma_bar, mph) && w;
+    ok = __syncthreads_and(w) != 0;
     mph ^= 1;
+    mma_pending = false;
     fence_after();
     if (!ok) break;
     if (warp < 2) {                         // Delta' = beta U - beta W S, row r = tid
       const int r = tid;
-      const __nv_bfloat16* urow = reinterpret_cast<const __nv_bfloat16*>(st + S_U + r * 128);
-      float v[DVS / 16][16];
+      float v[DVS];
+      tmem_ld64(d1 + lane_off, v);
+      const uint4* urow = reinterpret_cast<const uint4*>(st + S_U + r * 128);
 #pragma unroll
-      for (int cb = 0; cb < DVS / 16; ++cb) tmem_ld16(d1 + lane_addr_off + 16 * cb, v[cb]);
+      for (int cc = 0; cc < DVS / 8; ++cc) {
+        const uint4 u = urow[cc ^ (r & 7)];
+        const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-      for (int cb = 0; cb < DVS / 16; ++cb) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[cb][e] += __bfloat162float(urow[16 * cb + e]);
-        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(16 * cb, r, 64)) = pack8(v[cb]);
-        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(16 * cb + 8, r, 64)) = pack8(v[cb] + 8);
+        for (int t = 0; t < 4; ++t) {
+          const float2 x = __bfloat1622float2(pu[t]);
+          v[8 * cc + 2 * t] += x.x;
+          v[8 * cc + 2 * t + 1] += x.y;
+        }
+        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(8 * cc, r, 64)) = pack8(v + 8 * cc);
       }
     }
     fence_async_smem();
@@ -551,9 +570,9 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     if (tid == 0) {
       const uint32_t pb = smem_u32(st + S_PB), kb = smem_u32(st + S_KB);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) mma(d1, desc_k(pb, 128, j), desc_mn(delta, 64, j), ID_1, 1);
-#pragma unroll
       for (int j = 0; j < 4; ++j) mma(d2, desc_mn(kb, 64, j), desc_mn(delta, 64, j), ID_3, j > 0);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma(d1, desc_k(pb, 128, j), desc_mn(delta, 64, j), ID_1, 1);
       mma_commit(mma_bar);
     }
     ok = cta_wait(mma_bar, mph);
@@ -563,32 +582,15 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
     {
       const float eg = reinterpret_cast<const float*>(st + S_EG)[i];
-      float v[DVS / 16][16];
+      float v[DVS];
+      tmem_ld64(d2 + lane_off, v);
 #pragma unroll
-      for (int cb = 0; cb < DVS / 16; ++cb) tmem_ld16(d2 + lane_addr_off + 16 * cb, v[cb]);
-#pragma unroll
-      for (int cb = 0; cb < DVS / 16; ++cb)
-#pragma unroll
-        for (int e = 0; e < 16; ++e) S[16 * cb + e] = fmaf(eg, S[16 * cb + e], v[cb][e]);
+      for (int j = 0; j < DVS; ++j) S[j] = fmaf(eg, S[j], v[j]);
 #pragma unroll
       for (int cch = 0; cch < DVS / 8; ++cch)
         *reinterpret_cast<uint4*>(sm + C_SB + off_mn(8 * cch, i, 128)) = pack8(S + 8 * cch);
     }
     const int L = min(C, len - c * C);
-    if (warp >= 2) {                        // outputs: rows 64-127 of d1
-      const int r = tid - 64;
-      __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0;
-      float v[DVS / 16][16];
-#pragma unroll
-      for (int cb = 0; cb < DVS / 16; ++cb) tmem_ld16(d1 + lane_addr_off + 16 * cb, v[cb]);
-      if (r < L) {
-#pragma unroll
-        for (int cb = 0; cb < DVS / 16; ++cb) {
-          *reinterpret_cast<uint4*>(orow + 16 * cb) = pack8(v[cb]);
-          *reinterpret_cast<uint4*>(orow + 16 * cb + 8) = pack8(v[cb] + 8);
-        }
-      }
-    }
     const int pos = c * C + L;
     if (a.ckpt_stride > 0 && pos % a.ckpt_stride == 0) {
       const int64_t idx = (int64_t)sched.ckpt_base[n] + pos / a.ckpt_stride - 1;
@@ -608,11 +610,31 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     fence_before();
     __syncthreads();
     fence_after();
-    if (tid == 0 && c + 2 < nch) { issue(c + 2); ++issued; }
+    if (tid == 0 && c + 1 < nch) {
+      tok = mbar_wait(full0 + 8 * ((c + 1) & 1), ((c + 1) >> 1) & 1);
+      if (tok) { issue_mma1(c + 1); mma_pending = true; }
+    }
+    // stage s is free (MMA2/3 of chunk c are done): warp 2 fetches chunk c + 2 into it
+    if (tid == 64 && c + 2 < nch) issue(c + 2);
+    if (warp >= 2) {                        // outputs of chunk c: rows 64-127 of d1[c&1]
+      const int r = tid - 64;
+      float v[DVS];
+      tmem_ld64(d1 + lane_off, v);
+      if (r < L) {
+        __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0;
+#pragma unroll
+        for (int cc = 0; cc < DVS / 8; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(v + 8 * cc);
+      }
+    }
   }
+  ok = __syncthreads_and(ok && tok) != 0;
   if (!ok && tid == 0) {
-    // drain copies still in flight before leaving (bounded)
-    for (int c = waited; c < issued; ++c) mbar_wait(full0 + 8 * (c & 1), (c >> 1) & 1);
+    // Drain what may still be in flight before leaving (bounded waits): the
+    // image copies of the chunks after the one that stopped (issued up to two
+    // ahead) and a product whose commit was not waited for.
+    const int last = min(nch, c + 2);
+    for (int cc = c; cc < last; ++cc) mbar_wait(full0 + 8 * (cc & 1), (cc >> 1) & 1);
+    if (mma_pending) mbar_wait(mma_bar, mph);
   }
   if (ok) {
     float* dst = a.S_final + (((int64_t)n * H + h) * DKT + i) * DV + col0;
@@ -622,7 +644,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 128);
+  if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -662,6 +684,7 @@ cudaError_t launch_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned 
     PrepMaps maps;
     if (!make_map(&maps.k, a.k, a.T, (int64_t)a.H * DKT, DKT, false) ||
         !make_map(&maps.q, a.q, a.T, (int64_t)a.H * DKT, DKT, false) ||
+        !make_map(&maps.g, a.g, a.T, (int64_t)a.H * DKT, DKT, false) ||
         !make_map(&maps.v, a.v, a.T, (int64_t)a.H * DV, 64, true))
       return cudaErrorInvalidValue;
     auto prep = kda_chunk_prep_kernel<DV>;
