@@ -49,11 +49,12 @@ __host__ __device__ constexpr size_t step_smem_floats(int steps) {
   return (size_t)steps * C::STAGE + kqw_floats(steps, NW) + 2 * (size_t)NW * C::RED;
 }
 
-template <int DK, int DV, int NW, int HPC, typename T>
+template <int DK, int DV, int NW, int HPC, int MAXS, typename T>
 __global__ void __launch_bounds__(32 * NW * HPC)
 kda_step_kernel(const StepArgs a) {
   using C = StepCfg<DK, DV, NW>;
   constexpr int NT = C::NT, TPR = C::TPR, RG = C::RG, RPT = C::RPT;
+  constexpr int EK = (DK + NT - 1) / NT, EV = (DV + NT - 1) / NT;   // channels per thread
 
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
@@ -95,23 +96,54 @@ kda_step_kernel(const StepArgs a) {
   const T* v = reinterpret_cast<const T*>(a.v);
   const T* g = reinterpret_cast<const T*>(a.g);
   const T* beta = reinterpret_cast<const T*>(a.beta);
-  for (int s = 0; s < n; ++s) {
-    const int64_t hs = (int64_t)s * nheads + head;      // (step, b, h) flattened
-    float* st = stage + (size_t)s * C::STAGE;
-    float kq = 0.f;
-    for (int i = tid; i < DK; i += NT) {
-      float ki = active ? to_f32(k[hs * DK + i]) : 0.f;
-      float qi = active ? to_f32(q[hs * DK + i]) : 0.f;
-      st[i] = ki;
-      st[DK + i] = qi;
-      st[2 * DK + i] = active ? expf(to_f32(g[hs * DK + i])) : 1.f;
-      kq = fmaf(ki, qi, kq);
-    }
-    for (int j = tid; j < DV; j += NT) st[3 * DK + j] = active ? to_f32(v[hs * DV + j]) : 0.f;
-    if (tid == 0) st[3 * DK + DV] = active ? to_f32(beta[hs]) : 0.f;
+  // All steps' loads are issued before any is used (MAXS is 1 for decode, the
+  // draft bound for replay), so staging costs one memory round trip, not one
+  // per step.
+  float rk[MAXS][EK], rq[MAXS][EK], rg_[MAXS][EK], rv[MAXS][EV], rb[MAXS];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-    if (lane == 0) kqw[s * NW + warp] = kq;
+  for (int s = 0; s < MAXS; ++s) {
+    const bool live = active && s < n;
+    const int64_t hs = (int64_t)s * nheads + head;      // (step, b, h) flattened
+#pragma unroll
+    for (int u = 0; u < EK; ++u) {
+      const int i = tid + u * NT;
+      const bool ok = live && i < DK;
+      rk[s][u] = ok ? to_f32(k[hs * DK + i]) : 0.f;
+      rq[s][u] = ok ? to_f32(q[hs * DK + i]) : 0.f;
+      rg_[s][u] = ok ? to_f32(g[hs * DK + i]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < EV; ++u) {
+      const int j = tid + u * NT;
+      rv[s][u] = live && j < DV ? to_f32(v[hs * DV + j]) : 0.f;
+    }
+    rb[s] = live && tid == 0 ? to_f32(beta[hs]) : 0.f;
+  }
+#pragma unroll
+  for (int s = 0; s < MAXS; ++s) {
+    if (s < n) {
+      float* st = stage + (size_t)s * C::STAGE;
+      float kq = 0.f;
+#pragma unroll
+      for (int u = 0; u < EK; ++u) {
+        const int i = tid + u * NT;
+        if (i < DK) {
+          st[i] = rk[s][u];
+          st[DK + i] = rq[s][u];
+          st[2 * DK + i] = expf(rg_[s][u]);
+          kq = fmaf(rk[s][u], rq[s][u], kq);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < EV; ++u) {
+        const int j = tid + u * NT;
+        if (j < DV) st[3 * DK + j] = rv[s][u];
+      }
+      if (tid == 0) st[3 * DK + DV] = rb[s];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+      if (lane == 0) kqw[s * NW + warp] = kq;
+    }
   }
   __syncthreads();
 
@@ -139,21 +171,28 @@ kda_step_kernel(const StepArgs a) {
       pb.x += __shfl_xor_sync(0xffffffffu, pb.x, off); pb.y += __shfl_xor_sync(0xffffffffu, pb.y, off);
       pb.z += __shfl_xor_sync(0xffffffffu, pb.z, off); pb.w += __shfl_xor_sync(0xffffffffu, pb.w, off);
     }
-    float* rb = red + (size_t)(s & 1) * NW * C::RED;
-    if (lane < TPR) {
-      *reinterpret_cast<float4*>(rb + warp * C::RED + 4 * c4) = pa;
-      *reinterpret_cast<float4*>(rb + warp * C::RED + DV + 4 * c4) = pb;
-    }
-    __syncthreads();
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f), Bq = A;
     float kq = 0.f;
+    if constexpr (NW == 1) {
+      // one warp per head: the butterfly above left the full sums in every lane
+      A = pa;
+      Bq = pb;
+      kq = kqw[s];
+    } else {
+      float* rb = red + (size_t)(s & 1) * NW * C::RED;
+      if (lane < TPR) {
+        *reinterpret_cast<float4*>(rb + warp * C::RED + 4 * c4) = pa;
+        *reinterpret_cast<float4*>(rb + warp * C::RED + DV + 4 * c4) = pb;
+      }
+      __syncthreads();
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      float4 x = *reinterpret_cast<const float4*>(rb + w * C::RED + 4 * c4);
-      float4 z = *reinterpret_cast<const float4*>(rb + w * C::RED + DV + 4 * c4);
-      A.x += x.x; A.y += x.y; A.z += x.z; A.w += x.w;
-      Bq.x += z.x; Bq.y += z.y; Bq.z += z.z; Bq.w += z.w;
-      kq += kqw[s * NW + w];
+      for (int w = 0; w < NW; ++w) {
+        float4 x = *reinterpret_cast<const float4*>(rb + w * C::RED + 4 * c4);
+        float4 z = *reinterpret_cast<const float4*>(rb + w * C::RED + DV + 4 * c4);
+        A.x += x.x; A.y += x.y; A.z += x.z; A.w += x.w;
+        Bq.x += z.x; Bq.y += z.y; Bq.z += z.z; Bq.w += z.w;
+        kq += kqw[s * NW + w];
+      }
     }
     const float bt = st[3 * DK + DV];
     const float4 vv = *reinterpret_cast<const float4*>(st + 3 * DK + 4 * c4);
@@ -210,13 +249,22 @@ cudaError_t launch_dims(const StepArgs& a, cudaStream_t s) {
     kern<<<(unsigned)grid, block, total, s>>>(a);
     return cudaGetLastError();
   };
+  if (a.steps == 1) {
+    if constexpr (HMAX >= 4) {
+      if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, 1, T>, 4);
+    }
+    if constexpr (HMAX >= 2) {
+      if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, 1, T>, 2);
+    }
+    return run(kda_step_kernel<DK, DV, NW, 1, 1, T>, 1);
+  }
   if constexpr (HMAX >= 4) {
-    if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, T>, 4);
+    if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, KDA_MAX_DRAFT, T>, 4);
   }
   if constexpr (HMAX >= 2) {
-    if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, T>, 2);
+    if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, KDA_MAX_DRAFT, T>, 2);
   }
-  return run(kda_step_kernel<DK, DV, NW, 1, T>, 1);
+  return run(kda_step_kernel<DK, DV, NW, 1, KDA_MAX_DRAFT, T>, 1);
 }
 
 template <typename T>
