@@ -75,10 +75,6 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
   return u;
 }
 
-__device__ __forceinline__ float sel4(const float (&a)[4], int i) {
-  return i == 0 ? a[0] : (i == 1 ? a[1] : (i == 2 ? a[2] : a[3]));
-}
-
 __device__ __forceinline__ int find_seq(const PrefillSched& s, int chunk) {
   int lo = 0, hi = s.n_seqs - 1;
   while (lo < hi) {                     // last n with chunk_base[n] <= chunk
@@ -157,116 +153,130 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   uint32_t phase = 0;
   bool ok = true;
 
-  // ---- gates: thread i owns key channel i ----------------------------------
-  const int i = tid;
-  // Pass 1: the block reference values Gamma_m(R) (8th token of each 16-token
-  // block) and Gamma_C (last token), from the g tile the TMA brought in.
+  // ---- gates: thread t owns key channels 2p, 2p+1 (p = t % 64) for rows
+  // 32 hf .. 32 hf + 31 (hf = t / 64); every store is one packed bf16 pair.
+  const int pch = tid & 63, hf = tid >> 6, c0 = 2 * pch;
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(sm + P_R1 + 16384);  // g [64][64 pairs]
+  const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(sm + P_APB);
+  const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(sm + P_APB + 16384);
   ok = cta_wait(mbar_in, 0);
-  const __nv_bfloat16* graw = reinterpret_cast<const __nv_bfloat16*>(sm + P_R1 + 16384);   // [64][128]
-  float gall[C];
-#pragma unroll
-  for (int r = 0; r < C; ++r) gall[r] = r < L ? __bfloat162float(graw[r * DKT + i]) : 0.f;
-  float gm[4], GC;
+  // Pass 1: full cumsum of both channels; the block reference values Gamma_m(R)
+  // (8th token of each 16-token block), Gamma_C (last token) and the running sum
+  // where this thread's rows start.
+  float gm[4][2], GC[2], acc0[2] = {0.f, 0.f};
   {
-    float acc = 0.f;
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
     for (int r = 0; r < C; ++r) {
-      acc += gall[r];
-      if ((r & 15) == 7) gm[r >> 4] = acc;
+      const float2 gv = r < L ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
+      if (r == 32 && hf == 1) { acc0[0] = a0; acc0[1] = a1; }
+      a0 += gv.x;
+      a1 += gv.y;
+      if ((r & 15) == 7) { gm[r >> 4][0] = a0; gm[r >> 4][1] = a1; }
     }
-    GC = acc;
+    GC[0] = a0;
+    GC[1] = a1;
   }
-  float egm[4], egcm[4];
+  float egm[4][2], egcm[4][2];
 #pragma unroll
-  for (int R = 0; R < 4; ++R) {
-    egm[R] = __expf(gm[R]);
-    egcm[R] = __expf(GC - gm[R]);
-  }
+  for (int R = 0; R < 4; ++R)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      egm[R][u] = __expf(gm[R][u]);
+      egcm[R][u] = __expf(GC[u] - gm[R][u]);
+    }
+  if (hf == 0)
+    *reinterpret_cast<float2*>(img + img_eg(DV) + 4 * c0) = make_float2(__expf(GC[0]), __expf(GC[1]));
+  __syncthreads();                 // pass 2 overwrites the g tile (it is the Y buffer)
 
-  // Pass 2: the running cumsum again, with every gated operand of the chunk;
-  // k and q of the next 16 rows are loaded while the current 16 are processed.
+  // Pass 2: every gated operand of the chunk for this thread's rows.
   __nv_bfloat16* X = reinterpret_cast<__nv_bfloat16*>(sm + P_R1);          // [64][128]
   __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(sm + P_R1 + 16384);  // [64][128]
-  uint32_t xo[8];
-#pragma unroll
-  for (int rr = 0; rr < 8; ++rr) xo[rr] = (uint32_t)(rr * 128 + ((((i & 63) >> 3) ^ rr) << 4) + (i & 7) * 2);
-  const uint32_t kblk64 = (uint32_t)(i >> 6) * 64 * 128, kblk128 = (uint32_t)(i >> 6) * 128 * 128;
-  const __nv_bfloat16* kraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_APB);           // [64][128]
-  const __nv_bfloat16* qraw = reinterpret_cast<const __nv_bfloat16*>(sm + P_APB + 16384);   // [64][128]
   {
-    float acc = 0.f;
+    float ac0 = acc0[0], ac1 = acc0[1];
 #pragma unroll
-    for (int R = 0; R < 4; ++R) {
-      const int r0 = 16 * R;
-      const float gmR = gm[R], egmR = egm[R], egcmR = egcm[R];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int r = r0 + e;
-        const float prev = acc;               // Gamma_{r-1}
-        acc += gall[r];                       // Gamma_r
-        // rows past the sequence end come from the next sequence (or fill): masked
-        const float kr = r < L ? __bfloat162float(kraw[r * DKT + i]) : 0.f;
-        const float qr = r < L ? __bfloat162float(qraw[r * DKT + i]) : 0.f;
-        const float d = acc - gmR;
-        const float E = __expf(d), Einv = __expf(-d);
-        const float EG = decay_first ? E : __expf(prev - gmR);
-        // K-major offsets of (row r, column i) and MN-major offsets of (mn i, row r)
-        const uint32_t rg = (uint32_t)(r >> 3) * 1024 + xo[r & 7];
-        const uint32_t mn = (uint32_t)(i >> 6) * 64 * 128 + (uint32_t)(r >> 3) * 1024 +
-                            (uint32_t)(r & 7) * 128 + ((((i & 63) >> 3) ^ (r & 7)) << 4) + (i & 7) * 2;
-        st_bf16(sm + P_KHAT, kblk64 + rg, kr * Einv);
-        st_bf16(sm + P_KTIL, mn, kr * EG * egmR);
-        st_bf16(img + IMG_WQ, kblk128 + 8192 + rg, qr * E * egmR);      // row 64 + r
-        st_bf16(img + IMG_KB, mn, kr * Einv * egcmR);
-        X[r * DKT + i] = __float2bfloat16_rn(kr * EG);
-        Y[r * DKT + i] = __float2bfloat16_rn(qr * E);
-      }
+    for (int rr = 0; rr < 32; ++rr) {
+      const int r = 32 * hf + rr;
+      const int R = r >> 4;                       // 2 hf + rr / 16: known per unrolled rr up to hf
+      const bool in = r < L;
+      const float2 gv = in ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
+      const float2 kv = in ? __bfloat1622float2(k2[r * 64 + pch]) : make_float2(0.f, 0.f);
+      const float2 qv = in ? __bfloat1622float2(q2[r * 64 + pch]) : make_float2(0.f, 0.f);
+      const float p0 = ac0, p1 = ac1;             // Gamma_{r-1}
+      ac0 += gv.x;                                // Gamma_r
+      ac1 += gv.y;
+      const float gm0 = hf ? gm[2 + (rr >> 4)][0] : gm[rr >> 4][0];
+      const float gm1 = hf ? gm[2 + (rr >> 4)][1] : gm[rr >> 4][1];
+      const float em0 = hf ? egm[2 + (rr >> 4)][0] : egm[rr >> 4][0];
+      const float em1 = hf ? egm[2 + (rr >> 4)][1] : egm[rr >> 4][1];
+      const float ec0 = hf ? egcm[2 + (rr >> 4)][0] : egcm[rr >> 4][0];
+      const float ec1 = hf ? egcm[2 + (rr >> 4)][1] : egcm[rr >> 4][1];
+      (void)R;
+      const float d0 = ac0 - gm0, d1 = ac1 - gm1;
+      const float E0 = __expf(d0), E1 = __expf(d1), Ei0 = __expf(-d0), Ei1 = __expf(-d1);
+      const float EG0 = decay_first ? E0 : __expf(p0 - gm0);
+      const float EG1 = decay_first ? E1 : __expf(p1 - gm1);
+      *reinterpret_cast<__nv_bfloat162*>(sm + P_KHAT + off_k(r, c0, 64)) =
+          __floats2bfloat162_rn(kv.x * Ei0, kv.y * Ei1);
+      *reinterpret_cast<__nv_bfloat162*>(sm + P_KTIL + off_mn(c0, r, 64)) =
+          __floats2bfloat162_rn(kv.x * EG0 * em0, kv.y * EG1 * em1);
+      *reinterpret_cast<__nv_bfloat162*>(img + IMG_WQ + off_k(64 + r, c0, 128)) =
+          __floats2bfloat162_rn(qv.x * E0 * em0, qv.y * E1 * em1);
+      *reinterpret_cast<__nv_bfloat162*>(img + IMG_KB + off_mn(c0, r, 64)) =
+          __floats2bfloat162_rn(kv.x * Ei0 * ec0, kv.y * Ei1 * ec1);
+      *reinterpret_cast<__nv_bfloat162*>(X + r * DKT + c0) = __floats2bfloat162_rn(kv.x * EG0, kv.y * EG1);
+      *reinterpret_cast<__nv_bfloat162*>(Y + r * DKT + c0) = __floats2bfloat162_rn(qv.x * E0, qv.y * E1);
     }
   }
-  reinterpret_cast<float*>(img + img_eg(DV))[i] = __expf(GC);
-
   __syncthreads();            // X and Y rows are read by other threads below
 
   // ---- A and P: one tcgen05 MMA chain per 16-token column block ------------
   const uint32_t apb = smem_u32(sm + P_APB);
   const uint32_t khat = smem_u32(sm + P_KHAT);
   constexpr uint32_t ID_AP = idesc_bf16(128, 16, false, false);
-  for (int S = 0; S < 4 && ok; ++S) {
-    if (S > 0) {                                   // previous MMA must finish reading APB
+  // Column blocks from last to first: build S writes only rows >= 16 S (rows
+  // above stay zero from the first build, which zeroes rows 0..47).
+  __nv_bfloat16* s_fac16 = reinterpret_cast<__nv_bfloat16*>(s_fac);   // [4][128] bf16
+  for (int S = 3; S >= 0 && ok; --S) {
+    if (S < 3) {                                   // previous MMA must finish reading APB
       ok = cta_wait(mbar, phase);
       phase ^= 1;
       fence_after();
       if (!ok) break;
     }
-    // block-to-block factors e^{Gamma_m(R) - Gamma_m(S)} <= 1 for R >= S
-    const float gmS = sel4(gm, S);
-    float fR[4];
+    // block-to-block factors e^{Gamma_m(R) - Gamma_m(S)} <= 1 for R >= S; they are
+    // per key channel, so publish them for the 16-byte chunks below (8 channels each)
+    if (hf == 0) {
+      const float gS0 = S == 0 ? gm[0][0] : (S == 1 ? gm[1][0] : (S == 2 ? gm[2][0] : gm[3][0]));
+      const float gS1 = S == 0 ? gm[0][1] : (S == 1 ? gm[1][1] : (S == 2 ? gm[2][1] : gm[3][1]));
 #pragma unroll
-    for (int R = 0; R < 4; ++R) fR[R] = R >= S ? __expf(gm[R] - gmS) : 0.f;
-    // The factors are per key channel: publish them so that the 16-byte chunks
-    // below (8 channels of one row each) scale every channel by its own factor.
-#pragma unroll
-    for (int R = 0; R < 4; ++R) s_fac[R * DKT + i] = fR[R];
+      for (int R = 0; R < 4; ++R)
+        *reinterpret_cast<__nv_bfloat162*>(s_fac16 + R * DKT + c0) =
+            __floats2bfloat162_rn(R >= S ? __expf(gm[R][0] - gS0) : 0.f, R >= S ? __expf(gm[R][1] - gS1) : 0.f);
+    }
     __syncthreads();
-    // 16-byte chunks: (row r, channels 8cc..8cc+7) of X (rows 0-63) and Y (rows 64-127)
-#pragma unroll 4
-    for (int e = tid; e < 2 * C * 16; e += NT) {
-      const int half = e >> 10, r = (e >> 4) & 63, cc = e & 15;
-      const float* fc = s_fac + (r >> 4) * DKT + 8 * cc;
-      const float4 f0 = *reinterpret_cast<const float4*>(fc);
-      const float4 f1 = *reinterpret_cast<const float4*>(fc + 4);
-      const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-      const __nv_bfloat16* src = (half ? Y : X) + r * DKT + 8 * cc;
-      const uint4 raw = *reinterpret_cast<const uint4*>(src);
-      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
-      float v8[8];
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float2 x = __bfloat1622float2(pr[t]);
-        v8[2 * t] = x.x * f[2 * t];
-        v8[2 * t + 1] = x.y * f[2 * t + 1];
+    if (S == 3) {
+      // rows 0..47 of both halves are zero in every build
+      for (int e = tid; e < 2 * 48 * 16; e += NT) {
+        const int half = e / 768, rr = (e % 768) >> 4, cc = e & 15;
+        *reinterpret_cast<uint4*>(sm + P_APB + off_k(64 * half + rr, 8 * cc, 128)) = make_uint4(0, 0, 0, 0);
       }
-      *reinterpret_cast<uint4*>(sm + P_APB + off_k(64 * half + r, 8 * cc, 128)) = pack8(v8);
+    }
+    // rows 16 S..63 of X (A half) and Y (P half), 16-byte chunks of 8 channels;
+    // bf16 x bf16 products are exact before the one rounding, as in fp32
+    const int rows = 64 - 16 * S;
+#pragma unroll 4
+    for (int e = tid; e < 2 * rows * 16; e += NT) {
+      const int half = e / (rows * 16), rr = 16 * S + (e % (rows * 16)) / 16, cc = e & 15;
+      const uint4 x = *reinterpret_cast<const uint4*>((half ? Y : X) + rr * DKT + 8 * cc);
+      const uint4 f = *reinterpret_cast<const uint4*>(s_fac16 + (rr >> 4) * DKT + 8 * cc);
+      uint4 y;
+      const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&x);
+      const __nv_bfloat162* fp = reinterpret_cast<const __nv_bfloat162*>(&f);
+      __nv_bfloat162* yp = reinterpret_cast<__nv_bfloat162*>(&y);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) yp[t] = __hmul2(xp[t], fp[t]);
+      *reinterpret_cast<uint4*>(sm + P_APB + off_k(64 * half + rr, 8 * cc, 128)) = y;
     }
     fence_async_smem();
     fence_before();
@@ -326,39 +336,59 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 
   // ---- UT solve T = (I + A)^{-1}: 16x16 diagonal blocks, then block levels --
   if (tid < 64) {
+    // column cc of the inverse of diagonal block J, by forward substitution
     const int J = tid >> 4, cc = tid & 15, b0 = 16 * J;
     float x[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      float acc = 0.f;
+      float arow[16];
 #pragma unroll
-      for (int s = 0; s < j; ++s) acc = fmaf(AF[(b0 + j) * 65 + b0 + s], x[s], acc);
-      x[j] = j == cc ? 1.f : (j < cc ? 0.f : -acc);
+      for (int s2 = 0; s2 < j; ++s2) arow[s2] = AF[(b0 + j) * 65 + b0 + s2];
+      float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < j; ++s2) {
+        if (s2 & 1) e1 = fmaf(arow[s2], x[s2], e1); else e0 = fmaf(arow[s2], x[s2], e0);
+      }
+      x[j] = j == cc ? 1.f : (j < cc ? 0.f : -(e0 + e1));
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) TF[(b0 + j) * 65 + b0 + cc] = x[j];
   }
   __syncthreads();
   float* XT = reinterpret_cast<float*>(sm + P_R1);               // [3][16][16]
+  // level d: blocks (I, J = I - d) from the blocks already known
+  //   X = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II X
+#pragma unroll
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;
-    for (int e = tid; e < nb * 256; e += NT) {
-      const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
-      float acc = 0.f;
-      for (int K = J; K < I; ++K)
 #pragma unroll
-        for (int s = 0; s < 16; ++s)
-          acc = fmaf(AF[(16 * I + ar) * 65 + 16 * K + s], TF[(16 * K + s) * 65 + 16 * J + bc], acc);
-      XT[e] = acc;
+    for (int m = 0; m < (nb * 256 + NT - 1) / NT; ++m) {
+      const int e = tid + m * NT;
+      if (e < nb * 256) {
+        const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < d; ++kk) {
+          const int K = J + kk;
+#pragma unroll
+          for (int s2 = 0; s2 < 16; ++s2)
+            a4[s2 & 3] = fmaf(AF[(16 * I + ar) * 65 + 16 * K + s2], TF[(16 * K + s2) * 65 + 16 * J + bc], a4[s2 & 3]);
+        }
+        XT[e] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+      }
     }
     __syncthreads();
-    for (int e = tid; e < nb * 256; e += NT) {
-      const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
-      float acc = 0.f;
 #pragma unroll
-      for (int s = 0; s < 16; ++s)
-        if (s <= ar) acc = fmaf(TF[(16 * I + ar) * 65 + 16 * I + s], XT[(J << 8) + s * 16 + bc], acc);
-      TF[(16 * I + ar) * 65 + 16 * J + bc] = -acc;
+    for (int m = 0; m < (nb * 256 + NT - 1) / NT; ++m) {
+      const int e = tid + m * NT;
+      if (e < nb * 256) {
+        const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s2 = 0; s2 < 16; ++s2)
+          if (s2 <= ar) a4[s2 & 3] = fmaf(TF[(16 * I + ar) * 65 + 16 * I + s2], XT[(J << 8) + s2 * 16 + bc], a4[s2 & 3]);
+        TF[(16 * I + ar) * 65 + 16 * J + bc] = -((a4[0] + a4[1]) + (a4[2] + a4[3]));
+      }
     }
     __syncthreads();
   }
