@@ -55,14 +55,17 @@ __host__ __device__ constexpr uint32_t img_eg(int dv) { return IMG_U + 64u * dv 
 __host__ __device__ constexpr uint32_t img_bytes(int dv) { return img_eg(dv) + 512u; }
 
 // ---- prep kernel shared memory ---------------------------------------------
+constexpr int PNT = 256;                // prep threads: 64 channel pairs x 4 blocks of 16 tokens
 constexpr uint32_t P_KHAT = 0;          // 16 KB  Khat K-major [64][128]; later V (MN-major, K=64)
-constexpr uint32_t P_APB = 16384;       // 33 KB  [Ktil_S; Qtil_S] K-major [128][128]; later A, T fp32 [64][65]
+constexpr uint32_t P_APB = 16384;       // 33 KB  [X; Y] K-major [128][128]; later A, T fp32 [64][65]
 constexpr uint32_t P_KTIL = 50176;      // 16 KB  k e^{G} MN-major (mn = dk, K = 64)
-constexpr uint32_t P_R1 = 66560;        // 32 KB  X, Y bf16 [64][128]; later XT scratch + TOP
-constexpr uint32_t P_TOP = P_R1 + 16384;  // 16 KB [T; 0] K-major [128][64]
+constexpr uint32_t P_R1 = 66560;        // 32 KB  g tile; then Khat_1..3; then XT scratch + TOP
+constexpr uint32_t P_KH1 = P_R1, P_KH2 = P_R1 + 4096, P_KH3 = P_R1 + 12288;   // 16, 32, 48 rows
+constexpr uint32_t P_TOP = P_R1 + 16384;  // 16 KB [T; T] K-major [128][64]
 constexpr uint32_t P_MISC = 99328;      // beta fp32[64] | mbar | tmem slot
-constexpr uint32_t P_FAC = P_MISC + 512;  // fp32 [4][128]: block-to-block factors of one build
-constexpr uint32_t P_SMEM = P_FAC + 2048 + 1024;
+constexpr uint32_t P_FAC = P_MISC + 512;  // bf16 [6][128]: e^{Gamma_m(R) - Gamma_m(S)}, S < R
+constexpr uint32_t P_PART = P_FAC + 1536; // float4 [4][64]: per-block partial sums of g
+constexpr uint32_t P_SMEM = P_PART + 4096 + 1024;
 
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
@@ -97,28 +100,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(mbar) : "memory");
 }
 
-// Tensor maps of one prefill launch: k, q and g as [T][H*128] with a plain
-// 128 x 64 box (a chunk's rows of one head, row-major in shared memory); v as
-// [T][H*DV] with a 64 x 64 box and 128-byte swizzle, which lands exactly in the
-// MN-major operand layout the U = T V contraction reads.
+// Tensor maps of one prefill launch: k and q as [T][H*128] with a 64 x 64 box
+// and 128-byte swizzle (two boxes per chunk and head land as the K-major
+// operand layout); g as [T][H*128] with a plain 128 x 64 box (row-major in
+// shared memory); v as [T][H*DV] with a 64 x 64 box and 128-byte swizzle, which
+// lands exactly in the MN-major operand layout the U = T V contraction reads.
 struct PrepMaps {
   CUtensorMap k, q, g, v;
 };
 
 template <int DV>
-__global__ void __launch_bounds__(NT, 2)
+__global__ void __launch_bounds__(PNT, 2)
 kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned char* __restrict__ ws,
                       const __grid_constant__ PrepMaps maps) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   float* s_beta = reinterpret_cast<float*>(sm + P_MISC);
-  float* s_fac = reinterpret_cast<float*>(sm + P_FAC);
   const uint32_t mbar = smem_u32(sm + P_MISC + 256);       // tensor-core commits
-  const uint32_t mbar_in = smem_u32(sm + P_MISC + 272);    // k and q tiles
+  const uint32_t mbar_in = smem_u32(sm + P_MISC + 272);    // k, q and g tiles
   const uint32_t mbar_v = smem_u32(sm + P_MISC + 280);     // v tile
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + P_MISC + 264);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // heads vary fastest across the grid: CTAs running together read whole token rows
   const int H = a.H;
   const int h = (int)(blockIdx.x % (unsigned)H), chunk = (int)(blockIdx.x / (unsigned)H);
@@ -135,14 +138,16 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     mbar_init(mbar_in, 1);
     mbar_init(mbar_v, 1);
     mbar_init_fence();
-    // raw k and q tiles of this (chunk, head) into the A/P buffer, idle until the
-    // first build; the g tile into the Y buffer: thread i reads g[r][i] into a
-    // register before it writes Y[r][i] at the same address, and no other thread
-    // touches either.
+    // k and q land 128-byte swizzled as the K-major rows 0-63 and 64-127 of the
+    // [X; Y] operand, so the gating pass rewrites each element in place; the g
+    // tile lands row-major in R1.
     mbar_expect_tx(mbar_in, 3 * 16384);
-    tma_load_2d(smem_u32(sm + P_APB), &maps.k, h * DKT, (int)t0, mbar_in);
-    tma_load_2d(smem_u32(sm + P_APB + 16384), &maps.q, h * DKT, (int)t0, mbar_in);
-    tma_load_2d(smem_u32(sm + P_R1 + 16384), &maps.g, h * DKT, (int)t0, mbar_in);
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      tma_load_2d(smem_u32(sm + P_APB + b * 16384), &maps.k, h * DKT + 64 * b, (int)t0, mbar_in);
+      tma_load_2d(smem_u32(sm + P_APB + b * 16384 + 8192), &maps.q, h * DKT + 64 * b, (int)t0, mbar_in);
+    }
+    tma_load_2d(smem_u32(sm + P_R1), &maps.g, h * DKT, (int)t0, mbar_in);
   }
   if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
   if (tid < C) s_beta[tid] = tid < L ? ldf(bg + (t0 + tid) * H + h) : 0.f;
@@ -153,141 +158,151 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   uint32_t phase = 0;
   bool ok = true;
 
-  // ---- gates: thread t owns key channels 2p, 2p+1 (p = t % 64) for rows
-  // 32 hf .. 32 hf + 31 (hf = t / 64); every store is one packed bf16 pair.
-  const int pch = tid & 63, hf = tid >> 6, c0 = 2 * pch;
-  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(sm + P_R1 + 16384);  // g [64][64 pairs]
-  const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(sm + P_APB);
-  const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(sm + P_APB + 16384);
+  // ---- gates: thread t owns key channels 2p, 2p+1 (p = t % 64) for the 16
+  // tokens of block qb = t / 64; every store is one packed bf16 pair.
+  const int pch = tid & 63, qb = tid >> 6, c0 = 2 * pch;
+  const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(sm + P_R1);   // g [64][64 pairs]
+  float4* part = reinterpret_cast<float4*>(sm + P_PART);
   ok = cta_wait(mbar_in, 0);
-  // Pass 1: full cumsum of both channels; the block reference values Gamma_m(R)
-  // (8th token of each 16-token block), Gamma_C (last token) and the running sum
-  // where this thread's rows start.
-  float gm[4][2], GC[2], acc0[2] = {0.f, 0.f};
+  // Pass 1: sums of the block's 16 gates up to its reference token (the 8th)
+  // and in total, exchanged so every thread has the cumsum at all four
+  // reference tokens, at the end of the chunk and before its own block.
+  float2 graw[16];
   {
-    float a0 = 0.f, a1 = 0.f;
+    float a0 = 0.f, a1 = 0.f, p0 = 0.f, p1 = 0.f;
 #pragma unroll
-    for (int r = 0; r < C; ++r) {
-      const float2 gv = r < L ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
-      if (r == 32 && hf == 1) { acc0[0] = a0; acc0[1] = a1; }
-      a0 += gv.x;
-      a1 += gv.y;
-      if ((r & 15) == 7) { gm[r >> 4][0] = a0; gm[r >> 4][1] = a1; }
+    for (int rr = 0; rr < 16; ++rr) {
+      const int r = 16 * qb + rr;
+      graw[rr] = r < L ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
+      a0 += graw[rr].x;
+      a1 += graw[rr].y;
+      if (rr == 7) { p0 = a0; p1 = a1; }
     }
-    GC[0] = a0;
-    GC[1] = a1;
+    part[qb * 64 + pch] = make_float4(p0, p1, a0, a1);
   }
-  float egm[4][2], egcm[4][2];
+  __syncthreads();
+  float gm[4][2], GC[2] = {0.f, 0.f}, acc0[2] = {0.f, 0.f};
 #pragma unroll
-  for (int R = 0; R < 4; ++R)
+  for (int R = 0; R < 4; ++R) {
+    const float4 pr = part[R * 64 + pch];
+    gm[R][0] = GC[0] + pr.x;
+    gm[R][1] = GC[1] + pr.y;
+    if (R < qb) { acc0[0] += pr.z; acc0[1] += pr.w; }
+    GC[0] += pr.z;
+    GC[1] += pr.w;
+  }
+  // block-to-block factors e^{Gamma_m(R) - Gamma_m(S)} <= 1 (S < R), six pairs
+  __nv_bfloat162* fac2 = reinterpret_cast<__nv_bfloat162*>(sm + P_FAC);
+  if (qb < 3) {
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      egm[R][u] = __expf(gm[R][u]);
-      egcm[R][u] = __expf(GC[u] - gm[R][u]);
+      const int idx = 2 * qb + u;                       // (S, R) = (0,1) (0,2) (1,2) (0,3) (1,3) (2,3)
+      const int R = idx == 0 ? 1 : (idx < 3 ? 2 : 3);
+      const int S = idx - R * (R - 1) / 2;
+      const float gR0 = R == 1 ? gm[1][0] : (R == 2 ? gm[2][0] : gm[3][0]);
+      const float gR1 = R == 1 ? gm[1][1] : (R == 2 ? gm[2][1] : gm[3][1]);
+      const float gS0 = S == 0 ? gm[0][0] : (S == 1 ? gm[1][0] : gm[2][0]);
+      const float gS1 = S == 0 ? gm[0][1] : (S == 1 ? gm[1][1] : gm[2][1]);
+      fac2[idx * 64 + pch] = __floats2bfloat162_rn(__expf(gR0 - gS0), __expf(gR1 - gS1));
     }
-  if (hf == 0)
+  } else {
     *reinterpret_cast<float2*>(img + img_eg(DV) + 4 * c0) = make_float2(__expf(GC[0]), __expf(GC[1]));
-  __syncthreads();                 // pass 2 overwrites the g tile (it is the Y buffer)
+  }
 
-  // Pass 2: every gated operand of the chunk for this thread's rows.
-  __nv_bfloat16* X = reinterpret_cast<__nv_bfloat16*>(sm + P_R1);          // [64][128]
-  __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(sm + P_R1 + 16384);  // [64][128]
+  // Pass 2: every gated operand of the chunk for this thread's 16 tokens.
   {
+    const float gmq0 = qb == 0 ? gm[0][0] : (qb == 1 ? gm[1][0] : (qb == 2 ? gm[2][0] : gm[3][0]));
+    const float gmq1 = qb == 0 ? gm[0][1] : (qb == 1 ? gm[1][1] : (qb == 2 ? gm[2][1] : gm[3][1]));
+    const float em0 = __expf(gmq0), em1 = __expf(gmq1);                  // e^{Gamma_m}
+    const float ec0 = __expf(GC[0] - gmq0), ec1 = __expf(GC[1] - gmq1);  // e^{Gamma_C - Gamma_m}
     float ac0 = acc0[0], ac1 = acc0[1];
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr) {
-      const int r = 32 * hf + rr;
-      const int R = r >> 4;                       // 2 hf + rr / 16: known per unrolled rr up to hf
+    for (int rr = 0; rr < 16; ++rr) {
+      const int r = 16 * qb + rr;
       const bool in = r < L;
-      const float2 gv = in ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
-      const float2 kv = in ? __bfloat1622float2(k2[r * 64 + pch]) : make_float2(0.f, 0.f);
-      const float2 qv = in ? __bfloat1622float2(q2[r * 64 + pch]) : make_float2(0.f, 0.f);
+      const uint32_t ox = off_k(r, c0, 128), oy = off_k(64 + r, c0, 128);
+      __nv_bfloat162* xp = reinterpret_cast<__nv_bfloat162*>(sm + P_APB + ox);
+      __nv_bfloat162* yp = reinterpret_cast<__nv_bfloat162*>(sm + P_APB + oy);
+      const float2 kv = in ? __bfloat1622float2(*xp) : make_float2(0.f, 0.f);
+      const float2 qv = in ? __bfloat1622float2(*yp) : make_float2(0.f, 0.f);
       const float p0 = ac0, p1 = ac1;             // Gamma_{r-1}
-      ac0 += gv.x;                                // Gamma_r
-      ac1 += gv.y;
-      const float gm0 = hf ? gm[2 + (rr >> 4)][0] : gm[rr >> 4][0];
-      const float gm1 = hf ? gm[2 + (rr >> 4)][1] : gm[rr >> 4][1];
-      const float em0 = hf ? egm[2 + (rr >> 4)][0] : egm[rr >> 4][0];
-      const float em1 = hf ? egm[2 + (rr >> 4)][1] : egm[rr >> 4][1];
-      const float ec0 = hf ? egcm[2 + (rr >> 4)][0] : egcm[rr >> 4][0];
-      const float ec1 = hf ? egcm[2 + (rr >> 4)][1] : egcm[rr >> 4][1];
-      (void)R;
-      const float d0 = ac0 - gm0, d1 = ac1 - gm1;
+      ac0 += graw[rr].x;                          // Gamma_r
+      ac1 += graw[rr].y;
+      const float d0 = ac0 - gmq0, d1 = ac1 - gmq1;
       const float E0 = __expf(d0), E1 = __expf(d1), Ei0 = __expf(-d0), Ei1 = __expf(-d1);
-      const float EG0 = decay_first ? E0 : __expf(p0 - gm0);
-      const float EG1 = decay_first ? E1 : __expf(p1 - gm1);
+      const float EG0 = decay_first ? E0 : __expf(p0 - gmq0);
+      const float EG1 = decay_first ? E1 : __expf(p1 - gmq1);
       *reinterpret_cast<__nv_bfloat162*>(sm + P_KHAT + off_k(r, c0, 64)) =
           __floats2bfloat162_rn(kv.x * Ei0, kv.y * Ei1);
       *reinterpret_cast<__nv_bfloat162*>(sm + P_KTIL + off_mn(c0, r, 64)) =
           __floats2bfloat162_rn(kv.x * EG0 * em0, kv.y * EG1 * em1);
-      *reinterpret_cast<__nv_bfloat162*>(img + IMG_WQ + off_k(64 + r, c0, 128)) =
+      *reinterpret_cast<__nv_bfloat162*>(img + IMG_WQ + oy) =
           __floats2bfloat162_rn(qv.x * E0 * em0, qv.y * E1 * em1);
       *reinterpret_cast<__nv_bfloat162*>(img + IMG_KB + off_mn(c0, r, 64)) =
           __floats2bfloat162_rn(kv.x * Ei0 * ec0, kv.y * Ei1 * ec1);
-      *reinterpret_cast<__nv_bfloat162*>(X + r * DKT + c0) = __floats2bfloat162_rn(kv.x * EG0, kv.y * EG1);
-      *reinterpret_cast<__nv_bfloat162*>(Y + r * DKT + c0) = __floats2bfloat162_rn(qv.x * E0, qv.y * E1);
+      *xp = __floats2bfloat162_rn(kv.x * EG0, kv.y * EG1);     // X = k e^{G - Gamma_m}
+      *yp = __floats2bfloat162_rn(qv.x * E0, qv.y * E1);       // Y = q e^{Gamma - Gamma_m}
     }
   }
-  __syncthreads();            // X and Y rows are read by other threads below
+  fence_async_smem();
+  fence_before();
+  __syncthreads();
+  fence_after();
 
-  // ---- A and P: one tcgen05 MMA chain per 16-token column block ------------
+  // ---- A and P on tcgen05: D = [X; Y] x (K side)^T over all 128 rows --------
+  // Row block R takes its factor split at reference token m(R): the diagonal
+  // block reads Khat (k e^{Gamma_m(R) - Gamma}) as it is; the blocks left of it
+  // read Khat_R = Khat x e^{Gamma_m(R) - Gamma_m(S)}, built once per R.
+  // TMEM columns: diagonal blocks at 16 R; Khat_1, Khat_2, Khat_3 products at
+  // 64, 80 and 112 (16, 32 and 48 columns).
   const uint32_t apb = smem_u32(sm + P_APB);
   const uint32_t khat = smem_u32(sm + P_KHAT);
-  constexpr uint32_t ID_AP = idesc_bf16(128, 16, false, false);
-  // Column blocks from last to first: build S writes only rows >= 16 S (rows
-  // above stay zero from the first build, which zeroes rows 0..47).
-  __nv_bfloat16* s_fac16 = reinterpret_cast<__nv_bfloat16*>(s_fac);   // [4][128] bf16
-  for (int S = 3; S >= 0 && ok; --S) {
-    if (S < 3) {                                   // previous MMA must finish reading APB
-      ok = cta_wait(mbar, phase);
-      phase ^= 1;
-      fence_after();
-      if (!ok) break;
-    }
-    // block-to-block factors e^{Gamma_m(R) - Gamma_m(S)} <= 1 for R >= S; they are
-    // per key channel, so publish them for the 16-byte chunks below (8 channels each)
-    if (hf == 0) {
-      const float gS0 = S == 0 ? gm[0][0] : (S == 1 ? gm[1][0] : (S == 2 ? gm[2][0] : gm[3][0]));
-      const float gS1 = S == 0 ? gm[0][1] : (S == 1 ? gm[1][1] : (S == 2 ? gm[2][1] : gm[3][1]));
+  if (ok && tid == 0) {
 #pragma unroll
-      for (int R = 0; R < 4; ++R)
-        *reinterpret_cast<__nv_bfloat162*>(s_fac16 + R * DKT + c0) =
-            __floats2bfloat162_rn(R >= S ? __expf(gm[R][0] - gS0) : 0.f, R >= S ? __expf(gm[R][1] - gS1) : 0.f);
-    }
-    __syncthreads();
-    if (S == 3) {
-      // rows 0..47 of both halves are zero in every build
-      for (int e = tid; e < 2 * 48 * 16; e += NT) {
-        const int half = e / 768, rr = (e % 768) >> 4, cc = e & 15;
-        *reinterpret_cast<uint4*>(sm + P_APB + off_k(64 * half + rr, 8 * cc, 128)) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    // rows 16 S..63 of X (A half) and Y (P half), 16-byte chunks of 8 channels;
-    // bf16 x bf16 products are exact before the one rounding, as in fp32
-    const int rows = 64 - 16 * S;
-#pragma unroll 4
-    for (int e = tid; e < 2 * rows * 16; e += NT) {
-      const int half = e / (rows * 16), rr = 16 * S + (e % (rows * 16)) / 16, cc = e & 15;
-      const uint4 x = *reinterpret_cast<const uint4*>((half ? Y : X) + rr * DKT + 8 * cc);
-      const uint4 f = *reinterpret_cast<const uint4*>(s_fac16 + (rr >> 4) * DKT + 8 * cc);
+    for (int R = 0; R < 4; ++R)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mma(tmem + 16 * R, desc_k(apb, 128, j), desc_k(khat + 2048 * R, 64, j), idesc_bf16(128, 16, false, false),
+            j > 0);
+  }
+  {
+    const __nv_bfloat16* facb = reinterpret_cast<const __nv_bfloat16*>(sm + P_FAC);
+    const int sr = tid >> 4, cc = tid & 15;
+#pragma unroll
+    for (int m = 0; m < 6; ++m) {
+      const int R = m == 0 ? 1 : (m < 3 ? 2 : 3);
+      const int S = m == 0 ? 0 : (m < 3 ? m - 1 : m - 3);
+      const int s = 16 * S + sr;
+      const uint32_t dst = R == 1 ? P_KH1 : (R == 2 ? P_KH2 : P_KH3);
+      const uint4 x = *reinterpret_cast<const uint4*>(sm + P_KHAT + off_k(s, 8 * cc, 64));
+      const uint4 f = *reinterpret_cast<const uint4*>(facb + (R * (R - 1) / 2 + S) * DKT + 8 * cc);
       uint4 y;
       const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&x);
       const __nv_bfloat162* fp = reinterpret_cast<const __nv_bfloat162*>(&f);
       __nv_bfloat162* yp = reinterpret_cast<__nv_bfloat162*>(&y);
 #pragma unroll
       for (int t = 0; t < 4; ++t) yp[t] = __hmul2(xp[t], fp[t]);
-      *reinterpret_cast<uint4*>(sm + P_APB + off_k(64 * half + rr, 8 * cc, 128)) = y;
+      *reinterpret_cast<uint4*>(sm + dst + off_k(s, 8 * cc, 16 * R)) = y;
     }
-    fence_async_smem();
-    fence_before();
-    __syncthreads();
-    fence_after();
-    if (tid == 0) {
+  }
+  fence_async_smem();
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (ok && tid == 0) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma(tmem + 16 * S, desc_k(apb, 128, j), desc_k(khat + 2048 * S, 64, j), ID_AP, j > 0);
-      mma_commit(mbar);
-    }
+    for (int j = 0; j < 8; ++j)
+      mma(tmem + 64, desc_k(apb, 128, j), desc_k(smem_u32(sm + P_KH1), 16, j), idesc_bf16(128, 16, false, false),
+          j > 0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      mma(tmem + 80, desc_k(apb, 128, j), desc_k(smem_u32(sm + P_KH2), 32, j), idesc_bf16(128, 32, false, false),
+          j > 0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      mma(tmem + 112, desc_k(apb, 128, j), desc_k(smem_u32(sm + P_KH3), 48, j), idesc_bf16(128, 48, false, false),
+          j > 0);
+    mma_commit(mbar);
   }
   if (ok) { ok = cta_wait(mbar, phase); phase ^= 1; fence_after(); }
   // the A/P products are done with Khat: bring v into its place (MN-major, swizzled)
@@ -299,37 +314,77 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       tma_load_2d(smem_u32(sm + P_KHAT + b * 8192), &maps.v, h * DV + 64 * b, (int)t0, mbar_v);
   }
 
-  // ---- read A (lanes 0-63) and P (lanes 64-127) ----------------------------
+  // ---- read A (lanes 0-63) and P (lanes 64-127); warps w and w + 4 share a
+  // lane quadrant and take the left and right columns of its rows.
   float* AF = reinterpret_cast<float*>(sm + P_APB);            // [64][65]
   float* TF = AF + 64 * 65;                                     // [64][65]
   if (ok) {
-    const int r = tid & 63;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    const int qd = warp & 3, hw = warp >> 2;
+    const bool lo = lane < 16;
+    const int r = 32 * (qd & 1) + lane;                         // token row of this lane
+    const uint32_t la = tmem + ((uint32_t)(32 * qd) << 16);
+    float v[32];
+    int s0, nv;                                                 // v holds columns s0 .. s0 + nv - 1
+    if ((qd & 1) == 0) {                                        // rows 0-31: blocks 0 and 1
+      float a16[16];
+      if (hw == 0) {
+        float b16[16];
+        tmem_ld16(la + 0, a16);
+        tmem_ld16(la + 64, b16);
 #pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      float v[32];
-      tmem_ld32(lane_addr + 32 * hb, v);
-      if (warp < 2) {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int s = 32 * hb + e;
-          AF[r * 65 + s] = s < r ? s_beta[s] * v[e] : 0.f;
-        }
+        for (int e = 0; e < 16; ++e) v[e] = lo ? a16[e] : b16[e];
+        s0 = 0;
       } else {
+        tmem_ld16(la + 16, a16);
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
+        for (int e = 0; e < 16; ++e) v[e] = a16[e];
+        s0 = 16;
+      }
+#pragma unroll
+      for (int e = 16; e < 32; ++e) v[e] = 0.f;
+      nv = 16;
+    } else {                                                    // rows 32-63: blocks 2 and 3
+      if (hw == 0) {
+        float b[32];
+        tmem_ld32(la + 80, v);
+        tmem_ld32(la + 112, b);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = lo ? v[e] : b[e];
+        s0 = 0;
+      } else {
+        float b16[16];
+        tmem_ld32(la + 32, v);
+        tmem_ld16(la + 144, b16);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = lo ? v[e] : b16[e];
+        s0 = 32;
+      }
+      nv = 32;
+    }
+    if (qd < 2) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int s = s0 + e;
+        if (e < nv && s < r) AF[r * 65 + s] = s_beta[s] * v[e];
+      }
+    } else {
+#pragma unroll
+      for (int q8 = 0; q8 < 4; ++q8) {
+        if (8 * q8 < nv) {
           float p8[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = 32 * hb + 8 * q8 + e;
-            p8[e] = s <= r ? v[8 * q8 + e] : 0.f;
-          }
-          *reinterpret_cast<uint4*>(img + IMG_P + off_k(r, 32 * hb + 8 * q8, 64)) = pack8(p8);
+          for (int e = 0; e < 8; ++e) p8[e] = s0 + 8 * q8 + e <= r ? v[8 * q8 + e] : 0.f;
+          *reinterpret_cast<uint4*>(img + IMG_P + off_k(r, s0 + 8 * q8, 64)) = pack8(p8);
         }
+      }
+      if ((qd & 1) == 0 && hw == 1) {                           // rows 0-31 are zero right of column 31
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8)
+          *reinterpret_cast<uint4*>(img + IMG_P + off_k(r, 32 + 8 * q8, 64)) = make_uint4(0, 0, 0, 0);
       }
     }
   }
-  for (int e = tid; e < 64 * 65; e += NT) TF[e] = 0.f;
+  for (int e = tid; e < 64 * 65; e += PNT) TF[e] = 0.f;
   fence_before();
   __syncthreads();
   fence_after();
@@ -362,8 +417,8 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;
 #pragma unroll
-    for (int m = 0; m < (nb * 256 + NT - 1) / NT; ++m) {
-      const int e = tid + m * NT;
+    for (int m = 0; m < (nb * 256 + PNT - 1) / PNT; ++m) {
+      const int e = tid + m * PNT;
       if (e < nb * 256) {
         const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
         float a4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -379,8 +434,8 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     }
     __syncthreads();
 #pragma unroll
-    for (int m = 0; m < (nb * 256 + NT - 1) / NT; ++m) {
-      const int e = tid + m * NT;
+    for (int m = 0; m < (nb * 256 + PNT - 1) / PNT; ++m) {
+      const int e = tid + m * PNT;
       if (e < nb * 256) {
         const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
         float a4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -393,15 +448,15 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     __syncthreads();
   }
 
-  // ---- [T; 0] as bf16 A operand, V as MN-major B operand --------------------
+  // ---- [T; T] as bf16 A operand (the copy feeds lanes 64-127) -----------------
   {
-    const int r = tid;
+    const int r = tid & 127, c32 = 32 * (tid >> 7);
 #pragma unroll
-    for (int cch = 0; cch < 8; ++cch) {
+    for (int cch = 0; cch < 4; ++cch) {
       float t8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) t8[e] = r < 64 ? TF[r * 65 + 8 * cch + e] : 0.f;
-      *reinterpret_cast<uint4*>(sm + P_TOP + off_k(r, 8 * cch, 128)) = pack8(t8);
+      for (int e = 0; e < 8; ++e) t8[e] = TF[(r & 63) * 65 + c32 + 8 * cch + e];
+      *reinterpret_cast<uint4*>(sm + P_TOP + off_k(r, c32 + 8 * cch, 128)) = pack8(t8);
     }
   }
   fence_async_smem();
@@ -421,33 +476,38 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   }
   if (ok) { ok = cta_wait(mbar, phase); phase ^= 1; fence_after(); }
 
-  // ---- -beta W and beta U rows to the chunk image ----------------------------
-  if (ok && warp < 2) {
-    const int r = tid;
+  // ---- -beta W (lanes 0-63) and beta U (lanes 64-127) to the chunk image -----
+  if (ok) {
+    const int qd = warp & 3, hw = warp >> 2;
+    const int r = (32 * qd + lane) & 63;
+    const uint32_t la = tmem + ((uint32_t)(32 * qd) << 16);
     const float br = s_beta[r];
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    if (qd < 2) {
 #pragma unroll
-    for (int cb = 0; cb < 8; ++cb) {
-      float v[16];
-      tmem_ld16(lane_addr + 16 * cb, v);
+      for (int cb = 0; cb < 4; ++cb) {
+        const int j = 64 * hw + 16 * cb;
+        float v[16];
+        tmem_ld16(la + j, v);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] *= -br;
-      *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, 16 * cb, 128)) = pack8(v);
-      *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, 16 * cb + 8, 128)) = pack8(v + 8);
-    }
+        for (int e = 0; e < 16; ++e) v[e] *= -br;
+        *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, j, 128)) = pack8(v);
+        *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, j + 8, 128)) = pack8(v + 8);
+      }
+    } else {
 #pragma unroll
-    for (int cb = 0; cb < DV / 16; ++cb) {
-      float v[16];
-      tmem_ld16(lane_addr + 128 + 16 * cb, v);
+      for (int cb = 0; cb < DV / 32; ++cb) {
+        const int j = (DV / 2) * hw + 16 * cb;
+        float v[16];
+        tmem_ld16(la + 128 + j, v);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] *= br;
-      // row r of each 64-column block: 16-byte chunk c at position c ^ (r % 8), so the
-      // chain's row-per-thread reads hit distinct banks
-      const int j = 16 * cb;
-      unsigned char* blk = img + IMG_U + (j >> 6) * 8192 + r * 128;
-      const int c0 = (j & 63) >> 3;
-      *reinterpret_cast<uint4*>(blk + (((c0) ^ (r & 7)) << 4)) = pack8(v);
-      *reinterpret_cast<uint4*>(blk + (((c0 + 1) ^ (r & 7)) << 4)) = pack8(v + 8);
+        for (int e = 0; e < 16; ++e) v[e] *= br;
+        // row r of each 64-column block: 16-byte chunk c at position c ^ (r % 8), so the
+        // chain's row-per-thread reads hit distinct banks
+        unsigned char* blk = img + IMG_U + (j >> 6) * 8192 + r * 128;
+        const int cj = (j & 63) >> 3;
+        *reinterpret_cast<uint4*>(blk + (((cj) ^ (r & 7)) << 4)) = pack8(v);
+        *reinterpret_cast<uint4*>(blk + (((cj + 1) ^ (r & 7)) << 4)) = pack8(v + 8);
+      }
     }
   }
   if (!ok && tid == 0) {
@@ -712,15 +772,15 @@ cudaError_t launch_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned 
   cudaError_t e;
   if (total_chunks > 0) {
     PrepMaps maps;
-    if (!make_map(&maps.k, a.k, a.T, (int64_t)a.H * DKT, DKT, false) ||
-        !make_map(&maps.q, a.q, a.T, (int64_t)a.H * DKT, DKT, false) ||
+    if (!make_map(&maps.k, a.k, a.T, (int64_t)a.H * DKT, 64, true) ||
+        !make_map(&maps.q, a.q, a.T, (int64_t)a.H * DKT, 64, true) ||
         !make_map(&maps.g, a.g, a.T, (int64_t)a.H * DKT, DKT, false) ||
         !make_map(&maps.v, a.v, a.T, (int64_t)a.H * DV, 64, true))
       return cudaErrorInvalidValue;
     auto prep = kda_chunk_prep_kernel<DV>;
     e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
     if (e != cudaSuccess) return e;
-    prep<<<(unsigned)((int64_t)a.H * total_chunks), NT, P_SMEM, s>>>(a, sched, ws, maps);
+    prep<<<(unsigned)((int64_t)a.H * total_chunks), PNT, P_SMEM, s>>>(a, sched, ws, maps);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   auto chain = kda_chain_kernel<DV>;
