@@ -35,6 +35,7 @@
 
 #include <cstdio>
 #include <mutex>
+#include <type_traits>
 
 namespace kda {
 namespace {
@@ -42,7 +43,6 @@ using namespace tc;
 
 constexpr int C = 64;
 constexpr int DKT = 128;
-constexpr int NT = 128;
 
 // ---- chunk image: byte offsets inside the image of one (chunk, head) -------
 // WQ: K-major [128 rows][128]: rows 0-63 = -beta W, rows 64-127 = q e^{Gamma}
@@ -56,11 +56,11 @@ __host__ __device__ constexpr uint32_t img_bytes(int dv) { return img_eg(dv) + 5
 
 // ---- prep kernel shared memory ---------------------------------------------
 constexpr int PNT = 256;                // prep threads: 64 channel pairs x 4 blocks of 16 tokens
-constexpr uint32_t P_KHAT = 0;          // 16 KB  Khat K-major [64][128]; later V (MN-major, K=64)
+constexpr uint32_t P_KHAT = 0;          // 16 KB  Khat K-major [64][128]; later XT scratch
 constexpr uint32_t P_APB = 16384;       // 33 KB  [X; Y] K-major [128][128]; later A, T fp32 [64][65]
 constexpr uint32_t P_KTIL = 50176;      // 16 KB  k e^{G} MN-major (mn = dk, K = 64)
-constexpr uint32_t P_R1 = 66560;        // 32 KB  g tile; then Khat_1..3; then XT scratch + TOP
-constexpr uint32_t P_KH1 = P_R1, P_KH2 = P_R1 + 4096, P_KH3 = P_R1 + 12288;   // 16, 32, 48 rows
+constexpr uint32_t P_R1 = 66560;        // 32 KB  g tile; then [Khat_1; Khat_2; Khat_3]; then V + TOP
+constexpr uint32_t P_KHS = P_R1;        // 24 KB  Khat_1, Khat_2, Khat_3 stacked: K-major [96][128]
 constexpr uint32_t P_TOP = P_R1 + 16384;  // 16 KB [T; T] K-major [128][64]
 constexpr uint32_t P_MISC = 99328;      // beta fp32[64] | mbar | tmem slot
 constexpr uint32_t P_FAC = P_MISC + 512;  // bf16 [6][128]: e^{Gamma_m(R) - Gamma_m(S)}, S < R
@@ -253,17 +253,15 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   // Row block R takes its factor split at reference token m(R): the diagonal
   // block reads Khat (k e^{Gamma_m(R) - Gamma}) as it is; the blocks left of it
   // read Khat_R = Khat x e^{Gamma_m(R) - Gamma_m(S)}, built once per R.
-  // TMEM columns: diagonal blocks at 16 R; Khat_1, Khat_2, Khat_3 products at
-  // 64, 80 and 112 (16, 32 and 48 columns).
+  // Two products: [X; Y] x Khat^T into TMEM columns 0-63 (row block R keeps
+  // columns 16 R .. 16 R + 15, its diagonal block) and [X; Y] x [Khat_1; Khat_2;
+  // Khat_3]^T into columns 64-159 (Khat_1 at 64, Khat_2 at 80, Khat_3 at 112).
   const uint32_t apb = smem_u32(sm + P_APB);
   const uint32_t khat = smem_u32(sm + P_KHAT);
-  if (ok && tid == 0) {
+  if (ok && warp == 0) {
 #pragma unroll
-    for (int R = 0; R < 4; ++R)
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma(tmem + 16 * R, desc_k(apb, 128, j), desc_k(khat + 2048 * R, 64, j), idesc_bf16(128, 16, false, false),
-            j > 0);
+    for (int j = 0; j < 8; ++j)
+      mma_w(tmem, desc_k(apb, 128, j), desc_k(khat, 64, j), idesc_bf16(128, 64, false, false), j > 0);
   }
   {
     const __nv_bfloat16* facb = reinterpret_cast<const __nv_bfloat16*>(sm + P_FAC);
@@ -273,7 +271,7 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       const int R = m == 0 ? 1 : (m < 3 ? 2 : 3);
       const int S = m == 0 ? 0 : (m < 3 ? m - 1 : m - 3);
       const int s = 16 * S + sr;
-      const uint32_t dst = R == 1 ? P_KH1 : (R == 2 ? P_KH2 : P_KH3);
+      const int row0 = R == 1 ? 0 : (R == 2 ? 16 : 48);            // Khat_R's first row in the stack
       const uint4 x = *reinterpret_cast<const uint4*>(sm + P_KHAT + off_k(s, 8 * cc, 64));
       const uint4 f = *reinterpret_cast<const uint4*>(facb + (R * (R - 1) / 2 + S) * DKT + 8 * cc);
       uint4 y;
@@ -282,36 +280,29 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       __nv_bfloat162* yp = reinterpret_cast<__nv_bfloat162*>(&y);
 #pragma unroll
       for (int t = 0; t < 4; ++t) yp[t] = __hmul2(xp[t], fp[t]);
-      *reinterpret_cast<uint4*>(sm + dst + off_k(s, 8 * cc, 16 * R)) = y;
+      *reinterpret_cast<uint4*>(sm + P_KHS + off_k(row0 + s, 8 * cc, 96)) = y;
     }
   }
   fence_async_smem();
   fence_before();
   __syncthreads();
   fence_after();
-  if (ok && tid == 0) {
+  if (ok && warp == 0) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      mma(tmem + 64, desc_k(apb, 128, j), desc_k(smem_u32(sm + P_KH1), 16, j), idesc_bf16(128, 16, false, false),
-          j > 0);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      mma(tmem + 80, desc_k(apb, 128, j), desc_k(smem_u32(sm + P_KH2), 32, j), idesc_bf16(128, 32, false, false),
-          j > 0);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      mma(tmem + 112, desc_k(apb, 128, j), desc_k(smem_u32(sm + P_KH3), 48, j), idesc_bf16(128, 48, false, false),
-          j > 0);
-    mma_commit(mbar);
+      mma_w(tmem + 64, desc_k(apb, 128, j), desc_k(smem_u32(sm + P_KHS), 96, j), idesc_bf16(128, 96, false, false),
+            j > 0);
+    mma_commit_w(mbar);
   }
   if (ok) { ok = cta_wait(mbar, phase); phase ^= 1; fence_after(); }
-  // the A/P products are done with Khat: bring v into its place (MN-major, swizzled)
+  // the A/P products are done with the stacked Khat_R: v lands there (MN-major,
+  // swizzled), right after k e^{G}, so [k e^{G} | v] is one B operand
   const bool v_issued = ok;
   if (ok && tid == 0) {
     mbar_expect_tx(mbar_v, 64 * DV * 2);
 #pragma unroll
     for (int b = 0; b < DV / 64; ++b)
-      tma_load_2d(smem_u32(sm + P_KHAT + b * 8192), &maps.v, h * DV + 64 * b, (int)t0, mbar_v);
+      tma_load_2d(smem_u32(sm + P_R1 + b * 8192), &maps.v, h * DV + 64 * b, (int)t0, mbar_v);
   }
 
   // ---- read A (lanes 0-63) and P (lanes 64-127); warps w and w + 4 share a
@@ -410,7 +401,7 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     for (int j = 0; j < 16; ++j) TF[(b0 + j) * 65 + b0 + cc] = x[j];
   }
   __syncthreads();
-  float* XT = reinterpret_cast<float*>(sm + P_R1);               // [3][16][16]
+  float* XT = reinterpret_cast<float*>(sm + P_KHAT);             // [3][16][16]
   // level d: blocks (I, J = I - d) from the blocks already known
   //   X = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II X
 #pragma unroll
@@ -464,15 +455,12 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   __syncthreads();
   fence_after();
   if (ok) ok = cta_wait(mbar_v, 0);     // v rows past the sequence end meet beta = 0
-  if (ok && tid == 0) {
+  if (ok && warp == 0) {
     const uint32_t top = smem_u32(sm + P_TOP);
-    constexpr uint32_t ID_W = idesc_bf16(128, 128, false, true);
-    constexpr uint32_t ID_U = idesc_bf16(128, DV, false, true);
+    constexpr uint32_t ID_WU = idesc_bf16(128, 128 + DV, false, true);   // W in columns 0-127, U after
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mma(tmem, desc_k(top, 128, j), desc_mn(smem_u32(sm + P_KTIL), 64, j), ID_W, j > 0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) mma(tmem + 128, desc_k(top, 128, j), desc_mn(khat, 64, j), ID_U, j > 0);
-    mma_commit(mbar);
+    for (int j = 0; j < 4; ++j) mma_w(tmem, desc_k(top, 128, j), desc_mn(smem_u32(sm + P_KTIL), 64, j), ID_WU, j > 0);
+    mma_commit_w(mbar);
   }
   if (ok) { ok = cta_wait(mbar, phase); phase ^= 1; fence_after(); }
 
@@ -522,7 +510,12 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 }
 
 // ---- chain kernel -------------------------------------------------------------
-constexpr int DVS = 64;
+// One CTA per (sequence, head, 64-column slice of dv), 256 threads.  Warps w
+// and w + 4 share TMEM lane quadrant w % 4 and take the left and right 32
+// columns of its rows, so every per-row step (Delta', state update, outputs)
+// is 32 values per thread.
+constexpr int DVS = 64;                            // state columns per CTA
+constexpr int CNT = 256;                           // chain threads
 constexpr uint32_t S_WQ = 0, S_KB = 32768, S_PB = 49152, S_U = 65536, S_EG = 73728;
 constexpr uint32_t STAGE = 75776;                 // 74 KB, keeps every stage 1024-aligned
 constexpr uint32_t C_DELTA = 2 * STAGE;           // 8 KB  Delta' MN-major (mn = 64 cols, K = 64 tokens)
@@ -531,15 +524,22 @@ constexpr uint32_t C_MISC = C_SB + 16384;
 constexpr uint32_t C_SMEM = C_MISC + 128 + 1024;
 constexpr uint32_t CHUNK_TX = 32768 + 16384 + 8192 + 8192 + 512;
 
+// warps 0, 1, 4 and 5 (the Delta' rows) only
+__device__ __forceinline__ void bar_sync_delta() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 template <int DV>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(CNT, 1)
 kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned char* __restrict__ ws) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t full0 = smem_u32(sm + C_MISC), mma_bar = smem_u32(sm + C_MISC + 16);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C_MISC + 32);
+  const uint32_t full0 = smem_u32(sm + C_MISC);         // two image stages
+  const uint32_t bar1 = smem_u32(sm + C_MISC + 16);     // [-bW; Qt] S done
+  const uint32_t bar3 = smem_u32(sm + C_MISC + 24);     // Kbar^T Delta' done
+  const uint32_t bar2 = smem_u32(sm + C_MISC + 32);     // P Delta' done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C_MISC + 48);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, hh = warp >> 2;             // lane quadrant, column half
   const int sl = blockIdx.x, h = blockIdx.y, H = a.H;
   const int n = sched.order[blockIdx.z];
   const int64_t start = sched.start[n];
@@ -548,31 +548,34 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   const int64_t ib = img_bytes(DV);
   const unsigned char* img0 = ws + ((int64_t)sched.chunk_base[n] * H + h) * ib;
   const int col0 = sl * DVS;
+  const int jc = 32 * hh;                              // this thread's first column inside the slice
 
   if (tid == 0) {
     mbar_init(full0, 1);
     mbar_init(full0 + 8, 1);
-    mbar_init(mma_bar, 1);
+    mbar_init(bar1, 1);
+    mbar_init(bar3, 1);
+    mbar_init(bar2, 1);
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
   // zero rows 0-63 of both [0; P] buffers (never written by the copies)
-  for (int e = tid; e < 2 * 512; e += NT) {
+  for (int e = tid; e < 2 * 512; e += CNT) {
     const int s = e >> 9, o = e & 511;
     reinterpret_cast<uint4*>(sm + s * STAGE + S_PB)[o] = make_uint4(0, 0, 0, 0);
   }
-  // state row i = tid, columns col0..col0+63
-  const int i = tid;
-  float S[DVS];
-  const int64_t srow = (((int64_t)n * H + h) * DKT + i) * DV + col0;
+  // state row i, columns col0 + jc .. col0 + jc + 31
+  const int i = 32 * qd + lane;
+  float S[32];
+  const int64_t srow = (((int64_t)n * H + h) * DKT + i) * DV + col0 + jc;
 #pragma unroll
-  for (int j = 0; j < DVS; j += 4) {
+  for (int j = 0; j < 32; j += 4) {
     float4 x = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + srow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
     S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
   }
 #pragma unroll
-  for (int cch = 0; cch < DVS / 8; ++cch)
-    *reinterpret_cast<uint4*>(sm + C_SB + off_mn(8 * cch, i, 128)) = pack8(S + 8 * cch);
+  for (int cch = 0; cch < 4; ++cch)
+    *reinterpret_cast<uint4*>(sm + C_SB + off_mn(jc + 8 * cch, i, 128)) = pack8(S + 8 * cch);
   fence_async_smem();
   fence_before();
   __syncthreads();
@@ -580,8 +583,9 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   const uint32_t tmem = *tslot;
   // TMEM: two output/WS accumulators (one per chunk parity) and the state update
   const uint32_t d2 = tmem + 128;          // d1 of chunk c: tmem + 64 * (c & 1)
+  const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
 
-  auto issue = [&](int cidx) {
+  auto issue = [&](int cidx) {                                     // one thread
     const int s = cidx & 1;
     const unsigned char* src = img0 + (int64_t)cidx * H * ib;
     const uint32_t dst = smem_u32(sm + s * STAGE);
@@ -596,89 +600,98 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   constexpr uint32_t ID_1 = idesc_bf16(128, DVS, false, true);   // [-bW; Qt] (K-major) x S (MN-major)
   constexpr uint32_t ID_3 = idesc_bf16(128, DVS, true, true);    // Kbar^T (MN-major) x Delta' (MN-major)
   const uint32_t delta = smem_u32(sm + C_DELTA), sb = smem_u32(sm + C_SB);
-  auto issue_mma1 = [&](int cidx) {                                // thread 0 only
-    const uint32_t wq = smem_u32(sm + (cidx & 1) * STAGE + S_WQ);
+  auto issue_mma1 = [&](auto stage_tag) {                          // warp 0, converged
+    constexpr int s = decltype(stage_tag)::value;
+    const uint32_t wq = smem_u32(sm + s * STAGE + S_WQ);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) mma(tmem + 64u * (cidx & 1), desc_k(wq, 128, j), desc_mn(sb, 128, j), ID_1, j > 0);
-    mma_commit(mma_bar);
+    for (int j = 0; j < 8; ++j) mma_w(tmem + 64u * s, desc_k(wq, 128, j), desc_mn(sb, 128, j), ID_1, j > 0);
+    mma_commit_w(bar1);
   };
   bool ok = true;
-  bool tok = true;                          // thread 0's own waits; joined in block votes
-  bool mma_pending = false;                 // thread 0: a commit not yet waited for
-  if (tid == 0 && nch > 0) {
-    issue(0);
-    if (nch > 1) issue(1);
-    tok = mbar_wait(full0, 0);            // chunk 0's images, then its first product
-    if (tok) { issue_mma1(0); mma_pending = true; }
+  bool tok = true;                          // this thread's own waits; joined in block votes
+  int last1 = -1, last2 = -1;               // warp 0: last chunk whose MMA1 / MMA3+MMA2 it issued
+  if (warp == 0 && nch > 0) {
+    if (lane == 0) {
+      issue(0);
+      if (nch > 1) issue(1);
+    }
+    __syncwarp();
+    tok = __all_sync(0xffffffffu, mbar_wait(full0, 0));   // chunk 0's images, then its first product
+    if (tok) { issue_mma1(std::integral_constant<int, 0>{}); last1 = 0; }
   }
-  uint32_t mph = 0;
   __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
-  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
 
   // Per chunk c: MMA1(c) was issued at the end of chunk c-1 (or above).
-  //   Delta' = bU + (-bW S)             (warps 0-1, rows 0-63 of d1[c&1])
-  //   MMA2: d1[c&1] rows 64-127 += P Delta';  MMA3: d2 = Kbar^T Delta'
+  //   Delta' = bU + (-bW S)             (warps 0, 1, 4, 5: rows 0-63 of d1[c&1])
+  //   MMA3: d2 = Kbar^T Delta' (bar3);  MMA2: d1[c&1] rows 64-127 += P Delta' (bar2)
   //   S <- e^{Gamma_C} S + d2; S as bf16 for the next MMA1; checkpoints
   //   issue MMA1(c+1) into d1[(c+1)&1], then write the outputs of chunk c
-  //   from d1[c&1] rows 64-127 (warps 2-3) while it runs.
-  int c = 0;
-  for (; c < nch && ok; ++c) {
-    const int s = c & 1;
+  //   from d1[c&1] rows 64-127 (warps 2, 3, 6, 7) while it runs.
+  // The body is instantiated once per stage so that every shared-memory and
+  // TMEM operand address of the products is loop-invariant.
+  auto body = [&](auto stage_tag, int c) -> bool {
+    constexpr int s = decltype(stage_tag)::value;
+    const uint32_t ph = (uint32_t)(c & 1);
     unsigned char* st = sm + s * STAGE;
     const uint32_t d1 = tmem + 64u * s;
-    ok = __syncthreads_and(tok) != 0;               // MMA1(c) was issued
-    if (!ok) break;
-    bool w = mbar_wait(full0 + 8 * s, (c >> 1) & 1);  // already complete: acquires the images
-    w = mbar_wait(mma_bar, mph) && w;
-    ok = __syncthreads_and(w) != 0;
-    mph ^= 1;
-    mma_pending = false;
-    fence_after();
-    if (!ok) break;
-    if (warp < 2) {                         // Delta' = beta U - beta W S, row r = tid
-      const int r = tid;
-      float v[DVS];
-      tmem_ld64(d1 + lane_off, v);
-      const uint4* urow = reinterpret_cast<const uint4*>(st + S_U + r * 128);
+    bool wv = true;
+    if (qd < 2) {                           // Delta' = beta U - beta W S, token row r
+      bool w = mbar_wait(full0 + 8 * s, (c >> 1) & 1);  // already complete: acquires the images
+      w = mbar_wait(bar1, ph) && w;
+      w = __all_sync(0xffffffffu, w);
+      wv = w;
+      fence_after();
+      const int r = i;
+      if (w) {
+        float v[32];
+        tmem_ld32(d1 + lane_off + jc, v);
+        const uint4* urow = reinterpret_cast<const uint4*>(st + S_U + r * 128);
 #pragma unroll
-      for (int cc = 0; cc < DVS / 8; ++cc) {
-        const uint4 u = urow[cc ^ (r & 7)];
-        const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u);
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint4 u = urow[(4 * hh + cc) ^ (r & 7)];
+          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float2 x = __bfloat1622float2(pu[t]);
-          v[8 * cc + 2 * t] += x.x;
-          v[8 * cc + 2 * t + 1] += x.y;
+          for (int t = 0; t < 4; ++t) {
+            const float2 x = __bfloat1622float2(pu[t]);
+            v[8 * cc + 2 * t] += x.x;
+            v[8 * cc + 2 * t + 1] += x.y;
+          }
+          *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(jc + 8 * cc, r, 64)) = pack8(v + 8 * cc);
         }
-        *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(8 * cc, r, 64)) = pack8(v + 8 * cc);
+      }
+      fence_async_smem();
+      fence_before();
+      bar_sync_delta();
+      fence_after();
+      if (warp == 0) {
+        tok = w;
+        if (w) {
+          const uint32_t pb = smem_u32(st + S_PB), kb = smem_u32(st + S_KB);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma_w(d2, desc_mn(kb, 64, j), desc_mn(delta, 64, j), ID_3, j > 0);
+          mma_commit_w(bar3);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma_w(d1, desc_k(pb, 128, j), desc_mn(delta, 64, j), ID_1, 1);
+          mma_commit_w(bar2);
+          last2 = c;
+        }
       }
     }
-    fence_async_smem();
+    // MMA3 done (a product that was never issued lets the bounded wait run out)
+    const bool w3 = tok && wv && mbar_wait(bar3, ph);
     fence_before();
-    __syncthreads();
+    if (__syncthreads_and(w3) == 0) return false;
     fence_after();
-    if (tid == 0) {
-      const uint32_t pb = smem_u32(st + S_PB), kb = smem_u32(st + S_KB);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma(d2, desc_mn(kb, 64, j), desc_mn(delta, 64, j), ID_3, j > 0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma(d1, desc_k(pb, 128, j), desc_mn(delta, 64, j), ID_1, 1);
-      mma_commit(mma_bar);
-    }
-    ok = cta_wait(mma_bar, mph);
-    mph ^= 1;
-    fence_after();
-    if (!ok) break;
     // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
     {
       const float eg = reinterpret_cast<const float*>(st + S_EG)[i];
-      float v[DVS];
-      tmem_ld64(d2 + lane_off, v);
+      float v[32];
+      tmem_ld32(d2 + lane_off + jc, v);
 #pragma unroll
-      for (int j = 0; j < DVS; ++j) S[j] = fmaf(eg, S[j], v[j]);
+      for (int j = 0; j < 32; ++j) S[j] = fmaf(eg, S[j], v[j]);
 #pragma unroll
-      for (int cch = 0; cch < DVS / 8; ++cch)
-        *reinterpret_cast<uint4*>(sm + C_SB + off_mn(8 * cch, i, 128)) = pack8(S + 8 * cch);
+      for (int cch = 0; cch < 4; ++cch)
+        *reinterpret_cast<uint4*>(sm + C_SB + off_mn(jc + 8 * cch, i, 128)) = pack8(S + 8 * cch);
     }
     const int L = min(C, len - c * C);
     const int pos = c * C + L;
@@ -686,50 +699,67 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       const int64_t idx = (int64_t)sched.ckpt_base[n] + pos / a.ckpt_stride - 1;
       if (idx < a.num_ckpt) {
         float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
-        float* prow = page + ((int64_t)h * DKT + i) * DV + col0;
+        float* prow = page + ((int64_t)h * DKT + i) * DV + col0 + jc;
 #pragma unroll
-        for (int j = 0; j < DVS; j += 4) *reinterpret_cast<float4*>(prow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(prow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         if (h == 0 && sl == 0) {
           const int64_t used = (int64_t)H * DKT * DV, total = a.page_bytes / 4;
-          for (int64_t e = used + tid; e < total; e += NT) page[e] = 0.f;
+          for (int64_t e = used + tid; e < total; e += CNT) page[e] = 0.f;
           if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = pos;
         }
       }
     }
     fence_async_smem();
     fence_before();
-    __syncthreads();
+    if (__syncthreads_and(tok) == 0) return false;
     fence_after();
-    if (tid == 0 && c + 1 < nch) {
-      tok = mbar_wait(full0 + 8 * ((c + 1) & 1), ((c + 1) >> 1) & 1);
-      if (tok) { issue_mma1(c + 1); mma_pending = true; }
+    if (warp == 0 && c + 1 < nch) {
+      tok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * (s ^ 1), ((c + 1) >> 1) & 1));
+      if (tok) { issue_mma1(std::integral_constant<int, s ^ 1>{}); last1 = c + 1; }
     }
-    // stage s is free (MMA2/3 of chunk c are done): warp 2 fetches chunk c + 2 into it
-    if (tid == 64 && c + 2 < nch) issue(c + 2);
-    if (warp >= 2) {                        // outputs of chunk c: rows 64-127 of d1[c&1]
-      const int r = tid - 64;
-      float v[DVS];
-      tmem_ld64(d1 + lane_off, v);
-      if (r < L) {
-        __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0;
+    if (qd >= 2) {                          // outputs of chunk c: rows 64-127 of d1[c&1]
+      const bool w = __all_sync(0xffffffffu, mbar_wait(bar2, ph));
+      fence_after();
+      if (!w) tok = false;
+      const int r = i - 64;
+      if (w) {
+        float v[32];
+        tmem_ld32(d1 + lane_off + jc, v);
+        if (r < L) {
+          __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0 + jc;
 #pragma unroll
-        for (int cc = 0; cc < DVS / 8; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(v + 8 * cc);
+          for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(v + 8 * cc);
+        }
       }
     }
+    // stage s is free (MMA2/3 of chunk c are done): thread 64 fetches chunk c + 2 into it
+    if (tid == 64 && tok && c + 2 < nch) issue(c + 2);
+    return true;
+  };
+  int c = 0;
+  while (c < nch && ok) {
+    ok = body(std::integral_constant<int, 0>{}, c);
+    if (!ok) break;
+    if (++c >= nch) break;
+    ok = body(std::integral_constant<int, 1>{}, c);
+    if (!ok) break;
+    ++c;
   }
   ok = __syncthreads_and(ok && tok) != 0;
-  if (!ok && tid == 0) {
+  if (!ok && warp == 0) {
     // Drain what may still be in flight before leaving (bounded waits): the
     // image copies of the chunks after the one that stopped (issued up to two
-    // ahead) and a product whose commit was not waited for.
+    // ahead) and the last products issued (a phase that already completed
+    // returns at once).
     const int last = min(nch, c + 2);
     for (int cc = c; cc < last; ++cc) mbar_wait(full0 + 8 * (cc & 1), (cc >> 1) & 1);
-    if (mma_pending) mbar_wait(mma_bar, mph);
+    if (last1 >= 0) mbar_wait(bar1, (uint32_t)(last1 & 1));
+    if (last2 >= 0) { mbar_wait(bar3, (uint32_t)(last2 & 1)); mbar_wait(bar2, (uint32_t)(last2 & 1)); }
   }
   if (ok) {
-    float* dst = a.S_final + (((int64_t)n * H + h) * DKT + i) * DV + col0;
+    float* dst = a.S_final + (((int64_t)n * H + h) * DKT + i) * DV + col0 + jc;
 #pragma unroll
-    for (int j = 0; j < DVS; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
   }
   fence_before();
   __syncthreads();
@@ -786,7 +816,7 @@ cudaError_t launch_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned 
   auto chain = kda_chain_kernel<DV>;
   e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  chain<<<dim3(DV / DVS, a.H, sched.n_seqs), NT, C_SMEM, s>>>(a, sched, ws);
+  chain<<<dim3(DV / DVS, a.H, sched.n_seqs), CNT, C_SMEM, s>>>(a, sched, ws);
   return cudaGetLastError();
 }
 

@@ -66,6 +66,21 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uin
       "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
       :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
+// The same, executed by a whole converged warp: one elected lane (the lowest,
+// so always the same one) issues.  Descriptors stay warp-uniform, which makes
+// a run of issues several times cheaper than from a single-thread branch.
+__device__ __forceinline__ void mma_w(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p, e; .reg .b32 r; elect.sync r|e, 0xffffffff; setp.ne.b32 p, %4, 0; "
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+      :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t mbar) {
+  asm volatile(
+      "{ .reg .pred e; .reg .b32 r; elect.sync r|e, 0xffffffff; "
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }"
+      :: "r"(mbar) : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                :: "r"(mbar) : "memory");
