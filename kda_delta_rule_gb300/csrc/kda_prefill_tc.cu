@@ -510,12 +510,16 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 }
 
 // ---- chain kernel -------------------------------------------------------------
-// One CTA per (sequence, head, 64-column slice of dv), 256 threads.  Warps w
-// and w + 4 share TMEM lane quadrant w % 4 and take the left and right 32
-// columns of its rows, so every per-row step (Delta', state update, outputs)
-// is 32 values per thread.
+// One CTA per (sequence, head, 64-column slice of dv), nine warps.  Warp 8
+// issues every tensor-core product and every image copy; warps 0-7 do the
+// per-row work, warps w and w + 4 sharing TMEM lane quadrant w % 4 and taking
+// the left and right 32 columns of its rows.  Hand-offs go through mbarriers
+// only:  bar1 / bar3 / bar2 (product commits), dready (Delta' written by warps
+// 0, 1, 4, 5) and sready (chunk done by warps 0-7: state written, TMEM and
+// stage reads finished, the output rows of the chunk in registers).
 constexpr int DVS = 64;                            // state columns per CTA
-constexpr int CNT = 256;                           // chain threads
+constexpr int CNT = 288;                           // chain threads: 8 row warps + 1 issuing warp
+constexpr int CRW = 256;                           // row threads
 constexpr uint32_t S_WQ = 0, S_KB = 32768, S_PB = 49152, S_U = 65536, S_EG = 73728;
 constexpr uint32_t STAGE = 75776;                 // 74 KB, keeps every stage 1024-aligned
 constexpr uint32_t C_DELTA = 2 * STAGE;           // 8 KB  Delta' MN-major (mn = 64 cols, K = 64 tokens)
@@ -523,9 +527,6 @@ constexpr uint32_t C_SB = C_DELTA + 8192;         // 16 KB S bf16 MN-major (mn =
 constexpr uint32_t C_MISC = C_SB + 16384;
 constexpr uint32_t C_SMEM = C_MISC + 128 + 1024;
 constexpr uint32_t CHUNK_TX = 32768 + 16384 + 8192 + 8192 + 512;
-
-// warps 0, 1, 4 and 5 (the Delta' rows) only
-__device__ __forceinline__ void bar_sync_delta() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <int DV>
 __global__ void __launch_bounds__(CNT, 1)
@@ -536,10 +537,13 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   const uint32_t bar1 = smem_u32(sm + C_MISC + 16);     // [-bW; Qt] S done
   const uint32_t bar3 = smem_u32(sm + C_MISC + 24);     // Kbar^T Delta' done
   const uint32_t bar2 = smem_u32(sm + C_MISC + 32);     // P Delta' done
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C_MISC + 48);
+  const uint32_t dready = smem_u32(sm + C_MISC + 40);   // Delta' in shared memory (4 warps)
+  const uint32_t sready = smem_u32(sm + C_MISC + 48);   // chunk finished by the row warps (8 warps)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C_MISC + 64);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + C_MISC + 72);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qd = warp & 3, hh = warp >> 2;             // lane quadrant, column half
+  const int qd = warp & 3, hh = (warp >> 2) & 1;       // lane quadrant, column half (row warps)
   const int sl = blockIdx.x, h = blockIdx.y, H = a.H;
   const int n = sched.order[blockIdx.z];
   const int64_t start = sched.start[n];
@@ -556,26 +560,31 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     mbar_init(bar1, 1);
     mbar_init(bar3, 1);
     mbar_init(bar2, 1);
+    mbar_init(dready, 4);
+    mbar_init(sready, 8);
+    *s_abort = 0;
     mbar_init_fence();
   }
-  if (warp == 0) tmem_alloc(smem_u32(tslot), 256);
+  if (warp == 8) tmem_alloc(smem_u32(tslot), 256);
   // zero rows 0-63 of both [0; P] buffers (never written by the copies)
   for (int e = tid; e < 2 * 512; e += CNT) {
     const int s = e >> 9, o = e & 511;
     reinterpret_cast<uint4*>(sm + s * STAGE + S_PB)[o] = make_uint4(0, 0, 0, 0);
   }
-  // state row i, columns col0 + jc .. col0 + jc + 31
+  // row warps: state row i, columns col0 + jc .. col0 + jc + 31
   const int i = 32 * qd + lane;
   float S[32];
-  const int64_t srow = (((int64_t)n * H + h) * DKT + i) * DV + col0 + jc;
+  if (warp < 8) {
+    const int64_t srow = (((int64_t)n * H + h) * DKT + i) * DV + col0 + jc;
 #pragma unroll
-  for (int j = 0; j < 32; j += 4) {
-    float4 x = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + srow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-    S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+    for (int j = 0; j < 32; j += 4) {
+      float4 x = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + srow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+    }
+#pragma unroll
+    for (int cch = 0; cch < 4; ++cch)
+      *reinterpret_cast<uint4*>(sm + C_SB + off_mn(jc + 8 * cch, i, 128)) = pack8(S + 8 * cch);
   }
-#pragma unroll
-  for (int cch = 0; cch < 4; ++cch)
-    *reinterpret_cast<uint4*>(sm + C_SB + off_mn(jc + 8 * cch, i, 128)) = pack8(S + 8 * cch);
   fence_async_smem();
   fence_before();
   __syncthreads();
@@ -583,188 +592,221 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   const uint32_t tmem = *tslot;
   // TMEM: two output/WS accumulators (one per chunk parity) and the state update
   const uint32_t d2 = tmem + 128;          // d1 of chunk c: tmem + 64 * (c & 1)
-  const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
-
-  auto issue = [&](int cidx) {                                     // one thread
-    const int s = cidx & 1;
-    const unsigned char* src = img0 + (int64_t)cidx * H * ib;
-    const uint32_t dst = smem_u32(sm + s * STAGE);
-    const uint32_t fb = full0 + 8 * s;
-    mbar_expect_tx(fb, CHUNK_TX);
-    bulk_g2s(dst + S_WQ, src + IMG_WQ, 32768, fb);
-    bulk_g2s(dst + S_KB, src + IMG_KB, 16384, fb);
-    bulk_g2s(dst + S_PB + 8192, src + IMG_P, 8192, fb);
-    bulk_g2s(dst + S_U, src + IMG_U + sl * 8192, 8192, fb);
-    bulk_g2s(dst + S_EG, src + img_eg(DV), 512, fb);
-  };
+  const uint32_t delta = smem_u32(sm + C_DELTA), sb = smem_u32(sm + C_SB);
   constexpr uint32_t ID_1 = idesc_bf16(128, DVS, false, true);   // [-bW; Qt] (K-major) x S (MN-major)
   constexpr uint32_t ID_3 = idesc_bf16(128, DVS, true, true);    // Kbar^T (MN-major) x Delta' (MN-major)
-  const uint32_t delta = smem_u32(sm + C_DELTA), sb = smem_u32(sm + C_SB);
-  auto issue_mma1 = [&](auto stage_tag) {                          // warp 0, converged
-    constexpr int s = decltype(stage_tag)::value;
-    const uint32_t wq = smem_u32(sm + s * STAGE + S_WQ);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) mma_w(tmem + 64u * s, desc_k(wq, 128, j), desc_mn(sb, 128, j), ID_1, j > 0);
-    mma_commit_w(bar1);
-  };
-  bool ok = true;
-  bool tok = true;                          // this thread's own waits; joined in block votes
-  int last1 = -1, last2 = -1;               // warp 0: last chunk whose MMA1 / MMA3+MMA2 it issued
-  if (warp == 0 && nch > 0) {
-    if (lane == 0) {
-      issue(0);
-      if (nch > 1) issue(1);
-    }
-    __syncwarp();
-    tok = __all_sync(0xffffffffu, mbar_wait(full0, 0));   // chunk 0's images, then its first product
-    if (tok) { issue_mma1(std::integral_constant<int, 0>{}); last1 = 0; }
-  }
-  __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
 
-  // Per chunk c: MMA1(c) was issued at the end of chunk c-1 (or above).
-  //   Delta' = bU + (-bW S)             (warps 0, 1, 4, 5: rows 0-63 of d1[c&1])
-  //   MMA3: d2 = Kbar^T Delta' (bar3);  MMA2: d1[c&1] rows 64-127 += P Delta' (bar2)
-  //   S <- e^{Gamma_C} S + d2; S as bf16 for the next MMA1; checkpoints
-  //   issue MMA1(c+1) into d1[(c+1)&1], then write the outputs of chunk c
-  //   from d1[c&1] rows 64-127 (warps 2, 3, 6, 7) while it runs.
-  // The body is instantiated once per stage so that every shared-memory and
-  // TMEM operand address of the products is loop-invariant.
-  auto body = [&](auto stage_tag, int c) -> bool {
-    constexpr int s = decltype(stage_tag)::value;
-    const uint32_t ph = (uint32_t)(c & 1);
-    unsigned char* st = sm + s * STAGE;
-    const uint32_t d1 = tmem + 64u * s;
-    bool wv = true;
-    if (qd < 2) {                           // Delta' = beta U - beta W S, token row r
-      bool w = mbar_wait(full0 + 8 * s, (c >> 1) & 1);  // already complete: acquires the images
-      w = mbar_wait(bar1, ph) && w;
-      w = __all_sync(0xffffffffu, w);
-      wv = w;
+  if (warp == 8) {
+    // ---- issuing warp ----------------------------------------------------------
+    auto copy = [&](int cidx) {                                    // lane 0 only
+      const int s = cidx & 1;
+      const unsigned char* src = img0 + (int64_t)cidx * H * ib;
+      const uint32_t dst = smem_u32(sm + s * STAGE);
+      const uint32_t fb = full0 + 8 * s;
+      mbar_expect_tx(fb, CHUNK_TX);
+      bulk_g2s(dst + S_WQ, src + IMG_WQ, 32768, fb);
+      bulk_g2s(dst + S_KB, src + IMG_KB, 16384, fb);
+      bulk_g2s(dst + S_PB + 8192, src + IMG_P, 8192, fb);
+      bulk_g2s(dst + S_U, src + IMG_U + sl * 8192, 8192, fb);
+      bulk_g2s(dst + S_EG, src + img_eg(DV), 512, fb);
+    };
+    // operand descriptors, computed once: k-step j only moves the start address
+    // (16-byte units in the low bits): +2 j within a 128-byte swizzle row and
+    // +8 * R per 64-element K block (K-major, R rows), +128 j (MN-major)
+    const uint64_t dS = desc_mn(sb, 128, 0), dD = desc_mn(delta, 64, 0);
+    const uint64_t dW0 = desc_k(smem_u32(sm + S_WQ), 128, 0), dW1 = desc_k(smem_u32(sm + STAGE + S_WQ), 128, 0);
+    const uint64_t dK0 = desc_mn(smem_u32(sm + S_KB), 64, 0), dK1 = desc_mn(smem_u32(sm + STAGE + S_KB), 64, 0);
+    const uint64_t dP0 = desc_k(smem_u32(sm + S_PB), 128, 0), dP1 = desc_k(smem_u32(sm + STAGE + S_PB), 128, 0);
+    auto mma1 = [&](auto stage_tag) {
+      constexpr int s = decltype(stage_tag)::value;
+      const uint64_t dW = s ? dW1 : dW0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mma_w(tmem + 64u * s, dW + (uint64_t)((j >> 2) * 1024 + (j & 3) * 2), dS + (uint64_t)(128 * j), ID_1, j > 0);
+      mma_commit_w(bar1);
+    };
+    auto mma32 = [&](auto stage_tag) {
+      constexpr int s = decltype(stage_tag)::value;
+      const uint64_t dK = s ? dK1 : dK0, dP = s ? dP1 : dP0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_w(d2, dK + (uint64_t)(128 * j), dD + (uint64_t)(128 * j), ID_3, j > 0);
+      mma_commit_w(bar3);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_w(tmem + 64u * s, dP + (uint64_t)(2 * j), dD + (uint64_t)(128 * j), ID_1, 1);
+      mma_commit_w(bar2);
+    };
+    int issued = 0;                        // image copies issued
+    int last1 = -1, last2 = -1;            // last chunk whose MMA1 / MMA3+MMA2 were issued
+    bool ok = nch > 0;
+    if (ok) {
+      if (lane == 0) {
+        copy(0);
+        if (nch > 1) copy(1);
+      }
+      issued = min(nch, 2);
+      __syncwarp();
+      ok = __all_sync(0xffffffffu, mbar_wait(full0, 0));
+      if (ok) { mma1(std::integral_constant<int, 0>{}); last1 = 0; }
+    }
+    // chunk c: MMA3/MMA2 once Delta' is in; MMA1(c+1) once the row warps are
+    // through chunk c and its images are in; then stage c & 1 is free for c + 2
+    auto step = [&](auto stage_tag, int c) -> bool {
+      constexpr int s = decltype(stage_tag)::value;
+      const uint32_t ph = (uint32_t)(c & 1);
+      if (*s_abort) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(dready, ph))) return false;
       fence_after();
-      const int r = i;
-      if (w) {
+      mma32(stage_tag);
+      last2 = c;
+      if (c + 1 < nch) {
+        if (*s_abort) return false;
+        bool w = mbar_wait(sready, ph);
+        w = w && mbar_wait(full0 + 8 * (s ^ 1), ((c + 1) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, w)) return false;
+        fence_after();
+        mma1(std::integral_constant<int, s ^ 1>{});
+        last1 = c + 1;
+        if (c + 2 < nch) {
+          if (lane == 0) copy(c + 2);
+          issued = c + 3;
+        }
+      }
+      return true;
+    };
+    int c = 0;
+    while (ok && c < nch) {
+      ok = step(std::integral_constant<int, 0>{}, c);
+      if (!ok || ++c >= nch) break;
+      ok = step(std::integral_constant<int, 1>{}, c);
+      if (!ok) break;
+      ++c;
+    }
+    if (!ok && nch > 0) {
+      *s_abort = 1;
+      // leave nothing in flight (bounded waits; a phase that already completed
+      // returns at once): the image copies issued and the last products
+      for (int cc = max(0, issued - 2); cc < issued; ++cc) mbar_wait(full0 + 8 * (cc & 1), (cc >> 1) & 1);
+      if (last1 >= 0) mbar_wait(bar1, (uint32_t)(last1 & 1));
+      if (last2 >= 0) { mbar_wait(bar3, (uint32_t)(last2 & 1)); mbar_wait(bar2, (uint32_t)(last2 & 1)); }
+    }
+  } else {
+    // ---- row warps -------------------------------------------------------------
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
+    const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
+    const int ck_every = a.ckpt_stride > 0 ? a.ckpt_stride / C : 0;
+    int ck_left = ck_every;
+    auto row_step = [&](auto stage_tag, int c) -> bool {
+      constexpr int s = decltype(stage_tag)::value;
+      const uint32_t ph = (uint32_t)(c & 1);
+      const unsigned char* st = sm + s * STAGE;
+      const uint32_t d1 = tmem + 64u * s;
+      if (*s_abort) return false;
+      // the images of chunk c (complete long ago; acquires them for this thread)
+      if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (c >> 1) & 1))) return false;
+      if (qd < 2) {                         // Delta' = beta U - beta W S, token row r
+        if (!__all_sync(0xffffffffu, mbar_wait(bar1, ph))) return false;
+        fence_after();
+        const int r = i;
         float v[32];
         tmem_ld32(d1 + lane_off + jc, v);
         const uint4* urow = reinterpret_cast<const uint4*>(st + S_U + r * 128);
+        uint4 u[4];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) u[cc] = urow[(4 * hh + cc) ^ (r & 7)];   // all loads before any store
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          const uint4 u = urow[(4 * hh + cc) ^ (r & 7)];
-          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u);
+          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u[cc]);
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
             const float2 x = __bfloat1622float2(pu[t]);
             v[8 * cc + 2 * t] += x.x;
             v[8 * cc + 2 * t + 1] += x.y;
           }
-          *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(jc + 8 * cc, r, 64)) = pack8(v + 8 * cc);
         }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(jc + 8 * cc, r, 64)) = pack8(v + 8 * cc);
+        fence_async_smem();
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dready);
+      }
+      if (*s_abort) return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar3, ph))) return false;
+      fence_after();
+      // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
+      {
+        const float eg = reinterpret_cast<const float*>(st + S_EG)[i];
+        float v[32];
+        tmem_ld32(d2 + lane_off + jc, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[j] = fmaf(eg, S[j], v[j]);
+#pragma unroll
+        for (int cch = 0; cch < 4; ++cch)
+          *reinterpret_cast<uint4*>(sm + C_SB + off_mn(jc + 8 * cch, i, 128)) = pack8(S + 8 * cch);
+      }
+      const int L = min(C, len - c * C);
+      const int pos = c * C + L;
+      // a checkpoint ends every ckpt_stride / C full chunks (a partial chunk
+      // never ends on a multiple of the stride)
+      const bool ck = ck_every > 0 && --ck_left == 0;
+      if (ck) ck_left = ck_every;
+      if (ck && L == C) {
+        const int64_t idx = (int64_t)sched.ckpt_base[n] + pos / a.ckpt_stride - 1;
+        if (idx < a.num_ckpt) {
+          float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
+          float* prow = page + ((int64_t)h * DKT + i) * DV + col0 + jc;
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(prow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+          if (h == 0 && sl == 0) {
+            const int64_t used = (int64_t)H * DKT * DV, total = a.page_bytes / 4;
+            for (int64_t e = used + tid; e < total; e += CRW) page[e] = 0.f;
+            if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = pos;
+          }
+        }
+      }
+      float ov[32];
+      if (qd >= 2) {                        // outputs of chunk c: rows 64-127 of d1[c&1]
+        if (*s_abort) return false;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar2, ph))) return false;
+        fence_after();
+        tmem_ld32(d1 + lane_off + jc, ov);
       }
       fence_async_smem();
       fence_before();
-      bar_sync_delta();
-      fence_after();
-      if (warp == 0) {
-        tok = w;
-        if (w) {
-          const uint32_t pb = smem_u32(st + S_PB), kb = smem_u32(st + S_KB);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mma_w(d2, desc_mn(kb, 64, j), desc_mn(delta, 64, j), ID_3, j > 0);
-          mma_commit_w(bar3);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mma_w(d1, desc_k(pb, 128, j), desc_mn(delta, 64, j), ID_1, 1);
-          mma_commit_w(bar2);
-          last2 = c;
-        }
-      }
-    }
-    // MMA3 done (a product that was never issued lets the bounded wait run out)
-    const bool w3 = tok && wv && mbar_wait(bar3, ph);
-    fence_before();
-    if (__syncthreads_and(w3) == 0) return false;
-    fence_after();
-    // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
-    {
-      const float eg = reinterpret_cast<const float*>(st + S_EG)[i];
-      float v[32];
-      tmem_ld32(d2 + lane_off + jc, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) S[j] = fmaf(eg, S[j], v[j]);
-#pragma unroll
-      for (int cch = 0; cch < 4; ++cch)
-        *reinterpret_cast<uint4*>(sm + C_SB + off_mn(jc + 8 * cch, i, 128)) = pack8(S + 8 * cch);
-    }
-    const int L = min(C, len - c * C);
-    const int pos = c * C + L;
-    if (a.ckpt_stride > 0 && pos % a.ckpt_stride == 0) {
-      const int64_t idx = (int64_t)sched.ckpt_base[n] + pos / a.ckpt_stride - 1;
-      if (idx < a.num_ckpt) {
-        float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
-        float* prow = page + ((int64_t)h * DKT + i) * DV + col0 + jc;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(prow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-        if (h == 0 && sl == 0) {
-          const int64_t used = (int64_t)H * DKT * DV, total = a.page_bytes / 4;
-          for (int64_t e = used + tid; e < total; e += CNT) page[e] = 0.f;
-          if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = pos;
-        }
-      }
-    }
-    fence_async_smem();
-    fence_before();
-    if (__syncthreads_and(tok) == 0) return false;
-    fence_after();
-    if (warp == 0 && c + 1 < nch) {
-      tok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * (s ^ 1), ((c + 1) >> 1) & 1));
-      if (tok) { issue_mma1(std::integral_constant<int, s ^ 1>{}); last1 = c + 1; }
-    }
-    if (qd >= 2) {                          // outputs of chunk c: rows 64-127 of d1[c&1]
-      const bool w = __all_sync(0xffffffffu, mbar_wait(bar2, ph));
-      fence_after();
-      if (!w) tok = false;
-      const int r = i - 64;
-      if (w) {
-        float v[32];
-        tmem_ld32(d1 + lane_off + jc, v);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sready);
+      if (qd >= 2) {
+        const int r = i - 64;
         if (r < L) {
           __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0 + jc;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(v + 8 * cc);
+          for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(ov + 8 * cc);
         }
       }
+      return true;
+    };
+    bool ok = true;
+    int c = 0;
+    while (ok && c < nch) {
+      ok = row_step(std::integral_constant<int, 0>{}, c);
+      if (!ok || ++c >= nch) break;
+      ok = row_step(std::integral_constant<int, 1>{}, c);
+      if (!ok) break;
+      ++c;
     }
-    // stage s is free (MMA2/3 of chunk c are done): thread 64 fetches chunk c + 2 into it
-    if (tid == 64 && tok && c + 2 < nch) issue(c + 2);
-    return true;
-  };
-  int c = 0;
-  while (c < nch && ok) {
-    ok = body(std::integral_constant<int, 0>{}, c);
-    if (!ok) break;
-    if (++c >= nch) break;
-    ok = body(std::integral_constant<int, 1>{}, c);
-    if (!ok) break;
-    ++c;
-  }
-  ok = __syncthreads_and(ok && tok) != 0;
-  if (!ok && warp == 0) {
-    // Drain what may still be in flight before leaving (bounded waits): the
-    // image copies of the chunks after the one that stopped (issued up to two
-    // ahead) and the last products issued (a phase that already completed
-    // returns at once).
-    const int last = min(nch, c + 2);
-    for (int cc = c; cc < last; ++cc) mbar_wait(full0 + 8 * (cc & 1), (cc >> 1) & 1);
-    if (last1 >= 0) mbar_wait(bar1, (uint32_t)(last1 & 1));
-    if (last2 >= 0) { mbar_wait(bar3, (uint32_t)(last2 & 1)); mbar_wait(bar2, (uint32_t)(last2 & 1)); }
-  }
-  if (ok) {
-    float* dst = a.S_final + (((int64_t)n * H + h) * DKT + i) * DV + col0 + jc;
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    if (!ok) *s_abort = 1;
   }
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp < 8 && *s_abort == 0) {
+    float* dst = a.S_final + (((int64_t)n * H + h) * DKT + i) * DV + col0 + jc;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+  }
+  if (warp == 8) tmem_dealloc(tmem, 256);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
