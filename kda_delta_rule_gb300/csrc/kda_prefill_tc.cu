@@ -510,15 +510,18 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 }
 
 // ---- chain kernel -------------------------------------------------------------
-// One CTA per (sequence, head, 64-column slice of dv), nine warps.  Warp 8
-// issues every tensor-core product and every image copy; warps 0-7 do the
+// One CTA per (sequence, head, 64-column slice of dv), ten warps.  Warp 9
+// issues every tensor-core product and every image copy (it shares a
+// scheduler with warps 1 and 5, which wait on the products it issues; warp 8
+// only pads the block to put it there); warps 0-7 do the
 // per-row work, warps w and w + 4 sharing TMEM lane quadrant w % 4 and taking
 // the left and right 32 columns of its rows.  Hand-offs go through mbarriers
 // only:  bar1 / bar3 / bar2 (product commits), dready (Delta' written by warps
 // 0, 1, 4, 5) and sready (chunk done by warps 0-7: state written, TMEM and
 // stage reads finished, the output rows of the chunk in registers).
 constexpr int DVS = 64;                            // state columns per CTA
-constexpr int CNT = 288;                           // chain threads: 8 row warps + 1 issuing warp
+constexpr int CNT = 320;                           // chain threads: 8 row warps, 1 idle, 1 issuing
+constexpr int ISSUER = 9;                          // the issuing warp
 constexpr int CRW = 256;                           // row threads
 constexpr uint32_t S_WQ = 0, S_KB = 32768, S_PB = 49152, S_U = 65536, S_EG = 73728;
 constexpr uint32_t STAGE = 75776;                 // 74 KB, keeps every stage 1024-aligned
@@ -565,7 +568,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     *s_abort = 0;
     mbar_init_fence();
   }
-  if (warp == 8) tmem_alloc(smem_u32(tslot), 256);
+  if (warp == ISSUER) tmem_alloc(smem_u32(tslot), 256);
   // zero rows 0-63 of both [0; P] buffers (never written by the copies)
   for (int e = tid; e < 2 * 512; e += CNT) {
     const int s = e >> 9, o = e & 511;
@@ -596,7 +599,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   constexpr uint32_t ID_1 = idesc_bf16(128, DVS, false, true);   // [-bW; Qt] (K-major) x S (MN-major)
   constexpr uint32_t ID_3 = idesc_bf16(128, DVS, true, true);    // Kbar^T (MN-major) x Delta' (MN-major)
 
-  if (warp == 8) {
+  if (warp == ISSUER) {
     // ---- issuing warp ----------------------------------------------------------
     auto copy = [&](int cidx) {                                    // lane 0 only
       const int s = cidx & 1;
@@ -689,7 +692,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       if (last1 >= 0) mbar_wait(bar1, (uint32_t)(last1 & 1));
       if (last2 >= 0) { mbar_wait(bar3, (uint32_t)(last2 & 1)); mbar_wait(bar2, (uint32_t)(last2 & 1)); }
     }
-  } else {
+  } else if (warp < 8) {
     // ---- row warps -------------------------------------------------------------
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
     const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
@@ -806,7 +809,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
 #pragma unroll
     for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
   }
-  if (warp == 8) tmem_dealloc(tmem, 256);
+  if (warp == ISSUER) tmem_dealloc(tmem, 256);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
