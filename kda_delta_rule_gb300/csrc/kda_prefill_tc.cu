@@ -56,8 +56,8 @@ __host__ __device__ constexpr uint32_t img_bytes(int dv) { return img_eg(dv) + 5
 
 // ---- prep kernel shared memory ---------------------------------------------
 constexpr int PNT = 256;                // prep threads: 64 channel pairs x 4 blocks of 16 tokens
-constexpr uint32_t P_KHAT = 0;          // 16 KB  Khat K-major [64][128]; later XT scratch
-constexpr uint32_t P_APB = 16384;       // 33 KB  [X; Y] K-major [128][128]; later A, T fp32 [64][65]
+constexpr uint32_t P_KHAT = 0;          // 16 KB  Khat K-major [64][128]; later T fp32 [64][68] (into APB)
+constexpr uint32_t P_APB = 16384;       // 33 KB  [X; Y] K-major [128][128]; later A fp32 [64][65], XT
 constexpr uint32_t P_KTIL = 50176;      // 16 KB  k e^{G} MN-major (mn = dk, K = 64)
 constexpr uint32_t P_R1 = 66560;        // 32 KB  g tile; then [Khat_1; Khat_2; Khat_3]; then V + TOP
 constexpr uint32_t P_KHS = P_R1;        // 24 KB  Khat_1, Khat_2, Khat_3 stacked: K-major [96][128]
@@ -109,7 +109,11 @@ struct PrepMaps {
   CUtensorMap k, q, g, v;
 };
 
-template <int DV>
+constexpr int TS = 68;                  // row stride of T in floats (16-byte rows)
+constexpr uint32_t P_AF = P_APB + 1024;   // A fp32 [64][65] (T runs 1 KB into APB)
+constexpr uint32_t P_XT = P_AF + 16640;   // X blocks of one level, fp32 [3][16][16]
+
+template <int DV, bool DECAY_FIRST>
 __global__ void __launch_bounds__(PNT, 2)
 kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned char* __restrict__ ws,
                       const __grid_constant__ PrepMaps maps) {
@@ -129,7 +133,7 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   const int c = chunk - sched.chunk_base[n];
   const int64_t t0 = (int64_t)sched.start[n] + (int64_t)c * C;
   const int L = min(C, sched.len[n] - c * C);
-  const bool decay_first = a.mode == KDA_MODE_DECAY_FIRST;
+  constexpr bool decay_first = DECAY_FIRST;
   unsigned char* img = ws + ((int64_t)chunk * H + h) * img_bytes(DV);
   const __nv_bfloat16* bg = reinterpret_cast<const __nv_bfloat16*>(a.beta);
 
@@ -307,8 +311,8 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 
   // ---- read A (lanes 0-63) and P (lanes 64-127); warps w and w + 4 share a
   // lane quadrant and take the left and right columns of its rows.
-  float* AF = reinterpret_cast<float*>(sm + P_APB);            // [64][65]
-  float* TF = AF + 64 * 65;                                     // [64][65]
+  float* AF = reinterpret_cast<float*>(sm + P_AF);             // [64][65]
+  float* TF = reinterpret_cast<float*>(sm + P_KHAT);           // [64][TS]
   if (ok) {
     const int qd = warp & 3, hw = warp >> 2;
     const bool lo = lane < 16;
@@ -356,7 +360,7 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int s = s0 + e;
-        if (e < nv && s < r) AF[r * 65 + s] = s_beta[s] * v[e];
+        if (e < nv) AF[r * 65 + s] = s_beta[s] * v[e];   // entries with s >= r are never read
       }
     } else {
 #pragma unroll
@@ -375,7 +379,7 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       }
     }
   }
-  for (int e = tid; e < 64 * 65; e += PNT) TF[e] = 0.f;
+  for (int e = tid; e < 64 * TS / 4; e += PNT) reinterpret_cast<float4*>(TF)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   fence_before();
   __syncthreads();
   fence_after();
@@ -398,43 +402,50 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       x[j] = j == cc ? 1.f : (j < cc ? 0.f : -(e0 + e1));
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) TF[(b0 + j) * 65 + b0 + cc] = x[j];
+    for (int j = 0; j < 16; ++j) TF[(b0 + j) * TS + b0 + cc] = x[j];
   }
   __syncthreads();
-  float* XT = reinterpret_cast<float*>(sm + P_KHAT);             // [3][16][16]
+  float* XT = reinterpret_cast<float*>(sm + P_XT);               // [3][16][16]
   // level d: blocks (I, J = I - d) from the blocks already known
   //   X = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II X
+  // one thread per row and 4 columns of a block (J, row ar, columns 4 bq ..)
 #pragma unroll
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;
+    const int J = tid >> 6, ar = (tid >> 2) & 15, bq = tid & 3, I = J + d;
+    if (tid < 64 * nb) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int m = 0; m < (nb * 256 + PNT - 1) / PNT; ++m) {
-      const int e = tid + m * PNT;
-      if (e < nb * 256) {
-        const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
-        float a4[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int kk = 0; kk < d; ++kk) {
+        const int K = J + kk;
 #pragma unroll
-        for (int kk = 0; kk < d; ++kk) {
-          const int K = J + kk;
-#pragma unroll
-          for (int s2 = 0; s2 < 16; ++s2)
-            a4[s2 & 3] = fmaf(AF[(16 * I + ar) * 65 + 16 * K + s2], TF[(16 * K + s2) * 65 + 16 * J + bc], a4[s2 & 3]);
+        for (int s2 = 0; s2 < 16; ++s2) {
+          const float av = AF[(16 * I + ar) * 65 + 16 * K + s2];
+          const float4 t4 = *reinterpret_cast<const float4*>(TF + (16 * K + s2) * TS + 16 * J + 4 * bq);
+          acc.x = fmaf(av, t4.x, acc.x);
+          acc.y = fmaf(av, t4.y, acc.y);
+          acc.z = fmaf(av, t4.z, acc.z);
+          acc.w = fmaf(av, t4.w, acc.w);
         }
-        XT[e] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
       }
+      *reinterpret_cast<float4*>(XT + (J << 8) + ar * 16 + 4 * bq) = acc;
     }
     __syncthreads();
+    if (tid < 64 * nb) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int m = 0; m < (nb * 256 + PNT - 1) / PNT; ++m) {
-      const int e = tid + m * PNT;
-      if (e < nb * 256) {
-        const int J = e >> 8, ar = (e >> 4) & 15, bc = e & 15, I = J + d;
-        float a4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2)
-          if (s2 <= ar) a4[s2 & 3] = fmaf(TF[(16 * I + ar) * 65 + 16 * I + s2], XT[(J << 8) + s2 * 16 + bc], a4[s2 & 3]);
-        TF[(16 * I + ar) * 65 + 16 * J + bc] = -((a4[0] + a4[1]) + (a4[2] + a4[3]));
+      for (int s2 = 0; s2 < 16; ++s2) {
+        if (s2 <= ar) {
+          const float tv = TF[(16 * I + ar) * TS + 16 * I + s2];
+          const float4 x4 = *reinterpret_cast<const float4*>(XT + (J << 8) + s2 * 16 + 4 * bq);
+          acc.x = fmaf(tv, x4.x, acc.x);
+          acc.y = fmaf(tv, x4.y, acc.y);
+          acc.z = fmaf(tv, x4.z, acc.z);
+          acc.w = fmaf(tv, x4.w, acc.w);
+        }
       }
+      *reinterpret_cast<float4*>(TF + (16 * I + ar) * TS + 16 * J + 4 * bq) =
+          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
   }
@@ -444,9 +455,9 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     const int r = tid & 127, c32 = 32 * (tid >> 7);
 #pragma unroll
     for (int cch = 0; cch < 4; ++cch) {
-      float t8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) t8[e] = TF[(r & 63) * 65 + c32 + 8 * cch + e];
+      const float4 lo = *reinterpret_cast<const float4*>(TF + (r & 63) * TS + c32 + 8 * cch);
+      const float4 hi = *reinterpret_cast<const float4*>(TF + (r & 63) * TS + c32 + 8 * cch + 4);
+      const float t8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
       *reinterpret_cast<uint4*>(sm + P_TOP + off_k(r, c32 + 8 * cch, 128)) = pack8(t8);
     }
   }
@@ -852,7 +863,7 @@ cudaError_t launch_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned 
         !make_map(&maps.g, a.g, a.T, (int64_t)a.H * DKT, DKT, false) ||
         !make_map(&maps.v, a.v, a.T, (int64_t)a.H * DV, 64, true))
       return cudaErrorInvalidValue;
-    auto prep = kda_chunk_prep_kernel<DV>;
+    auto prep = a.mode == KDA_MODE_DECAY_FIRST ? kda_chunk_prep_kernel<DV, true> : kda_chunk_prep_kernel<DV, false>;
     e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
     if (e != cudaSuccess) return e;
     prep<<<(unsigned)((int64_t)a.H * total_chunks), PNT, P_SMEM, s>>>(a, sched, ws, maps);
