@@ -69,6 +69,24 @@ constexpr uint32_t P_SMEM = P_PART + 4096 + 1024;
 
 __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
+constexpr float kLog2e = 1.4426950408889634f;
+// 2^x with the hardware approximation (relative error ~2^-22); subnormal results
+// are kept: a cross-block factor can be subnormal while its product with a
+// large in-block factor is not
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// The same where the result is known to be normal: in-block factors
+// e^{+-(Gamma_r - Gamma_m)} with |Gamma_r - Gamma_m| <= 8 |g_min| log2(e) < 126
+// for g >= -10.
+__device__ __forceinline__ float ex2_normal(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint4 pack8(const float* v) {
   uint4 u;
   __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
@@ -170,16 +188,18 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   ok = cta_wait(mbar_in, 0);
   // Pass 1: sums of the block's 16 gates up to its reference token (the 8th)
   // and in total, exchanged so every thread has the cumsum at all four
-  // reference tokens, at the end of the chunk and before its own block.
-  float2 graw[16];
+  // reference tokens, at the end of the chunk and before its own block.  All
+  // cumsums are kept in log2 units (g log2(e)), so every factor is one ex2.
+  float2 gl[16];
   {
     float a0 = 0.f, a1 = 0.f, p0 = 0.f, p1 = 0.f;
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
       const int r = 16 * qb + rr;
-      graw[rr] = r < L ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
-      a0 += graw[rr].x;
-      a1 += graw[rr].y;
+      const float2 gv = r < L ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
+      gl[rr] = make_float2(gv.x * kLog2e, gv.y * kLog2e);
+      a0 += gl[rr].x;
+      a1 += gl[rr].y;
       if (rr == 7) { p0 = a0; p1 = a1; }
     }
     part[qb * 64 + pch] = make_float4(p0, p1, a0, a1);
@@ -207,46 +227,49 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       const float gR1 = R == 1 ? gm[1][1] : (R == 2 ? gm[2][1] : gm[3][1]);
       const float gS0 = S == 0 ? gm[0][0] : (S == 1 ? gm[1][0] : gm[2][0]);
       const float gS1 = S == 0 ? gm[0][1] : (S == 1 ? gm[1][1] : gm[2][1]);
-      fac2[idx * 64 + pch] = __floats2bfloat162_rn(__expf(gR0 - gS0), __expf(gR1 - gS1));
+      fac2[idx * 64 + pch] = __floats2bfloat162_rn(ex2(gR0 - gS0), ex2(gR1 - gS1));
     }
   } else {
-    *reinterpret_cast<float2*>(img + img_eg(DV) + 4 * c0) = make_float2(__expf(GC[0]), __expf(GC[1]));
+    *reinterpret_cast<float2*>(img + img_eg(DV) + 4 * c0) = make_float2(ex2(GC[0]), ex2(GC[1]));
   }
 
-  // Pass 2: every gated operand of the chunk for this thread's 16 tokens.
+  // Pass 2: every gated operand of the chunk for this thread's 16 tokens.  Row r
+  // of Khat, k e^{G} and the image's Kbar share one offset (a [64][128] tile is
+  // laid out alike K-major and MN-major), as do Y and the image's q e^{Gamma}.
   {
     const float gmq0 = qb == 0 ? gm[0][0] : (qb == 1 ? gm[1][0] : (qb == 2 ? gm[2][0] : gm[3][0]));
     const float gmq1 = qb == 0 ? gm[0][1] : (qb == 1 ? gm[1][1] : (qb == 2 ? gm[2][1] : gm[3][1]));
-    const float em0 = __expf(gmq0), em1 = __expf(gmq1);                  // e^{Gamma_m}
-    const float ec0 = __expf(GC[0] - gmq0), ec1 = __expf(GC[1] - gmq1);  // e^{Gamma_C - Gamma_m}
-    float ac0 = acc0[0], ac1 = acc0[1];
+    const float em0 = ex2(gmq0), em1 = ex2(gmq1);                    // e^{Gamma_m}
+    const float ec0 = ex2(GC[0] - gmq0), ec1 = ex2(GC[1] - gmq1);    // e^{Gamma_C - Gamma_m}
+    auto rows = [&](auto full_tag) {
+      constexpr bool FULL = decltype(full_tag)::value;              // no token past the end
+      float ac0 = acc0[0] - gmq0, ac1 = acc0[1] - gmq1;             // Gamma - Gamma_m, log2 units
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) {
-      const int r = 16 * qb + rr;
-      const bool in = r < L;
-      const uint32_t ox = off_k(r, c0, 128), oy = off_k(64 + r, c0, 128);
-      __nv_bfloat162* xp = reinterpret_cast<__nv_bfloat162*>(sm + P_APB + ox);
-      __nv_bfloat162* yp = reinterpret_cast<__nv_bfloat162*>(sm + P_APB + oy);
-      const float2 kv = in ? __bfloat1622float2(*xp) : make_float2(0.f, 0.f);
-      const float2 qv = in ? __bfloat1622float2(*yp) : make_float2(0.f, 0.f);
-      const float p0 = ac0, p1 = ac1;             // Gamma_{r-1}
-      ac0 += graw[rr].x;                          // Gamma_r
-      ac1 += graw[rr].y;
-      const float d0 = ac0 - gmq0, d1 = ac1 - gmq1;
-      const float E0 = __expf(d0), E1 = __expf(d1), Ei0 = __expf(-d0), Ei1 = __expf(-d1);
-      const float EG0 = decay_first ? E0 : __expf(p0 - gmq0);
-      const float EG1 = decay_first ? E1 : __expf(p1 - gmq1);
-      *reinterpret_cast<__nv_bfloat162*>(sm + P_KHAT + off_k(r, c0, 64)) =
-          __floats2bfloat162_rn(kv.x * Ei0, kv.y * Ei1);
-      *reinterpret_cast<__nv_bfloat162*>(sm + P_KTIL + off_mn(c0, r, 64)) =
-          __floats2bfloat162_rn(kv.x * EG0 * em0, kv.y * EG1 * em1);
-      *reinterpret_cast<__nv_bfloat162*>(img + IMG_WQ + oy) =
-          __floats2bfloat162_rn(qv.x * E0 * em0, qv.y * E1 * em1);
-      *reinterpret_cast<__nv_bfloat162*>(img + IMG_KB + off_mn(c0, r, 64)) =
-          __floats2bfloat162_rn(kv.x * Ei0 * ec0, kv.y * Ei1 * ec1);
-      *xp = __floats2bfloat162_rn(kv.x * EG0, kv.y * EG1);     // X = k e^{G - Gamma_m}
-      *yp = __floats2bfloat162_rn(qv.x * E0, qv.y * E1);       // Y = q e^{Gamma - Gamma_m}
-    }
+      for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * qb + rr;
+        const bool in = FULL || r < L;
+        const uint32_t ox = off_k(r, c0, 128), oy = off_k(64 + r, c0, 128), o64 = off_k(r, c0, 64);
+        __nv_bfloat162* xp = reinterpret_cast<__nv_bfloat162*>(sm + P_APB + ox);
+        __nv_bfloat162* yp = reinterpret_cast<__nv_bfloat162*>(sm + P_APB + oy);
+        const float2 kv = in ? __bfloat1622float2(*xp) : make_float2(0.f, 0.f);
+        const float2 qv = in ? __bfloat1622float2(*yp) : make_float2(0.f, 0.f);
+        const float p0 = ac0, p1 = ac1;             // Gamma_{r-1} - Gamma_m
+        ac0 += gl[rr].x;                            // Gamma_r - Gamma_m
+        ac1 += gl[rr].y;
+        const float E0 = ex2_normal(ac0), E1 = ex2_normal(ac1), Ei0 = ex2_normal(-ac0), Ei1 = ex2_normal(-ac1);
+        const float EG0 = decay_first ? E0 : ex2_normal(p0), EG1 = decay_first ? E1 : ex2_normal(p1);
+        const float Fq0 = E0 * em0, Fq1 = E1 * em1;       // e^{Gamma}
+        const float Fg0 = EG0 * em0, Fg1 = EG1 * em1;     // e^{G}
+        const float Fc0 = Ei0 * ec0, Fc1 = Ei1 * ec1;     // e^{Gamma_C - Gamma}
+        *reinterpret_cast<__nv_bfloat162*>(sm + P_KHAT + o64) = __floats2bfloat162_rn(kv.x * Ei0, kv.y * Ei1);
+        *reinterpret_cast<__nv_bfloat162*>(sm + P_KTIL + o64) = __floats2bfloat162_rn(kv.x * Fg0, kv.y * Fg1);
+        *reinterpret_cast<__nv_bfloat162*>(img + IMG_WQ + oy) = __floats2bfloat162_rn(qv.x * Fq0, qv.y * Fq1);
+        *reinterpret_cast<__nv_bfloat162*>(img + IMG_KB + o64) = __floats2bfloat162_rn(kv.x * Fc0, kv.y * Fc1);
+        *xp = __floats2bfloat162_rn(kv.x * EG0, kv.y * EG1);     // X = k e^{G - Gamma_m}
+        *yp = __floats2bfloat162_rn(qv.x * E0, qv.y * E1);       // Y = q e^{Gamma - Gamma_m}
+      }
+    };
+    if (L == C) rows(std::true_type{}); else rows(std::false_type{});
   }
   fence_async_smem();
   fence_before();
