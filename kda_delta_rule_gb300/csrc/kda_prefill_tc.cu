@@ -546,8 +546,9 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 // ---- chain kernel -------------------------------------------------------------
 // One CTA per (sequence, head, 64-column slice of dv), ten warps.  Warp 9
 // issues every tensor-core product and every image copy (it shares a
-// scheduler with warps 1 and 5, which wait on the products it issues; warp 8
-// only pads the block to put it there); warps 0-7 do the
+// scheduler with warps 1 and 5, which wait on the products it issues); warp 8
+// writes checkpoint pages from a staging buffer the row warps fill, so no
+// global store precedes a hand-off on the critical path; warps 0-7 do the
 // per-row work, warps w and w + 4 sharing TMEM lane quadrant w % 4 and taking
 // the left and right 32 columns of its rows.  Hand-offs go through mbarriers
 // only:  bar1 / bar3 / bar2 (product commits), dready (Delta' written by warps
@@ -562,7 +563,9 @@ constexpr uint32_t STAGE = 75776;                 // 74 KB, keeps every stage 10
 constexpr uint32_t C_DELTA = 2 * STAGE;           // 8 KB  Delta' MN-major (mn = 64 cols, K = 64 tokens)
 constexpr uint32_t C_SB = C_DELTA + 8192;         // 16 KB S bf16 MN-major (mn = 64 cols, K = 128)
 constexpr uint32_t C_MISC = C_SB + 16384;
-constexpr uint32_t C_SMEM = C_MISC + 128 + 1024;
+constexpr uint32_t C_CK = C_MISC + 128;           // 34 KB checkpoint staging: fp32 [128 rows][64], rows 272 B apart
+constexpr uint32_t CK_ROW = 272;
+constexpr uint32_t C_SMEM = C_CK + 128 * CK_ROW + 1024;
 constexpr uint32_t CHUNK_TX = 32768 + 16384 + 8192 + 8192 + 512;
 
 template <int DV>
@@ -577,6 +580,8 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   const uint32_t dready = smem_u32(sm + C_MISC + 40);   // Delta' in shared memory (4 warps)
   const uint32_t sready = smem_u32(sm + C_MISC + 48);   // chunk finished by the row warps (8 warps)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C_MISC + 64);
+  const uint32_t ckfull = smem_u32(sm + C_MISC + 88);   // staging filled (8 row warps)
+  const uint32_t ckfree = smem_u32(sm + C_MISC + 96);   // staging written out (warp 8)
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + C_MISC + 72);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -599,6 +604,8 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     mbar_init(bar2, 1);
     mbar_init(dready, 4);
     mbar_init(sready, 8);
+    mbar_init(ckfull, 8);
+    mbar_init(ckfree, 1);
     *s_abort = 0;
     mbar_init_fence();
   }
@@ -726,12 +733,41 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       if (last1 >= 0) mbar_wait(bar1, (uint32_t)(last1 & 1));
       if (last2 >= 0) { mbar_wait(bar3, (uint32_t)(last2 & 1)); mbar_wait(bar2, (uint32_t)(last2 & 1)); }
     }
+  } else if (warp == 8) {
+    // ---- checkpoint writer: each staged checkpoint, 128 rows of 256 bytes --------
+    const int ck_every = a.ckpt_stride > 0 ? a.ckpt_stride / C : 0;
+    int k = 0;
+    if (ck_every > 0) {
+      for (int c = ck_every - 1; c < nch; c += ck_every) {
+        const int L = min(C, len - c * C);
+        if (L != C) break;
+        const int64_t idx = (int64_t)sched.ckpt_base[n] + (c * C + L) / a.ckpt_stride - 1;
+        if (idx >= a.num_ckpt) break;
+        const int32_t page_id = a.ckpt_page_ids[idx];
+        bool w = false;
+        while (!w && !*s_abort) w = __all_sync(0xffffffffu, mbar_wait(ckfull, (uint32_t)(k & 1)));
+        if (!w) break;
+        char* page = a.page_pool + (int64_t)page_id * a.page_bytes;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int row = lane + 32 * q4;
+          bulk_s2g(page + (((int64_t)h * DKT + row) * DV + col0) * 4, smem_u32(sm + C_CK + row * CK_ROW), DVS * 4);
+        }
+        bulk_commit();
+        bulk_wait_read_all();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ckfree);
+        ++k;
+      }
+    }
+    bulk_wait_all();
   } else if (warp < 8) {
     // ---- row warps -------------------------------------------------------------
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
     const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
     const int ck_every = a.ckpt_stride > 0 ? a.ckpt_stride / C : 0;
     int ck_left = ck_every;
+    int n_ck = 0;                          // checkpoints staged so far
     auto row_step = [&](auto stage_tag, int c) -> bool {
       constexpr int s = decltype(stage_tag)::value;
       const uint32_t ph = (uint32_t)(c & 1);
@@ -785,20 +821,25 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       const int L = min(C, len - c * C);
       const int pos = c * C + L;
       // a checkpoint ends every ckpt_stride / C full chunks (a partial chunk
-      // never ends on a multiple of the stride)
+      // never ends on a multiple of the stride); its rows go to the staging
+      // buffer once warp 8 has written out the previous checkpoint
       const bool ck = ck_every > 0 && --ck_left == 0;
       if (ck) ck_left = ck_every;
       if (ck && L == C) {
         const int64_t idx = (int64_t)sched.ckpt_base[n] + pos / a.ckpt_stride - 1;
         if (idx < a.num_ckpt) {
-          float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
-          float* prow = page + ((int64_t)h * DKT + i) * DV + col0 + jc;
+          if (n_ck > 0 && !__all_sync(0xffffffffu, mbar_wait(ckfree, (uint32_t)((n_ck - 1) & 1)))) return false;
+          float4* srow = reinterpret_cast<float4*>(sm + C_CK + i * CK_ROW + jc * 4);
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(prow + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+          for (int j = 0; j < 8; ++j) srow[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ckfull);
+          ++n_ck;
           if (h == 0 && sl == 0) {
+            float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
             const int64_t used = (int64_t)H * DKT * DV, total = a.page_bytes / 4;
-            for (int64_t e = used + tid; e < total; e += CRW) page[e] = 0.f;
+            for (int64_t e = used + tid; e < total; e += CRW) page[e] = 0.f;   // pad past the state
             if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = pos;
           }
         }

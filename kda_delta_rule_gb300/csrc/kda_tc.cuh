@@ -186,6 +186,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
       :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
+// shared -> global bulk copy tracked by bulk groups (16-byte aligned ends, size a multiple of 16)
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               :: "l"(dst), "r"(src_smem), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk groups have finished reading shared memory / have completed
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void st_bf16(unsigned char* base, uint32_t off, float x) {
   *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(x);
 }
