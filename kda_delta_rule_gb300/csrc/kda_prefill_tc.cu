@@ -129,7 +129,7 @@ struct PrepMaps {
 
 constexpr int TS = 68;                  // row stride of T in floats (16-byte rows)
 constexpr uint32_t P_AF = P_APB + 1024;   // A fp32 [64][65] (T runs 1 KB into APB)
-constexpr uint32_t P_XT = P_AF + 16640;   // X blocks of one level, fp32 [3][16][16]
+constexpr uint32_t P_XT = P_AF + 16640;   // intermediate products of the UT solve, fp32 [6][16][16]
 
 template <int DV, bool DECAY_FIRST>
 __global__ void __launch_bounds__(PNT, 2)
@@ -428,50 +428,78 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     for (int j = 0; j < 16; ++j) TF[(b0 + j) * TS + b0 + cc] = x[j];
   }
   __syncthreads();
-  float* XT = reinterpret_cast<float*>(sm + P_XT);               // [3][16][16]
-  // level d: blocks (I, J = I - d) from the blocks already known
-  //   X = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II X
-  // one thread per row and 4 columns of a block (J, row ar, columns 4 bq ..)
+  // Off-diagonal blocks by 2x2 doubling: T = [[T1, 0], [-T2 A21 T1, T2]] on the
+  // 32x32 halves, whose own off-diagonal blocks come first the same way.
+  // XT slots [6][16][16]: 0 A10 T00, 1 A32 T22, 2 A21 T11, 3 A31 T11, 4 A20 T00
+  // (+ A21 T10), 5 A30 T00 (+ A31 T10).  One thread per row and 4 columns.
+  float* XT = reinterpret_cast<float*>(sm + P_XT);
+  auto a_t = [&](int I, int K, int J, int ar, int bq, float4 acc) {   // acc += A_IK T_KJ (row ar, cols 4bq..)
 #pragma unroll
-  for (int d = 1; d < 4; ++d) {
-    const int nb = 4 - d;
-    const int J = tid >> 6, ar = (tid >> 2) & 15, bq = tid & 3, I = J + d;
-    if (tid < 64 * nb) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int kk = 0; kk < d; ++kk) {
-        const int K = J + kk;
-#pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2) {
-          const float av = AF[(16 * I + ar) * 65 + 16 * K + s2];
-          const float4 t4 = *reinterpret_cast<const float4*>(TF + (16 * K + s2) * TS + 16 * J + 4 * bq);
-          acc.x = fmaf(av, t4.x, acc.x);
-          acc.y = fmaf(av, t4.y, acc.y);
-          acc.z = fmaf(av, t4.z, acc.z);
-          acc.w = fmaf(av, t4.w, acc.w);
-        }
-      }
-      *reinterpret_cast<float4*>(XT + (J << 8) + ar * 16 + 4 * bq) = acc;
+    for (int s2 = 0; s2 < 16; ++s2) {
+      const float av = AF[(16 * I + ar) * 65 + 16 * K + s2];
+      const float4 t4 = *reinterpret_cast<const float4*>(TF + (16 * K + s2) * TS + 16 * J + 4 * bq);
+      acc.x = fmaf(av, t4.x, acc.x); acc.y = fmaf(av, t4.y, acc.y);
+      acc.z = fmaf(av, t4.z, acc.z); acc.w = fmaf(av, t4.w, acc.w);
     }
-    __syncthreads();
-    if (tid < 64 * nb) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    return acc;
+  };
+  auto t_x = [&](int I, int L, int slot, int ar, int bq, bool tri, float4 acc) {   // acc += T_IL X_slot
 #pragma unroll
-      for (int s2 = 0; s2 < 16; ++s2) {
-        if (s2 <= ar) {
-          const float tv = TF[(16 * I + ar) * TS + 16 * I + s2];
-          const float4 x4 = *reinterpret_cast<const float4*>(XT + (J << 8) + s2 * 16 + 4 * bq);
-          acc.x = fmaf(tv, x4.x, acc.x);
-          acc.y = fmaf(tv, x4.y, acc.y);
-          acc.z = fmaf(tv, x4.z, acc.z);
-          acc.w = fmaf(tv, x4.w, acc.w);
-        }
+    for (int s2 = 0; s2 < 16; ++s2) {
+      if (!tri || s2 <= ar) {
+        const float tv = TF[(16 * I + ar) * TS + 16 * L + s2];
+        const float4 x4 = *reinterpret_cast<const float4*>(XT + slot * 256 + s2 * 16 + 4 * bq);
+        acc.x = fmaf(tv, x4.x, acc.x); acc.y = fmaf(tv, x4.y, acc.y);
+        acc.z = fmaf(tv, x4.z, acc.z); acc.w = fmaf(tv, x4.w, acc.w);
       }
-      *reinterpret_cast<float4*>(TF + (16 * I + ar) * TS + 16 * J + 4 * bq) =
-          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
-    __syncthreads();
+    return acc;
+  };
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int ar = (tid >> 2) & 15, bq = tid & 3, blk = tid >> 6;
+  auto put = [&](float* base, float4 v) { *reinterpret_cast<float4*>(base) = v; };
+  auto neg = [](float4 v) { return make_float4(-v.x, -v.y, -v.z, -v.w); };
+  // 1: products of A with diagonal blocks only (six blocks, two per thread for tid < 128)
+  {
+    const int I1[4] = {1, 3, 2, 3}, K1[4] = {0, 2, 1, 1}, J1[4] = {0, 2, 1, 1};
+    float4 r = z4;
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      if (blk == b) r = a_t(I1[b], K1[b], J1[b], ar, bq, z4);
+    put(XT + blk * 256 + ar * 16 + 4 * bq, r);
+    if (tid < 128) {
+      const int I = blk == 0 ? 2 : 3;                        // slots 4 and 5: A20 T00, A30 T00
+      put(XT + (4 + blk) * 256 + ar * 16 + 4 * bq, a_t(I, 0, 0, ar, bq, z4));
+    }
   }
+  __syncthreads();
+  // 2: T10 = -T11 (A10 T00), T32 = -T33 (A32 T22)
+  if (tid < 128) {
+    const int I = blk == 0 ? 1 : 3, J = I - 1;
+    put(TF + (16 * I + ar) * TS + 16 * J + 4 * bq, neg(t_x(I, I, blk, ar, bq, true, z4)));
+  }
+  __syncthreads();
+  // 3: slots 4, 5 += A21 T10, A31 T10
+  if (tid < 128) {
+    const int I = blk == 0 ? 2 : 3;
+    float* xp = XT + (4 + blk) * 256 + ar * 16 + 4 * bq;
+    put(xp, a_t(I, 1, 0, ar, bq, *reinterpret_cast<const float4*>(xp)));
+  }
+  __syncthreads();
+  // 4: T20 = -T22 X20, T21 = -T22 X21, T30 = -(T32 X20 + T33 X30), T31 = -(T32 X21 + T33 X31)
+  {
+    const int I = blk < 2 ? 2 : 3, J = blk & 1;
+    const int sx2 = J == 0 ? 4 : 2, sx3 = J == 0 ? 5 : 3;   // X_2J and X_3J slots
+    float4 r;
+    if (I == 2) {
+      r = t_x(2, 2, sx2, ar, bq, true, z4);
+    } else {
+      r = t_x(3, 2, sx2, ar, bq, false, z4);
+      r = t_x(3, 3, sx3, ar, bq, true, r);
+    }
+    put(TF + (16 * I + ar) * TS + 16 * J + 4 * bq, neg(r));
+  }
+  __syncthreads();
 
   // ---- [T; T] as bf16 A operand (the copy feeds lanes 64-127) -----------------
   {
