@@ -321,6 +321,63 @@ def bench_replay(K, dev, warmup=3, runs=5):
     b.record(stream)
     torch.cuda.synchronize(dev)
     amort_ms = a.elapsed_time(b) / (runs * REP_SETS)
+    # the same 64 calls captured once in a CUDA graph: one launch replays them all,
+    # so the per-call figure is the kernels' own time on states that miss L2
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for s in sets:                 # warm the capture stream once
+                K.kda_verify_replay(s[0], s[1].q, s[1].k, s[1].v, s[1].g, s[1].beta, s[2], S_new=s[3], out=s[4],
+                                    stream=cap)
+        cap.synchronize()
+        with torch.cuda.graph(g, stream=cap):
+            for s in sets:
+                K.kda_verify_replay(s[0], s[1].q, s[1].k, s[1].v, s[1].g, s[1].beta, s[2], S_new=s[3], out=s[4],
+                                    stream=cap)
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        x, y = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x.record(stream)
+        for _ in range(runs):
+            g.replay()
+        y.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_ms = x.elapsed_time(y) / (runs * REP_SETS)
+    except Exception as e:                 # capture unsupported: report the stream figure only
+        print(f"replay graph capture failed: {e}", file=sys.stderr)
+    # the same 64 states as the KDA layers of one model: one launch replays them all
+    # (each layer its own state and draft projections, the accepted counts shared)
+    layers_ms, layers_bytes = None, None
+    try:
+        n_acc = sets[0][2]
+        S_l = torch.stack([s_[0] for s_ in sets])
+        pj = {nm: torch.stack([getattr(s_[1], nm) for s_ in sets]) for nm in ("q", "k", "v", "g", "beta")}
+        S_lnew = torch.empty_like(S_l)
+        out_l = torch.empty(REP_SETS, REP_B, REP_H, REP_DRAFT, REP_D, device=dev)
+        acc = int(n_acc.sum())
+        layers_bytes = REP_SETS * (2 * sets[0][0].numel() * 4 + acc * REP_H * (3 * REP_D + REP_D + 1) * 4
+                                   + sets[0][4].numel() * 4)
+
+        def call_layers():
+            K.kda_verify_replay_layers(S_l, pj["q"], pj["k"], pj["v"], pj["g"], pj["beta"], n_acc,
+                                       S_new=S_lnew, out=out_l, stream=stream)
+        for _ in range(warmup):
+            call_layers()
+        torch.cuda.synchronize(dev)
+        x, y = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x.record(stream)
+        for _ in range(runs):
+            call_layers()
+        y.record(stream)
+        torch.cuda.synchronize(dev)
+        layers_ms = x.elapsed_time(y) / runs
+        del S_l, pj, S_lnew, out_l
+    except Exception as e:
+        print(f"layered replay failed: {e}", file=sys.stderr)
     single = []
     for s in sets[:16]:
         x, y = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -329,7 +386,7 @@ def bench_replay(K, dev, warmup=3, runs=5):
         y.record(stream)
         torch.cuda.synchronize(dev)
         single.append(x.elapsed_time(y))
-    return amort_ms, n_bytes / REP_SETS, statistics.median(single)
+    return amort_ms, n_bytes / REP_SETS, statistics.median(single), graph_ms, (layers_ms, layers_bytes)
 
 
 # ---------------------------------------------------------------------------
@@ -409,12 +466,23 @@ def main():
                                         f"{DEC_STEPS} consecutive steps",
                             "ms_per_step": dms, "state_GBps": dgbs, "hbm_frac": dgbs / hbm,
                             "bytes_per_step": dbytes, "tokens_per_s": DEC_B / (dms / 1e3)}
-        ams, abytes, single_ms = bench_replay(K, dev)
+        ams, abytes, single_ms, graph_ms, (layers_ms, layers_bytes) = bench_replay(K, dev)
         agbs = abytes / (ams / 1e3) / 1e9
         extras["replay"] = {"workload": f"B={REP_B} H={REP_H} dk=dv={REP_D} draft={REP_DRAFT} fp32, "
                                         f"n_accepted~U{{0..8}}, {REP_SETS} distinct buffer sets",
                             "ms_per_call_amortised": ams, "ms_per_call_single": single_ms,
                             "state_GBps": agbs, "hbm_frac": agbs / hbm, "bytes_per_call": abytes}
+        if graph_ms:
+            ggbs = abytes / (graph_ms / 1e3) / 1e9
+            extras["replay"].update({"ms_per_call_cuda_graph": graph_ms, "state_GBps_cuda_graph": ggbs,
+                                     "hbm_frac_cuda_graph": ggbs / hbm})
+        if layers_ms:
+            lgbs = layers_bytes / (layers_ms / 1e3) / 1e9
+            extras["replay"]["layers_batched"] = {
+                "workload": f"the {REP_SETS} buffer sets as {REP_SETS} stacked KDA layers of one model, "
+                            "one kda_verify_replay_layers launch",
+                "ms_per_launch": layers_ms, "ms_per_layer": layers_ms / REP_SETS,
+                "bytes_per_launch": layers_bytes, "state_GBps": lgbs, "hbm_frac": lgbs / hbm}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt, threads = oracle_sample(heads=2)

@@ -117,6 +117,28 @@ int kda_verify_replay(const float* S_committed, const void* q, const void* k,
                       kda_stream_t stream);
 
 /*
+ * kda_verify_replay_layers -- kda_verify_replay for the KDA layers of one model
+ * in a single launch: every layer replays the same accepted prefix of its own
+ * draft projections from its own committed state.  [SERVE] §1.2 (one
+ * verify_and_replay per KDA layer; the accepted count is per sequence, shared
+ * by the layers).  kda_verify_replay is the case layers = 1.
+ *   S_committed  device fp32 [layers,B,H,dk,dv]       in, never written
+ *   q,k,g        device dtype [layers,draft,B,H,dk]   in (each layer in the
+ *                                                      draft-projection cache layout)
+ *   v            device dtype [layers,draft,B,H,dv]   in
+ *   beta         device dtype [layers,draft,B,H]      in
+ *   n_accepted   device int32 [B]                     in; clamped to [0, draft]
+ *   S_new        device fp32 [layers,B,H,dk,dv]       out
+ *   out          device dtype [layers,B,H,draft,dv]   out, zero for steps >= n_b
+ * Same rules and errors as kda_verify_replay; layers = 0 (or B*H = 0) is a no-op.
+ */
+int kda_verify_replay_layers(int layers, const float* S_committed, const void* q,
+                             const void* k, const void* v, const void* g,
+                             const void* beta, const int32_t* n_accepted, float* S_new,
+                             void* out, int draft, int B, int H, int dk, int dv,
+                             int dtype, int mode, kda_stream_t stream);
+
+/*
  * kda_num_checkpoints -- number of checkpoint states a prefill will emit:
  * sum over sequences of floor(L_n / ckpt_stride). Host only.
  *   cu_seqlens  host int32 [n_seqs+1] or NULL (one sequence of T tokens)

@@ -106,22 +106,23 @@ int kda_decode_step(float* S, const void* q, const void* k, const void* v, const
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = o;
   a.n_accepted = nullptr;
   a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = 1; a.dtype = dtype; a.mode = mode;
+  a.layers = 1;
   a.out_head_stride = dv; a.out_step_stride = 0;
   return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_decode_step launch");
 }
 
 // ---------------------------------------------------------------------------
-int kda_verify_replay(const float* S_committed, const void* q, const void* k, const void* v,
-                      const void* g, const void* beta, const int32_t* n_accepted, float* S_new,
-                      void* out, int draft, int B, int H, int dk, int dv, int dtype, int mode,
-                      kda_stream_t stream) {
+int kda_verify_replay_layers(int layers, const float* S_committed, const void* q, const void* k, const void* v,
+                             const void* g, const void* beta, const int32_t* n_accepted, float* S_new,
+                             void* out, int draft, int B, int H, int dk, int dv, int dtype, int mode,
+                             kda_stream_t stream) {
   if (int st = check_common(dk, dv, dtype, mode)) return st;
-  if (B < 0 || H < 0) return fail(KDA_ERR_SHAPE, "negative B=%d or H=%d", B, H);
+  if (layers < 0 || B < 0 || H < 0) return fail(KDA_ERR_SHAPE, "negative layers=%d, B=%d or H=%d", layers, B, H);
   if (draft < 1 || draft > KDA_MAX_DRAFT)
     return fail(KDA_ERR_SHAPE, "draft=%d outside [1, %d]", draft, KDA_MAX_DRAFT);
-  const int64_t heads = (int64_t)B * H;
+  const int64_t heads = (int64_t)layers * B * H;
   if (heads == 0) return ok();
-  if (heads > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "B*H too large");
+  if (heads > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "layers*B*H too large");
   if (!S_committed || !q || !k || !v || !g || !beta || !n_accepted || !S_new || !out)
     return fail(KDA_ERR_ARG, "null pointer argument");
   if (!aligned16(S_committed) || !aligned16(S_new) || !aligned16(q) || !aligned16(k) ||
@@ -139,8 +140,17 @@ int kda_verify_replay(const float* S_committed, const void* q, const void* k, co
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
   a.n_accepted = n_accepted;
   a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = draft; a.dtype = dtype; a.mode = mode;
+  a.layers = layers;
   a.out_head_stride = (int64_t)draft * dv; a.out_step_stride = dv;
   return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_verify_replay launch");
+}
+
+int kda_verify_replay(const float* S_committed, const void* q, const void* k, const void* v,
+                      const void* g, const void* beta, const int32_t* n_accepted, float* S_new,
+                      void* out, int draft, int B, int H, int dk, int dv, int dtype, int mode,
+                      kda_stream_t stream) {
+  return kda_verify_replay_layers(1, S_committed, q, k, v, g, beta, n_accepted, S_new, out, draft, B, H, dk, dv,
+                                  dtype, mode, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -17,6 +17,7 @@ struct StepArgs {
   void* out;
   const int32_t* n_accepted;   // device [B] or nullptr (all heads run `steps`)
   int B, H, dk, dv, steps, dtype, mode;
+  int layers;                  // stacked layers (replay); states [layers][B][H], projections [layers][steps][B][H]
   int64_t out_head_stride;     // elements between heads in `out`
   int64_t out_step_stride;     // elements between steps in `out`
 };

@@ -64,12 +64,13 @@ kda_step_kernel(const StepArgs a) {
   const int lane = tid & 31, warp = tid >> 5;
   const int c4 = tid % TPR;           // column group: columns 4*c4 .. 4*c4+3
   const int rg = tid / TPR;           // rows rg, rg+RG, ...
-  const int64_t nheads = (int64_t)a.B * a.H;
-  const int64_t head = (int64_t)blockIdx.x * HPC + y;
-  const bool active = head < nheads;
+  const int64_t nheads = (int64_t)a.B * a.H;          // heads of one layer
+  const int64_t head = (int64_t)blockIdx.x * HPC + y;  // over all stacked layers
+  const bool active = head < nheads * a.layers;
+  const int64_t layer = head / nheads, hl = head - layer * nheads;
   // The host picks HPC dividing H, so every head of this CTA belongs to the
-  // same sequence and the step count (and with it every barrier) is uniform.
-  const int b = (int)(((int64_t)blockIdx.x * HPC) / a.H);
+  // same layer and sequence and the step count (and with it every barrier) is uniform.
+  const int b = (int)((((int64_t)blockIdx.x * HPC) % nheads) / a.H);
 
   int n = a.steps;
   if (a.n_accepted != nullptr) {
@@ -103,7 +104,7 @@ kda_step_kernel(const StepArgs a) {
 #pragma unroll
   for (int s = 0; s < MAXS; ++s) {
     const bool live = active && s < n;
-    const int64_t hs = (int64_t)s * nheads + head;      // (step, b, h) flattened
+    const int64_t hs = (layer * a.steps + s) * nheads + hl;   // (layer, step, b, h) flattened
 #pragma unroll
     for (int u = 0; u < EK; ++u) {
       const int i = tid + u * NT;
@@ -245,7 +246,7 @@ cudaError_t launch_dims(const StepArgs& a, cudaStream_t s) {
       if (e != cudaSuccess) return e;
     }
     dim3 block(NT, HPCv);
-    int64_t grid = (nheads + HPCv - 1) / HPCv;
+    int64_t grid = (nheads * a.layers + HPCv - 1) / HPCv;
     kern<<<(unsigned)grid, block, total, s>>>(a);
     return cudaGetLastError();
   };
@@ -280,7 +281,7 @@ cudaError_t launch_t(const StepArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
-  if ((int64_t)a.B * a.H == 0) return cudaSuccess;
+  if ((int64_t)a.B * a.H * a.layers == 0) return cudaSuccess;
   if (a.dtype == KDA_BF16) return launch_t<__nv_bfloat16>(a, s);
   return launch_t<float>(a, s);
 }

@@ -42,6 +42,7 @@ def _load():
         "kda_last_error": ([], ctypes.c_char_p),
         "kda_decode_step": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
         "kda_verify_replay": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
+        "kda_verify_replay_layers": ([I, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
         "kda_num_checkpoints": ([P, I, L, I], L),
         "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, I, P], I),
         "kda_prefill_workspace_bytes": ([P, I, L, I, I, I, I], L),
@@ -153,6 +154,31 @@ def kda_verify_replay(S_committed, q, k, v, g, beta, n_accepted, S_new=None, out
                                   _ptr(n_accepted), _ptr(S_new), _ptr(out), draft, B, H, dk, dv,
                                   code, mode, _stream(stream, S_committed.device)),
            "kda_verify_replay")
+    return S_new, out
+
+
+def kda_verify_replay_layers(S_committed, q, k, v, g, beta, n_accepted, S_new=None, out=None,
+                             mode=DECAY_FIRST, stream=None):
+    """kda_verify_replay for a stack of KDA layers in one launch.
+
+    S_committed (L,B,H,dk,dv) fp32; projections (L,draft,B,H,D); n_accepted int32 (B,) shared
+    by the layers. Returns (S_new (L,B,H,dk,dv), out (L,B,H,draft,dv)).
+    """
+    Lr, B, H, dk, dv = S_committed.shape
+    draft = q.shape[1]
+    _cuda("S_committed", S_committed, torch.float32)
+    code, _, _ = _projections(q, k, v, g, beta, (Lr, draft, B, H))
+    _cuda("n_accepted", n_accepted, torch.int32, (B,))
+    if S_new is None:
+        S_new = torch.empty_like(S_committed)
+    if out is None:
+        out = torch.empty((Lr, B, H, draft, dv), device=S_committed.device, dtype=q.dtype)
+    _cuda("S_new", S_new, torch.float32, (Lr, B, H, dk, dv))
+    _cuda("out", out, q.dtype, (Lr, B, H, draft, dv))
+    _check(_lib.kda_verify_replay_layers(Lr, _ptr(S_committed), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                         _ptr(beta), _ptr(n_accepted), _ptr(S_new), _ptr(out), draft,
+                                         B, H, dk, dv, code, mode, _stream(stream, S_committed.device)),
+           "kda_verify_replay_layers")
     return S_new, out
 
 

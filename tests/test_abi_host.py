@@ -156,6 +156,18 @@ def test_replay_rejects_writing_the_committed_state(K):
     assert f(*args, 17, 2, 2, 32, 32, 0, 0, None) == -2       # draft > 16
 
 
+def test_replay_layers_validation(K):
+    f = K._lib.kda_verify_replay_layers
+    # layers x B x H x 32 x 32 fp32 = 3 x 4096 B per (b, h): S_new inside the stacked S_committed
+    args = [P(0), P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), P(6 << 20), P(4096 * 2),
+            P(7 << 20)]
+    assert f(3, *args, 4, 1, 1, 32, 32, 0, 0, None) == -7
+    args[7] = P(8 << 20)
+    assert f(-1, *args, 4, 1, 1, 32, 32, 0, 0, None) == -2
+    assert f(0, *args, 4, 1, 1, 32, 32, 0, 0, None) == 0      # no layers: no-op
+    assert f(2, *args, 0, 1, 1, 32, 32, 0, 0, None) == -2     # draft 0
+
+
 def test_prefill_validation(K):
     f = K._lib.kda_prefill_chunked
     cu = (ctypes.c_int32 * 3)(0, 100, 228)

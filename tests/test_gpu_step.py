@@ -128,3 +128,27 @@ def test_replay_refuses_in_place(K):
     with pytest.raises(K.KdaError) as e:
         K.kda_verify_replay(Sc, pr.q, pr.k, pr.v, pr.g, pr.beta, n.cuda(), S_new=Sc)
     assert e.value.status == -7
+
+
+@pytest.mark.parametrize("dk,dv,dtype", [(32, 32, torch.float32), (128, 128, torch.bfloat16)])
+def test_replay_layers_match_single_calls_and_oracle(K, dk, dv, dtype):
+    """Three stacked layers in one launch: bit-identical to three single-layer calls,
+    each layer within tolerance of the oracle, committed states untouched."""
+    Lr, B, H, draft = 3, 4, 4, 6
+    sets = [I.replay_inputs(B, H, dk, dv, draft, dtype=dtype, seed=40 + l) for l in range(Lr)]
+    n_acc = sets[0][2].cuda()                      # the accepted count is per sequence, shared
+    S = torch.stack([s[0] for s in sets]).cuda()
+    cat = lambda name: torch.stack([getattr(s[1], name) for s in sets]).cuda()
+    q, k, v, g, beta = (cat(n) for n in ("q", "k", "v", "g", "beta"))
+    snapshot = S.clone()
+    S_new, out = K.kda_verify_replay_layers(S, q, k, v, g, beta, n_acc)
+    torch.cuda.synchronize()
+    assert torch.equal(S, snapshot), "a committed state was written"
+    tol_out = TOL_F32 if dtype == torch.float32 else TOL_BF16_STORED_OUT
+    for l in range(Lr):
+        S1, o1 = K.kda_verify_replay(S[l], q[l], k[l], v[l], g[l], beta[l], n_acc)
+        torch.cuda.synchronize()
+        assert torch.equal(S1, S_new[l]) and torch.equal(o1, out[l])
+        S_ref, out_ref = O.verify_and_replay_batched(f(S[l]), f(q[l]), f(k[l]), f(v[l]), f(g[l]), f(beta[l]),
+                                                     n_acc.cpu().numpy())
+        assert rel(S_new[l], S_ref) < TOL_F32 and rel(out[l], out_ref) < tol_out
