@@ -43,6 +43,7 @@ from kda_delta_rule_gb300 import dist as D           # noqa: E402
 from kda_delta_rule_gb300 import inputs as I         # noqa: E402
 
 H, DK, DV, T, STRIDE, CHUNK = 32, 128, 128, 8192, 512, 64
+E2E_SEGMENT = 1024                      # tokens per copy/compute segment of the end-to-end call
 DEC_B, DEC_STEPS = 256, 256
 REP_B, REP_H, REP_D, REP_DRAFT, REP_SETS = 32, 16, 32, 8, 64
 WORKLOAD = (f"kda_prefill_chunked long single sequence: B=1 H={H} dk=dv={DK} T={T} bf16 "
@@ -224,28 +225,23 @@ def bench_prefill(K, dev, steps, warmup, rank):
     kern_ms = [a.elapsed_time(b) for a, b in evs]
     bytes_step = prefill_bytes(T, H, DK, DV, 2, n_ck, page_bytes)
 
-    # end to end through the C ABI from pinned host buffers: H2D inputs, prefill, D2H results
+    # end to end through the C ABI from pinned host buffers: kda_prefill_chunked_host moves
+    # the projections in and the outputs and final state out, segment by segment, with the
+    # copies overlapping the kernels; checkpoint pages stay in the device page pool
     host_in = {n: t.to("cpu").pin_memory() for n, t in p.items()}
     host_S0 = S0.to("cpu").pin_memory()
-    dev_in = {n: torch.empty_like(t) for n, t in p.items()}
-    dev_S0 = torch.empty_like(S0)
     host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     host_S = torch.empty(S_fin.shape, dtype=S_fin.dtype).pin_memory()
-    host_pages = torch.empty(pool.arena.shape, dtype=torch.uint8).pin_memory()
+    scratch = torch.empty(K.kda_prefill_host_scratch_bytes(H, DK, DV, torch.bfloat16, STRIDE, E2E_SEGMENT),
+                          dtype=torch.uint8, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + host_S0.numel() * 4
-    d2h = host_o.numel() * 2 + host_S.numel() * 4 + host_pages.numel()
+    d2h = host_o.numel() * 2 + host_S.numel() * 4
 
     def e2e_step():
-        for n in dev_in:
-            dev_in[n].copy_(host_in[n], non_blocking=True)
-        dev_S0.copy_(host_S0, non_blocking=True)
-        K.kda_prefill_chunked(dev_S0, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"],
-                              dev_in["beta"], cu_seqlens=cu, ckpt_stride=STRIDE, page_pool=pool,
-                              ckpt_page_ids=ids, ckpt_pos=pos, o=o, S_final=S_fin, stream=stream,
-                              workspace=ws)
-        host_o.copy_(o, non_blocking=True)
-        host_S.copy_(S_fin, non_blocking=True)
-        host_pages.copy_(pool.arena, non_blocking=True)
+        K.kda_prefill_chunked_host(host_S0, host_in["q"], host_in["k"], host_in["v"], host_in["g"],
+                                   host_in["beta"], host_o, host_S, scratch, cu_seqlens=cu,
+                                   ckpt_stride=STRIDE, page_pool=pool, ckpt_page_ids=ids, ckpt_pos=pos,
+                                   segment_tokens=E2E_SEGMENT, stream=stream)
 
     for _ in range(warmup):
         e2e_step()

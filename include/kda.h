@@ -241,6 +241,41 @@ int kda_prefill_chunked_noalloc(const float* S0, const void* q, const void* k,
                                 int mode, kda_stream_t stream);
 
 /*
+ * kda_prefill_chunked_host -- kda_prefill_chunked with the projections, S0,
+ * o and S_final in host memory: the call moves them itself, cut into
+ * segments of at most `segment_tokens` tokens so that the copies of one
+ * segment overlap the computation of its neighbours (two internal copy
+ * streams, events, the compute on `stream`).  A sequence is cut only at a
+ * multiple of ckpt_stride (of 64 without checkpoints) from its own start, so
+ * the results are the same bits as kda_prefill_chunked on device copies.
+ * [CACHE] "预填充为什么能分块并行"; the pages run prefill from device memory.
+ *   S0, q, k, v, g, beta   host, same shapes as kda_prefill_chunked (S0 may be
+ *                          NULL = zero state); pinned (page-locked) memory
+ *                          is needed for the copies to overlap
+ *   o, S_final             host outputs, same shapes
+ *   page_pool, ckpt_page_ids, ckpt_pos   device, as in kda_prefill_chunked;
+ *                          ckpt_pos (optional) gets positions from each
+ *                          sequence's start
+ *   scratch                device, 256-byte aligned, at least
+ *                          kda_prefill_host_scratch_bytes(...) bytes; owned by
+ *                          the caller, busy until `stream` passes this call
+ * Returns when everything is enqueued; all copies and kernels are ordered
+ * before later work on `stream` (synchronise it before reading o, S_final).
+ * Errors: as kda_prefill_chunked, KDA_ERR_SHAPE for a small scratch,
+ * KDA_ERR_ALIGN for an unaligned scratch, KDA_ERR_CUDA for a failed copy.
+ */
+int64_t kda_prefill_host_scratch_bytes(int H, int dk, int dv, int dtype, int ckpt_stride,
+                                       int64_t segment_tokens);
+int kda_prefill_chunked_host(const float* S0, const void* q, const void* k, const void* v,
+                             const void* g, const void* beta, const int32_t* cu_seqlens,
+                             int n_seqs, int64_t T, int H, int dk, int dv, int dtype,
+                             int chunk, int ckpt_stride, void* o, float* S_final,
+                             void* page_pool, int64_t page_bytes,
+                             const int32_t* ckpt_page_ids, int32_t* ckpt_pos,
+                             int64_t num_ckpt, void* scratch, int64_t scratch_bytes,
+                             int64_t segment_tokens, int mode, kda_stream_t stream);
+
+/*
  * kda_pack_heads -- gather (B,H,dk,dv) states into one flat head-contiguous
  * buffer, zero-filling it past B*H*dk*dv. [SERVE] §1.5 pack_heads.
  *   S         device fp32; element (b,h,i,j) at S[b*stride_b + h*stride_h + i*dv + j]

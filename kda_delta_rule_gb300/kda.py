@@ -47,6 +47,9 @@ def _load():
         "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, I, P], I),
         "kda_prefill_workspace_bytes": ([P, I, L, I, I, I, I], L),
         "kda_prefill_chunked_noalloc": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, I, P], I),
+        "kda_prefill_host_scratch_bytes": ([I, I, I, I, I, L], L),
+        "kda_prefill_chunked_host": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, L, I, P],
+                                     I),
         "kda_device_errors": ([ctypes.POINTER(ctypes.c_int)], I),
         "kda_pack_heads": ([P, L, L, P, L, I, I, I, I, P], I),
         "kda_unpack_heads": ([P, P, L, L, I, I, I, I, P], I),
@@ -258,6 +261,71 @@ def kda_prefill_chunked(S0, q, k, v, g, beta, cu_seqlens=None, chunk=64, ckpt_st
                                     _ptr(ckpt_page_ids), _ptr(ckpt_pos), n_ck,
                                     _ptr(workspace), ws_bytes, mode, _stream(stream, dev)),
            "kda_prefill_chunked")
+    return o, S_final
+
+
+def _host(name, t, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def kda_prefill_host_scratch_bytes(H, dk, dv, dtype, ckpt_stride=512, segment_tokens=1024) -> int:
+    """Device scratch kda_prefill_chunked_host needs."""
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    n = _lib.kda_prefill_host_scratch_bytes(H, dk, dv, code, ckpt_stride, segment_tokens)
+    if n < 0:
+        _check(int(n), "kda_prefill_host_scratch_bytes")
+    return int(n)
+
+
+def kda_prefill_chunked_host(S0, q, k, v, g, beta, o, S_final, scratch, cu_seqlens=None, chunk=64,
+                             ckpt_stride=512, page_pool=None, ckpt_page_ids=None, ckpt_pos=None,
+                             segment_tokens=1024, mode=DECAY_FIRST, stream=None, device=None):
+    """kda_prefill_chunked on host-resident tensors (pin them for the copies to overlap).
+
+    q,k,g (T,H,dk), v (T,H,dv), beta (T,H), S0 (N,H,dk,dv) or None, o (T,H,dv) and S_final
+    (N,H,dk,dv): CPU tensors. scratch: CUDA uint8 tensor of at least
+    kda_prefill_host_scratch_bytes(...) bytes. Checkpoint pages, ids and positions stay on the
+    device. The call returns once everything is enqueued on `stream`; synchronise it before
+    reading o and S_final. Returns (o, S_final).
+    """
+    T, Hq, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    code = _dtype_code(q)
+    for nm, t, shp in (("q", q, (T, Hq, dk)), ("k", k, (T, Hq, dk)), ("g", g, (T, Hq, dk)),
+                       ("v", v, (T, Hq, dv)), ("beta", beta, (T, Hq))):
+        _host(nm, t, dt, shp)
+    arr, N = _cu_array(cu_seqlens)
+    if S0 is not None:
+        _host("S0", S0, torch.float32, (N, Hq, dk, dv))
+    _host("o", o, dt, (T, Hq, dv))
+    _host("S_final", S_final, torch.float32, (N, Hq, dk, dv))
+    _cuda("scratch", scratch, torch.uint8)
+    dev = scratch.device if device is None else device
+    base, page_bytes, n_ck = None, 0, 0
+    if ckpt_page_ids is not None:
+        _cuda("ckpt_page_ids", ckpt_page_ids, torch.int32)
+        n_ck = ckpt_page_ids.numel()
+        if page_pool is None:
+            raise ValueError("ckpt_page_ids given without a page_pool")
+        base, page_bytes = ctypes.c_void_p(page_pool.arena.data_ptr()), page_pool.page_bytes
+    if ckpt_pos is not None:
+        _cuda("ckpt_pos", ckpt_pos, torch.int32)
+    _check(_lib.kda_prefill_chunked_host(_ptr(S0), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                         arr, N, T, Hq, dk, dv, code, chunk, ckpt_stride,
+                                         _ptr(o), _ptr(S_final), base, page_bytes,
+                                         _ptr(ckpt_page_ids), _ptr(ckpt_pos), n_ck,
+                                         _ptr(scratch), scratch.numel(), segment_tokens, mode,
+                                         _stream(stream, dev)),
+           "kda_prefill_chunked_host")
     return o, S_final
 
 

@@ -205,6 +205,24 @@ def test_prefill_validation(K):
                 ctypes.c_void_p(A + (10 << 24) + 8), ws_bytes=need) == -4
 
 
+def test_prefill_host_validation(K):
+    lib = K._lib
+    assert lib.kda_prefill_host_scratch_bytes(2, 32, 32, 0, 0, 100) > 0
+    assert lib.kda_prefill_host_scratch_bytes(2, 32, 32, 0, 96, 100) == -1   # stride not a multiple of 64
+    assert lib.kda_prefill_host_scratch_bytes(2, 48, 32, 0, 0, 100) == -2
+    need = lib.kda_prefill_host_scratch_bytes(2, 32, 32, 0, 0, 256)
+    cu = (ctypes.c_int32 * 3)(0, 100, 228)
+    f = lib.kda_prefill_chunked_host
+
+    def call(scratch, nbytes, chunk=64):
+        # host buffers are never touched: validation fails first
+        return f(None, P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), P(5 << 20), cu, 2, 228, 2, 32, 32, 0,
+                 chunk, 0, P(6 << 20), P(7 << 20), None, 0, None, None, 0, scratch, nbytes, 256, 0, None)
+    assert call(P(8 << 20), need - 256) == -2                # scratch too small
+    assert call(ctypes.c_void_p(A + (8 << 20) + 16), need) == -4   # not 256-byte aligned
+    assert call(P(8 << 20), need, chunk=32) == -1
+
+
 def test_pack_validation(K):
     f = K._lib.kda_pack_heads
     assert f(P(0), 4096, 1024, P(1 << 20), 100, 2, 2, 32, 32, None) == -2   # flat too small
