@@ -287,6 +287,42 @@ def bench_decode(K, dev, warmup=3, runs=3):
     return ms_per_step, bytes_step
 
 
+def bench_varlen(K, dev, warmup=1, runs=3):
+    """Varlen prefix-cache resume prefill: 64 sequences, lengths log-uniform in [512, 32768]
+    rounded to multiples of 64, H=32, dk=dv=128, bf16, S0 ~ N(0, 0.05), a checkpoint page
+    every 512 tokens of every sequence."""
+    lengths = I.varlen_lengths(64, seed=0)
+    S0, p, cu = I.prefill_inputs(lengths, H, DK, DV, dtype=torch.bfloat16, seed=7, device=dev)
+    Tv = cu[-1]
+    n_ck = K.kda_num_checkpoints(cu, Tv, STRIDE)
+    page_bytes = H * DK * DV * 4
+    pool = K.PagePool(page_bytes, n_ck, device=dev)
+    ids = torch.tensor(pool.alloc(n_ck), dtype=torch.int32, device=dev)
+    o = torch.empty(Tv, H, DV, dtype=torch.bfloat16, device=dev)
+    S_fin = torch.empty_like(S0)
+    ws = torch.empty(max(K.kda_prefill_workspace_bytes(cu, Tv, H, DK, DV, torch.bfloat16), 16),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu, ckpt_stride=STRIDE,
+                              page_pool=pool, ckpt_page_ids=ids, o=o, S_final=S_fin, stream=stream, workspace=ws)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(runs):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / runs
+    nbytes = prefill_bytes(Tv, H, DK, DV, 2, n_ck, page_bytes, n_seqs=len(lengths))
+    del S0, p, o, S_fin, ws, pool
+    torch.cuda.empty_cache()
+    return ms, Tv, len(lengths), n_ck, nbytes
+
+
 def bench_replay(K, dev, warmup=3, runs=5):
     sets = []
     n_bytes = 0
@@ -479,6 +515,13 @@ def main():
                             "one kda_verify_replay_layers launch",
                 "ms_per_launch": layers_ms, "ms_per_layer": layers_ms / REP_SETS,
                 "bytes_per_launch": layers_bytes, "state_GBps": lgbs, "hbm_frac": lgbs / hbm}
+        vms, vtok, vseq, vck, vbytes = bench_varlen(K, dev)
+        vgbs = vbytes / (vms / 1e3) / 1e9
+        extras["varlen"] = {"workload": f"{vseq} sequences, lengths log-uniform in [512, 32768] rounded to 64 "
+                                        f"({vtok} tokens), H={H} dk=dv={DK} bf16, S0 ~ N(0,0.05), "
+                                        f"ckpt every {STRIDE} ({vck} pages)",
+                            "ms_per_call": vms, "tokens_per_s": vtok / (vms / 1e3),
+                            "algorithmic_bytes": vbytes, "achieved_GBps": vgbs, "hbm_frac": vgbs / hbm}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt, threads = oracle_sample(heads=2)

@@ -99,6 +99,46 @@ def kda_decode_step(S, q, k, v, g, beta, mode=DECAY_FIRST):
 
 
 # ---------------------------------------------------------------------------
+# Raw-input ring ([SERVE] Tab 4 §7.2: RawInputRing, the streaming window of
+# raw draft projections that fold-every-commit replays)
+# ---------------------------------------------------------------------------
+
+class RawInputRing:
+    """Per-slot window of raw draft projections (q, k, v, g, beta), one entry per step.
+
+    [SERVE] Tab 4 §7.2: during verification each draft step's raw inputs are
+    streamed into the window instead of snapshotting the state; once it holds
+    ``capacity`` steps a push overwrites the oldest (FIFO), so the size stays
+    at ``capacity`` from the capacity-th push on; ``window()`` gives the held
+    steps oldest first in the draft-projection layout (draft, B, H, D), which
+    is what ``verify_and_replay`` consumes at commit time.
+    """
+
+    def __init__(self, capacity):
+        if int(capacity) < 1:
+            raise ValueError("capacity must be >= 1")
+        self.capacity = int(capacity)
+        self._steps = []                  # oldest first
+
+    def push(self, q, k, v, g, beta):
+        if len(self._steps) == self.capacity:
+            self._steps.pop(0)            # full: the oldest step is overwritten
+        self._steps.append(tuple(_f64(x).copy() for x in (q, k, v, g, beta)))
+
+    def __len__(self):
+        return len(self._steps)
+
+    def reset(self):
+        self._steps = []
+
+    def window(self):
+        """(q, k, v, g, beta), each stacked to (len, B, H, D) / (len, B, H), oldest first."""
+        if not self._steps:
+            raise ValueError("empty window")
+        return tuple(np.stack([st[i] for st in self._steps]) for i in range(5))
+
+
+# ---------------------------------------------------------------------------
 # Speculative verify and replay ([SERVE] §1.2, Tab 3 §6.4)
 # ---------------------------------------------------------------------------
 

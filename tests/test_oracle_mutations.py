@@ -101,3 +101,19 @@ def test_chunk_mutant_is_caught(name, monkeypatch):
 
 def test_unmutated_oracle_passes_the_same_pins():
     assert not _caught(_step_pins())
+
+
+RING_MUTANTS = {
+    "ring_drops_newest": ("self._steps.pop(0)", "self._steps.pop()"),
+    "ring_grows_past_capacity": ("if len(self._steps) == self.capacity:",
+                                 "if len(self._steps) > self.capacity:"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(RING_MUTANTS))
+def test_ring_mutant_is_caught(name, monkeypatch):
+    old, new = RING_MUTANTS[name]
+    monkeypatch.setattr(O.RawInputRing, "push", _mutant(O.RawInputRing.push, old, new))
+    checks = [pins.test_ring_window_sizes_printed, pins.test_ring_overwrites_oldest_first,
+              lambda: pins.test_ring_replay_equals_recurrent(0)]
+    assert _caught(checks), f"no pin catches mutant {name}"

@@ -272,6 +272,75 @@ def test_draft_window_layout():
         assert torch.all(proj.q[i] == i)
 
 
+def _ring_step(rng, B, H, dk, dv):
+    q, k = rng.normal(size=(B, H, dk)), rng.normal(size=(B, H, dk))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    return (q, k, rng.normal(size=(B, H, dv)), -5.0 / (1.0 + np.exp(-rng.normal(size=(B, H, dk)))),
+            1.0 / (1.0 + np.exp(-rng.normal(size=(B, H)))))
+
+
+def test_ring_window_sizes_printed():
+    # Tab 4 panel a: capacity 4, sizes 1, 2, 3, then 4 from push(3) on.
+    gold = _golden()["ring_window_sizes"]
+    ring = O.RawInputRing(gold["capacity"])
+    sizes = []
+    rng = np.random.default_rng(0)
+    for _ in gold["sizes_after_push"]:
+        ring.push(*_ring_step(rng, 1, 1, 2, 2))
+        sizes.append(len(ring))
+    assert sizes == gold["sizes_after_push"]
+
+
+def test_ring_window_layout_printed():
+    # Tab 4 panel b: window() of three pushes is (draft=3, B=1, H=2, D=3), row i holds i.
+    lay = _golden()["draft_window_layout"]
+    ring = O.RawInputRing(4)
+    for i in range(lay["draft"]):
+        x = np.full((lay["B"], lay["H"], lay["D"]), float(i))
+        ring.push(x, x, x, x, x[..., 0])
+    q, k, v, g, beta = ring.window()
+    assert q.shape == (3, 1, 2, 3) and beta.shape == (3, 1, 2)
+    for i in range(3):
+        assert np.all(q[i] == i) and np.all(beta[i] == i)
+
+
+def test_ring_overwrites_oldest_first():
+    rng = np.random.default_rng(1)
+    steps = [_ring_step(rng, 2, 3, 4, 5) for _ in range(6)]
+    ring = O.RawInputRing(4)
+    for st in steps:
+        ring.push(*st)
+    win = ring.window()
+    for j in range(4):                     # pushes 2, 3, 4, 5 in push order
+        for t in range(5):
+            assert np.array_equal(win[t][j], steps[2 + j][t])
+    ring.reset()
+    assert len(ring) == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_ring_replay_equals_recurrent(mode):
+    # Tab 4 panel c: replay from the window == the recurrence over the same steps, error 0.
+    gold = _golden()["ring_replay_error"]
+    rng = np.random.default_rng(2)
+    B, H, dk, dv = 2, 2, 4, 3
+    S0 = rng.normal(size=(B, H, dk, dv))
+    steps = [_ring_step(rng, B, H, dk, dv) for _ in range(6)]
+    ring = O.RawInputRing(4)
+    for st in steps:
+        ring.push(*st)
+    q, k, v, g, beta = ring.window()
+    S_new, out = O.verify_and_replay(S0, q, k, v, g, beta, 3, mode)
+    S = S0.copy()
+    outs = []
+    for j in range(3):                     # the oldest held step is push 2
+        o, S = O.kda_step(S, *steps[2 + j], mode)
+        outs.append(o)
+    assert np.max(np.abs(S_new - S)) == gold["max_abs_error"]
+    assert np.max(np.abs(out - np.stack(outs, axis=-2))) == gold["max_abs_error"]
+
+
 # --------------------------------------------------------------------------
 # Page packing
 # --------------------------------------------------------------------------
