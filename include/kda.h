@@ -139,6 +139,43 @@ int kda_verify_replay_layers(int layers, const float* S_committed, const void* q
                              int dtype, int mode, kda_stream_t stream);
 
 /*
+ * Raw-input ring -- the window of raw draft projections that a commit replays
+ * ([SERVE] Tab 4 §7.2, RawInputRing / fold-every-commit: during verification
+ * each draft step's raw (q, k, v, g, beta) is streamed into a per-slot window
+ * instead of snapshotting the state; once the window holds `capacity` steps
+ * a push overwrites the oldest; a commit replays the accepted prefix).
+ * The ring lives in device memory the caller provides (kda_ring_bytes bytes,
+ * 256-byte aligned) and is laid out like the draft-projection cache
+ * ([capacity][B][H][D] per tensor), so kda_verify_replay_ring reads it in
+ * place.  The handle is host state (the push count); one thread at a time.
+ *   kda_ring_bytes    device bytes of a ring (negative KDA_ERR_* if invalid):
+ *                     1 <= capacity <= KDA_MAX_DRAFT, dk, dv in {32,64,128}
+ *   kda_ring_create   wrap device_base; the window starts empty
+ *   kda_ring_push     copy one step (device q,k,g [B,H,dk], v [B,H,dv],
+ *                     beta [B,H], dtype of the ring) in, asynchronously on stream
+ *   kda_ring_len      steps in the window (<= capacity)
+ *   kda_ring_window   copy the window out, oldest first, as [len,B,H,D]
+ *   kda_ring_reset    empty the window (after a commit)
+ *   kda_verify_replay_ring  kda_verify_replay over the window: S_committed
+ *                     [B,H,dk,dv] fp32 never written, n_accepted [B] clamped to
+ *                     [0, len], S_new [B,H,dk,dv], out [B,H,len,dv]
+ */
+typedef struct kda_raw_ring kda_raw_ring;
+int64_t kda_ring_bytes(int capacity, int B, int H, int dk, int dv, int dtype);
+int kda_ring_create(void* device_base, int capacity, int B, int H, int dk, int dv,
+                    int dtype, kda_raw_ring** ring_out);
+int kda_ring_destroy(kda_raw_ring* ring);
+int kda_ring_reset(kda_raw_ring* ring);
+int kda_ring_len(const kda_raw_ring* ring);
+int kda_ring_push(kda_raw_ring* ring, const void* q, const void* k, const void* v,
+                  const void* g, const void* beta, kda_stream_t stream);
+int kda_ring_window(const kda_raw_ring* ring, void* q, void* k, void* v, void* g,
+                    void* beta, kda_stream_t stream);
+int kda_verify_replay_ring(const kda_raw_ring* ring, const float* S_committed,
+                           const int32_t* n_accepted, float* S_new, void* out, int mode,
+                           kda_stream_t stream);
+
+/*
  * kda_num_checkpoints -- number of checkpoint states a prefill will emit:
  * sum over sequences of floor(L_n / ckpt_stride). Host only.
  *   cu_seqlens  host int32 [n_seqs+1] or NULL (one sequence of T tokens)

@@ -106,7 +106,7 @@ int kda_decode_step(float* S, const void* q, const void* k, const void* v, const
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = o;
   a.n_accepted = nullptr;
   a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = 1; a.dtype = dtype; a.mode = mode;
-  a.layers = 1;
+  a.layers = 1; a.proj_steps = 1; a.ring_start = 0;
   a.out_head_stride = dv; a.out_step_stride = 0;
   return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_decode_step launch");
 }
@@ -140,7 +140,7 @@ int kda_verify_replay_layers(int layers, const float* S_committed, const void* q
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
   a.n_accepted = n_accepted;
   a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = draft; a.dtype = dtype; a.mode = mode;
-  a.layers = layers;
+  a.layers = layers; a.proj_steps = draft; a.ring_start = 0;
   a.out_head_stride = (int64_t)draft * dv; a.out_step_stride = dv;
   return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_verify_replay launch");
 }

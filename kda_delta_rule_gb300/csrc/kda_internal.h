@@ -17,7 +17,9 @@ struct StepArgs {
   void* out;
   const int32_t* n_accepted;   // device [B] or nullptr (all heads run `steps`)
   int B, H, dk, dv, steps, dtype, mode;
-  int layers;                  // stacked layers (replay); states [layers][B][H], projections [layers][steps][B][H]
+  int layers;                  // stacked layers (replay); states [layers][B][H], projections [layers][proj_steps][B][H]
+  int proj_steps;              // steps stored per layer in the projection arrays (>= steps)
+  int ring_start;              // step s reads stored step (ring_start + s) mod proj_steps
   int64_t out_head_stride;     // elements between heads in `out`
   int64_t out_step_stride;     // elements between steps in `out`
 };

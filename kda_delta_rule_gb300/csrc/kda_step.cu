@@ -104,7 +104,9 @@ kda_step_kernel(const StepArgs a) {
 #pragma unroll
   for (int s = 0; s < MAXS; ++s) {
     const bool live = active && s < n;
-    const int64_t hs = (layer * a.steps + s) * nheads + hl;   // (layer, step, b, h) flattened
+    int slot = a.ring_start + s;                       // stored step of step s
+    if (slot >= a.proj_steps) slot -= a.proj_steps;
+    const int64_t hs = (layer * a.proj_steps + slot) * nheads + hl;   // (layer, step, b, h) flattened
 #pragma unroll
     for (int u = 0; u < EK; ++u) {
       const int i = tid + u * NT;

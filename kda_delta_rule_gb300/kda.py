@@ -63,6 +63,14 @@ def _load():
         "kda_store_kda": ([P, ctypes.c_int32, P, L, L, I, I, I, I, P], I),
         "kda_load_kda": ([P, ctypes.c_int32, P, L, L, I, I, I, I, P], I),
         "kda_snapshot_cost_ratio": ([I, I, I], D),
+        "kda_ring_bytes": ([I, I, I, I, I, I], L),
+        "kda_ring_create": ([P, I, I, I, I, I, I, ctypes.POINTER(P)], I),
+        "kda_ring_destroy": ([P], I),
+        "kda_ring_reset": ([P], I),
+        "kda_ring_len": ([P], I),
+        "kda_ring_push": ([P, P, P, P, P, P, P], I),
+        "kda_ring_window": ([P, P, P, P, P, P, P], I),
+        "kda_verify_replay_ring": ([P, P, P, P, P, I, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -183,6 +191,73 @@ def kda_verify_replay_layers(S_committed, q, k, v, g, beta, n_accepted, S_new=No
                                          B, H, dk, dv, code, mode, _stream(stream, S_committed.device)),
            "kda_verify_replay_layers")
     return S_new, out
+
+
+class RawInputRing:
+    """Device window of raw draft projections replayed at commit (kda_ring_* entry points).
+
+    Owns a CUDA uint8 arena of kda_ring_bytes(...) bytes; push() copies one step's
+    (q, k, v, g, beta) of shapes (B,H,dk) / (B,H,dv) / (B,H) in, overwriting the oldest
+    step once `capacity` are held; window() returns the held steps oldest first as
+    (len,B,H,D) tensors; verify_replay() replays the accepted prefix in place.
+    """
+
+    def __init__(self, capacity, B, H, dk, dv, dtype=torch.float32, device="cuda"):
+        self.B, self.H, self.dk, self.dv, self.dtype = B, H, dk, dv, dtype
+        code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+        n = _lib.kda_ring_bytes(capacity, B, H, dk, dv, code)
+        if n < 0:
+            _check(int(n), "kda_ring_bytes")
+        self.arena = torch.empty(int(n), dtype=torch.uint8, device=device)
+        h = ctypes.c_void_p()
+        _check(_lib.kda_ring_create(ctypes.c_void_p(self.arena.data_ptr()), capacity, B, H, dk, dv, code,
+                                    ctypes.byref(h)), "kda_ring_create")
+        self._h = h
+        self.capacity = capacity
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _lib.kda_ring_destroy(self._h)
+            self._h = None
+
+    def __len__(self):
+        return int(_lib.kda_ring_len(self._h))
+
+    def reset(self):
+        _check(_lib.kda_ring_reset(self._h), "kda_ring_reset")
+
+    def push(self, q, k, v, g, beta, stream=None):
+        for nm, t, shp in (("q", q, (self.B, self.H, self.dk)), ("k", k, (self.B, self.H, self.dk)),
+                           ("g", g, (self.B, self.H, self.dk)), ("v", v, (self.B, self.H, self.dv)),
+                           ("beta", beta, (self.B, self.H))):
+            _cuda(nm, t, self.dtype, shp)
+        _check(_lib.kda_ring_push(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  _stream(stream, self.arena.device)), "kda_ring_push")
+
+    def window(self, stream=None):
+        n = len(self)
+        dev = self.arena.device
+        q = torch.empty((n, self.B, self.H, self.dk), dtype=self.dtype, device=dev)
+        k, g = torch.empty_like(q), torch.empty_like(q)
+        v = torch.empty((n, self.B, self.H, self.dv), dtype=self.dtype, device=dev)
+        beta = torch.empty((n, self.B, self.H), dtype=self.dtype, device=dev)
+        _check(_lib.kda_ring_window(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                    _stream(stream, dev)), "kda_ring_window")
+        return q, k, v, g, beta
+
+    def verify_replay(self, S_committed, n_accepted, S_new=None, out=None, mode=DECAY_FIRST, stream=None):
+        n = len(self)
+        _cuda("S_committed", S_committed, torch.float32, (self.B, self.H, self.dk, self.dv))
+        _cuda("n_accepted", n_accepted, torch.int32, (self.B,))
+        if S_new is None:
+            S_new = torch.empty_like(S_committed)
+        if out is None:
+            out = torch.empty((self.B, self.H, n, self.dv), dtype=self.dtype, device=S_committed.device)
+        _cuda("S_new", S_new, torch.float32, (self.B, self.H, self.dk, self.dv))
+        _cuda("out", out, self.dtype, (self.B, self.H, n, self.dv))
+        _check(_lib.kda_verify_replay_ring(self._h, _ptr(S_committed), _ptr(n_accepted), _ptr(S_new), _ptr(out),
+                                           mode, _stream(stream, S_committed.device)), "kda_verify_replay_ring")
+        return S_new, out
 
 
 def _cu_array(cu_seqlens: Optional[Sequence[int]]):

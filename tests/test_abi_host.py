@@ -223,6 +223,20 @@ def test_prefill_host_validation(K):
     assert call(P(8 << 20), need, chunk=32) == -1
 
 
+def test_ring_host_side(K):
+    lib = K._lib
+    assert lib.kda_ring_bytes(4, 2, 3, 32, 32, 0) > 0
+    assert lib.kda_ring_bytes(0, 2, 3, 32, 32, 0) == -2
+    assert lib.kda_ring_bytes(17, 2, 3, 32, 32, 0) == -2       # capacity above KDA_MAX_DRAFT
+    h = ctypes.c_void_p()
+    assert lib.kda_ring_create(P(16), 4, 2, 3, 32, 32, 0, ctypes.byref(h)) == -4   # not 256-aligned
+    assert lib.kda_ring_create(P(0), 4, 2, 3, 32, 32, 0, ctypes.byref(h)) == 0     # never dereferenced here
+    assert lib.kda_ring_len(h) == 0
+    assert lib.kda_verify_replay_ring(h, P(1 << 20), P(2 << 20), P(3 << 20), P(4 << 20), 0, None) == -2  # empty
+    assert lib.kda_ring_reset(h) == 0
+    assert lib.kda_ring_destroy(h) == 0
+
+
 def test_pack_validation(K):
     f = K._lib.kda_pack_heads
     assert f(P(0), 4096, 1024, P(1 << 20), 100, 2, 2, 32, 32, None) == -2   # flat too small
