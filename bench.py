@@ -260,10 +260,14 @@ def bench_prefill(K, dev, steps, warmup, rank):
                 n_ck=n_ck, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
 
 
-def bench_decode(K, dev, warmup=3, runs=3):
+def bench_decode(K, dev, warmup=3, runs=3, layout=None):
+    """Decode steps on dense (B,H,dk,dv) states, or (layout given) on B slots picked at random
+    from a pool of 2B slots stored in that layout (kda_decode_step_slots)."""
     gen = torch.Generator(device=dev)
     gen.manual_seed(0)
-    S = (0.05 * torch.randn(DEC_B, H, DK, DV, generator=gen, device=dev)).contiguous()
+    n_states = DEC_B if layout is None else 2 * DEC_B
+    S = (0.05 * torch.randn(n_states, H, DK, DV, generator=gen, device=dev)).contiguous()
+    slots = torch.randperm(n_states, generator=gen, device=dev)[:DEC_B].to(torch.int32)
     projs = [I.decode_step_projections(DEC_B, H, DK, DV, dtype=torch.bfloat16, seed=1000 + t, device=dev)
              for t in range(DEC_STEPS)]
     o = torch.empty(DEC_B, H, DV, dtype=torch.bfloat16, device=dev)
@@ -271,7 +275,11 @@ def bench_decode(K, dev, warmup=3, runs=3):
 
     def run():
         for p in projs:
-            K.kda_decode_step(S, p["q"], p["k"], p["v"], p["g"], p["beta"], o=o, stream=stream)
+            if layout is None:
+                K.kda_decode_step(S, p["q"], p["k"], p["v"], p["g"], p["beta"], o=o, stream=stream)
+            else:
+                K.kda_decode_step_slots(S, slots, p["q"], p["k"], p["v"], p["g"], p["beta"], o=o, layout=layout,
+                                        stream=stream)
 
     for _ in range(warmup):
         run()
@@ -284,6 +292,8 @@ def bench_decode(K, dev, warmup=3, runs=3):
     torch.cuda.synchronize(dev)
     ms_per_step = a.elapsed_time(b) / (runs * DEC_STEPS)
     bytes_step = 2 * DEC_B * H * DK * DV * 4 + DEC_B * H * (3 * DK + DV + 1) * 2 + DEC_B * H * DV * 2
+    del S, projs
+    torch.cuda.empty_cache()
     return ms_per_step, bytes_step
 
 
@@ -498,6 +508,14 @@ def main():
                                         f"{DEC_STEPS} consecutive steps",
                             "ms_per_step": dms, "state_GBps": dgbs, "hbm_frac": dgbs / hbm,
                             "bytes_per_step": dbytes, "tokens_per_s": DEC_B / (dms / 1e3)}
+        for name, lay in (("kv", K.LAYOUT_KV), ("vk", K.LAYOUT_VK)):
+            sms, sbytes = bench_decode(K, dev, layout=lay)
+            sgbs = sbytes / (sms / 1e3) / 1e9
+            extras["decode"][f"slots_{name}"] = {
+                "workload": f"the same steps on {DEC_B} of {2 * DEC_B} slots of a state pool stored "
+                            + ("(dk, dv)" if name == "kv" else "transposed, (dv, dk)")
+                            + ", kda_decode_step_slots",
+                "ms_per_step": sms, "state_GBps": sgbs, "hbm_frac": sgbs / hbm}
         ams, abytes, single_ms, graph_ms, (layers_ms, layers_bytes) = bench_replay(K, dev)
         agbs = abytes / (ams / 1e3) / 1e9
         extras["replay"] = {"workload": f"B={REP_B} H={REP_H} dk=dv={REP_D} draft={REP_DRAFT} fp32, "

@@ -138,6 +138,62 @@ int kda_verify_replay_layers(int layers, const float* S_committed, const void* q
                              void* out, int draft, int B, int H, int dk, int dv,
                              int dtype, int mode, kda_stream_t stream);
 
+/* state layouts of the slot-pool entry points */
+#define KDA_LAYOUT_KV  0   /* state (dk, dv): key channels are rows, dv contiguous   */
+#define KDA_LAYOUT_VK  1   /* state (dv, dk): value channels are rows, dk contiguous */
+
+/*
+ * kda_decode_step_slots -- kda_decode_step on states kept in a slot pool, in
+ * either layout: one layer of a serving engine's recurrent-state buffer,
+ * [slots, heads, d_v, d_k] for KDA_LAYOUT_VK.  [CACHE] "先统一记号：矩阵状态不等于
+ * 完整检查点" (the state is written [local_heads, d_k, d_v]; kernels and state
+ * pools may store it transposed, [local_heads, d_v, d_k]) and "一个逻辑检查点如何
+ * 展开" (SGLang's buffer [num_kda_layers, slots, local_heads, d_v, d_k]: one
+ * slot spans every KDA layer).  Same recurrence as kda_decode_step.
+ *   S_pool    device fp32 [n_slots,H,dk,dv] (KDA_LAYOUT_KV) or
+ *             [n_slots,H,dv,dk] (KDA_LAYOUT_VK), updated in place; for layer l
+ *             of a [layers,n_slots,H,...] buffer pass its base + l*n_slots*H*dk*dv
+ *   slot_ids  device int32 [B]: batch row b updates slot slot_ids[b].  An id
+ *             outside [0, n_slots) (such as -1 for a padded row) touches no
+ *             state and gives a zero output row.  Valid ids must be distinct
+ *             (two rows on one slot race); device memory, so not checked.
+ *   q,k,g,v,beta,o  as kda_decode_step ([B,H,...]); o must not overlap S_pool
+ * Errors: as kda_decode_step; KDA_ERR_ARG for a bad layout or NULL slot_ids,
+ * KDA_ERR_SHAPE for n_slots < 1.
+ */
+int kda_decode_step_slots(float* S_pool, int64_t n_slots, const int32_t* slot_ids, int layout,
+                          const void* q, const void* k, const void* v, const void* g,
+                          const void* beta, void* o, int B, int H, int dk, int dv, int dtype,
+                          int mode, kda_stream_t stream);
+
+/*
+ * kda_verify_replay_slots -- kda_verify_replay_layers on states kept in slot
+ * pools, in either layout.  Row b of layer l replays the accepted prefix from
+ * slot slot_in[b] of layer l of S_pool and writes the resulting state into
+ * slot slot_out[b] of layer l of S_pool_new.  [SERVE] §1.2 verify_and_replay
+ * over the [CACHE] "一个逻辑检查点如何展开" slot buffer.
+ *   S_pool      device fp32 [layers,n_slots,H,<state>]  in, the committed states
+ *   S_pool_new  device fp32 [layers,n_slots,H,<state>]  out.  It may be S_pool
+ *               itself (states move between slots, a commit is then a change of
+ *               slot ids): slot_out must then be given, its valid ids distinct
+ *               and disjoint from every valid slot_in id so that no committed
+ *               state is written -- device memory, so not checked
+ *   slot_in     device int32 [B]
+ *   slot_out    device int32 [B], or NULL for slot_in (needs S_pool_new != S_pool)
+ *   q,k,g,v,beta,n_accepted,out  as kda_verify_replay_layers
+ * <state> is (dk,dv) for KDA_LAYOUT_KV, (dv,dk) for KDA_LAYOUT_VK.  A row
+ * whose slot_in or slot_out id is outside [0, n_slots) touches no state and
+ * gives zero output rows.
+ * Errors: as kda_verify_replay_layers; KDA_ERR_ALIAS when S_pool_new is S_pool
+ * without a distinct slot_out array, or partly overlaps it.
+ */
+int kda_verify_replay_slots(int layers, const float* S_pool, float* S_pool_new, int64_t n_slots,
+                            const int32_t* slot_in, const int32_t* slot_out, int layout,
+                            const void* q, const void* k, const void* v, const void* g,
+                            const void* beta, const int32_t* n_accepted, void* out,
+                            int draft, int B, int H, int dk, int dv, int dtype, int mode,
+                            kda_stream_t stream);
+
 /*
  * Raw-input ring -- the window of raw draft projections that a commit replays
  * ([SERVE] Tab 4 §7.2, RawInputRing / fold-every-commit: during verification

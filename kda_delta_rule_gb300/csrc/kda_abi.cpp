@@ -154,6 +154,81 @@ int kda_verify_replay(const float* S_committed, const void* q, const void* k, co
 }
 
 // ---------------------------------------------------------------------------
+static int check_slots(int64_t n_slots, int layout, const int32_t* slot_ids) {
+  if (layout != KDA_LAYOUT_KV && layout != KDA_LAYOUT_VK) return fail(KDA_ERR_ARG, "layout=%d is not a KDA_LAYOUT_*", layout);
+  if (n_slots < 1) return fail(KDA_ERR_SHAPE, "n_slots=%lld, must be >= 1", (long long)n_slots);
+  if (!slot_ids) return fail(KDA_ERR_ARG, "slot ids are NULL");
+  return KDA_OK;
+}
+
+int kda_decode_step_slots(float* S_pool, int64_t n_slots, const int32_t* slot_ids, int layout, const void* q,
+                          const void* k, const void* v, const void* g, const void* beta, void* o, int B, int H,
+                          int dk, int dv, int dtype, int mode, kda_stream_t stream) {
+  if (int st = check_common(dk, dv, dtype, mode)) return st;
+  if (B < 0 || H < 0) return fail(KDA_ERR_SHAPE, "negative B=%d or H=%d", B, H);
+  const int64_t heads = (int64_t)B * H;
+  if (heads == 0) return ok();
+  if (heads > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "B*H too large");
+  if (int st = check_slots(n_slots, layout, slot_ids)) return st;
+  if (n_slots > (int64_t)1 << 40) return fail(KDA_ERR_SHAPE, "n_slots too large");
+  if (!S_pool || !q || !k || !v || !g || !beta || !o) return fail(KDA_ERR_ARG, "null pointer argument");
+  if (!aligned16(S_pool) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(o))
+    return fail(KDA_ERR_ALIGN, "state, projection and output pointers must be 16-byte aligned");
+  const size_t es = elem_size(dtype);
+  if (overlap(o, heads * dv * es, S_pool, (size_t)n_slots * H * dk * dv * 4))
+    return fail(KDA_ERR_ALIAS, "o overlaps the state pool");
+  kda::StepArgs a{};
+  a.S_in = S_pool; a.S_out = S_pool;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = o;
+  a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = 1; a.dtype = dtype; a.mode = mode;
+  a.layers = 1; a.proj_steps = 1; a.ring_start = 0;
+  a.out_head_stride = dv; a.out_step_stride = 0;
+  a.slot_in = slot_ids; a.slot_out = slot_ids; a.n_slots = n_slots; a.layout = layout;
+  return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_decode_step_slots launch");
+}
+
+int kda_verify_replay_slots(int layers, const float* S_pool, float* S_pool_new, int64_t n_slots,
+                            const int32_t* slot_in, const int32_t* slot_out, int layout, const void* q,
+                            const void* k, const void* v, const void* g, const void* beta,
+                            const int32_t* n_accepted, void* out, int draft, int B, int H, int dk, int dv,
+                            int dtype, int mode, kda_stream_t stream) {
+  if (int st = check_common(dk, dv, dtype, mode)) return st;
+  if (layers < 0 || B < 0 || H < 0) return fail(KDA_ERR_SHAPE, "negative layers=%d, B=%d or H=%d", layers, B, H);
+  if (draft < 1 || draft > KDA_MAX_DRAFT)
+    return fail(KDA_ERR_SHAPE, "draft=%d outside [1, %d]", draft, KDA_MAX_DRAFT);
+  const int64_t heads = (int64_t)layers * B * H;
+  if (heads == 0) return ok();
+  if (heads > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "layers*B*H too large");
+  if (int st = check_slots(n_slots, layout, slot_in)) return st;
+  if (n_slots > (int64_t)1 << 40) return fail(KDA_ERR_SHAPE, "n_slots too large");
+  if (!S_pool || !S_pool_new || !q || !k || !v || !g || !beta || !n_accepted || !out)
+    return fail(KDA_ERR_ARG, "null pointer argument");
+  if (!aligned16(S_pool) || !aligned16(S_pool_new) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(g) || !aligned16(out))
+    return fail(KDA_ERR_ALIGN, "state, projection and output pointers must be 16-byte aligned");
+  const size_t pbytes = (size_t)layers * n_slots * H * dk * dv * 4;
+  const size_t es = elem_size(dtype);
+  if (S_pool_new == S_pool) {
+    if (!slot_out || slot_out == slot_in)
+      return fail(KDA_ERR_ALIAS, "S_pool_new is S_pool: slot_out must name slots other than slot_in, "
+                                 "or the committed states would be written");
+  } else if (overlap(S_pool_new, pbytes, S_pool, pbytes)) {
+    return fail(KDA_ERR_ALIAS, "S_pool_new partly overlaps S_pool");
+  }
+  if (overlap(out, heads * draft * dv * es, S_pool, pbytes) || overlap(out, heads * draft * dv * es, S_pool_new, pbytes))
+    return fail(KDA_ERR_ALIAS, "out overlaps a state pool");
+  kda::StepArgs a{};
+  a.S_in = S_pool; a.S_out = S_pool_new;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.out = out;
+  a.n_accepted = n_accepted;
+  a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = draft; a.dtype = dtype; a.mode = mode;
+  a.layers = layers; a.proj_steps = draft; a.ring_start = 0;
+  a.out_head_stride = (int64_t)draft * dv; a.out_step_stride = dv;
+  a.slot_in = slot_in; a.slot_out = slot_out ? slot_out : slot_in; a.n_slots = n_slots; a.layout = layout;
+  return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_verify_replay_slots launch");
+}
+
+// ---------------------------------------------------------------------------
 static int check_seqlens(const int32_t* cu, int n_seqs, int64_t T) {
   if (T < 0) return fail(KDA_ERR_SHAPE, "negative T");
   if (T > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "T=%lld exceeds 2^31-1 tokens", (long long)T);

@@ -22,8 +22,16 @@ struct StepArgs {
   int ring_start;              // step s reads stored step (ring_start + s) mod proj_steps
   int64_t out_head_stride;     // elements between heads in `out`
   int64_t out_step_stride;     // elements between steps in `out`
+  const int32_t* slot_in;      // device [B] or nullptr: states are [layers][n_slots][H], row b reads slot slot_in[b]
+  const int32_t* slot_out;     // device [B]: row b writes slot slot_out[b] (used when slot_in is set)
+  int64_t n_slots;
+  int layout;                  // KDA_LAYOUT_KV: state (dk, dv); KDA_LAYOUT_VK: state (dv, dk)
 };
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+cudaError_t launch_step_kv_f32(const StepArgs& a, cudaStream_t s);
+cudaError_t launch_step_kv_bf16(const StepArgs& a, cudaStream_t s);
+cudaError_t launch_step_vk_f32(const StepArgs& a, cudaStream_t s);
+cudaError_t launch_step_vk_bf16(const StepArgs& a, cudaStream_t s);
 
 // Sequence schedule of one prefill launch, passed by value as a kernel
 // parameter: at most kMaxSeqs sequences.

@@ -1,291 +1,15 @@
-// Decode step and speculative verify/replay of the KDA gated delta rule.
-//
-// Recurrence (one head, state S in R^{dk x dv}, rows = key channels):
-//   decay first     ("Kimi Linear 的 KDA 缓存", section "KDA 的递推与充分状态"):
-//       S' = Diag(e^g) S,  delta = v - S'^T k,  S = S' + beta k delta^T,  o = S^T q
-//   undecayed delta (KIMI K3 Serve demo page, §1.3 kda_step):
-//       delta = v - S^T k,  S = Diag(e^g) S + beta k delta^T,  o = S^T q
-// Replay (KIMI K3 Serve demo page, §1.2 verify_and_replay) runs the accepted
-// prefix of a draft from a clone of the committed state.
-//
-// Single pass over the state.  Columns of S are independent given (q,k,g,beta),
-// and both orderings reduce to two row-reductions of the old state:
-//   a_j = sum_i w_i S_ij   with w = e^g * k (decay first) or k (undecayed delta)
-//   b_j = sum_i e^{g_i} q_i S_ij
-//   delta_j = v_j - a_j,   o_j = b_j + beta (k.q) delta_j,
-//   S_ij <- e^{g_i} S_ij + k_i (beta delta_j).
-// So a call reads every state element once and writes it once; replay keeps
-// the state in registers across all accepted steps.
-//
-// Thread layout per head: each thread owns 4 consecutive columns (one float4)
-// of RPT rows; a warp-wide load covers whole rows (dv*4 bytes contiguous), so
-// every state access is a coalesced 128-bit access.  Row reductions go through
-// warp shuffles and one shared-memory exchange per step.
-#include "kda_common.cuh"
+// Dispatch of the decode/replay kernels (kda_step.cuh) by state layout and
+// projection dtype; each combination is compiled in its own translation unit.
 #include "kda_internal.h"
 #include "../../include/kda.h"
 
 namespace kda {
-namespace {
-
-template <int DK, int DV, int NW>
-struct StepCfg {
-  static constexpr int NT = 32 * NW;        // threads per head
-  static constexpr int TPR = DV / 4;        // threads per state row
-  static constexpr int RG = NT / TPR;       // row groups
-  static constexpr int RPT = DK / RG;       // rows per thread
-  static constexpr int STAGE = 3 * DK + DV + 4;   // floats staged per step: k, q, e^g, v, beta
-  static constexpr int RED = 2 * DV + 4;          // floats per warp in the reduction buffer
-  static_assert(TPR <= 32 && (32 % TPR) == 0, "dv/4 must divide 32");
-  static_assert(NT % TPR == 0 && DK % RG == 0 && RPT >= 1, "bad head tiling");
-};
-
-// per-step k.q partials, rounded up so the reduction buffer stays 16-byte aligned
-__host__ __device__ constexpr size_t kqw_floats(int steps, int nw) { return ((size_t)steps * nw + 3) / 4 * 4; }
-
-template <int DK, int DV, int NW>
-__host__ __device__ constexpr size_t step_smem_floats(int steps) {
-  using C = StepCfg<DK, DV, NW>;
-  return (size_t)steps * C::STAGE + kqw_floats(steps, NW) + 2 * (size_t)NW * C::RED;
-}
-
-template <int DK, int DV, int NW, int HPC, int MAXS, typename T>
-__global__ void __launch_bounds__(32 * NW * HPC)
-kda_step_kernel(const StepArgs a) {
-  using C = StepCfg<DK, DV, NW>;
-  constexpr int NT = C::NT, TPR = C::TPR, RG = C::RG, RPT = C::RPT;
-  constexpr int EK = (DK + NT - 1) / NT, EV = (DV + NT - 1) / NT;   // channels per thread
-
-  extern __shared__ float4 smem4[];
-  float* smem = reinterpret_cast<float*>(smem4);
-
-  const int tid = threadIdx.x;
-  const int y = threadIdx.y;
-  const int lane = tid & 31, warp = tid >> 5;
-  const int c4 = tid % TPR;           // column group: columns 4*c4 .. 4*c4+3
-  const int rg = tid / TPR;           // rows rg, rg+RG, ...
-  const int64_t nheads = (int64_t)a.B * a.H;          // heads of one layer
-  const int64_t head = (int64_t)blockIdx.x * HPC + y;  // over all stacked layers
-  const bool active = head < nheads * a.layers;
-  const int64_t layer = head / nheads, hl = head - layer * nheads;
-  // The host picks HPC dividing H, so every head of this CTA belongs to the
-  // same layer and sequence and the step count (and with it every barrier) is uniform.
-  const int b = (int)((((int64_t)blockIdx.x * HPC) % nheads) / a.H);
-
-  int n = a.steps;
-  if (a.n_accepted != nullptr) {
-    int na = a.n_accepted[b];
-    n = na < 0 ? 0 : (na > a.steps ? a.steps : na);
-  }
-
-  // ---- issue all state loads first ----
-  float4 S[RPT];
-  const float* Sin = a.S_in + head * (int64_t)(DK * DV);
-  if (active) {
-#pragma unroll
-    for (int m = 0; m < RPT; ++m) S[m] = ld_stream(Sin + (rg + RG * m) * DV + 4 * c4);
-  }
-
-  // ---- stage the projections of every step this head runs ----
-  const size_t per_y = step_smem_floats<DK, DV, NW>(a.steps);
-  float* base = smem + y * per_y;
-  float* stage = base;                                  // [steps][STAGE]
-  float* kqw = stage + (size_t)a.steps * C::STAGE;      // [steps][NW]
-  float* red = kqw + kqw_floats(a.steps, NW);           // [2][NW][RED]
-  const T* q = reinterpret_cast<const T*>(a.q);
-  const T* k = reinterpret_cast<const T*>(a.k);
-  const T* v = reinterpret_cast<const T*>(a.v);
-  const T* g = reinterpret_cast<const T*>(a.g);
-  const T* beta = reinterpret_cast<const T*>(a.beta);
-  // All steps' loads are issued before any is used (MAXS is 1 for decode, the
-  // draft bound for replay), so staging costs one memory round trip, not one
-  // per step.
-  float rk[MAXS][EK], rq[MAXS][EK], rg_[MAXS][EK], rv[MAXS][EV], rb[MAXS];
-#pragma unroll
-  for (int s = 0; s < MAXS; ++s) {
-    const bool live = active && s < n;
-    int slot = a.ring_start + s;                       // stored step of step s
-    if (slot >= a.proj_steps) slot -= a.proj_steps;
-    const int64_t hs = (layer * a.proj_steps + slot) * nheads + hl;   // (layer, step, b, h) flattened
-#pragma unroll
-    for (int u = 0; u < EK; ++u) {
-      const int i = tid + u * NT;
-      const bool ok = live && i < DK;
-      rk[s][u] = ok ? to_f32(k[hs * DK + i]) : 0.f;
-      rq[s][u] = ok ? to_f32(q[hs * DK + i]) : 0.f;
-      rg_[s][u] = ok ? to_f32(g[hs * DK + i]) : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < EV; ++u) {
-      const int j = tid + u * NT;
-      rv[s][u] = live && j < DV ? to_f32(v[hs * DV + j]) : 0.f;
-    }
-    rb[s] = live && tid == 0 ? to_f32(beta[hs]) : 0.f;
-  }
-#pragma unroll
-  for (int s = 0; s < MAXS; ++s) {
-    if (s < n) {
-      float* st = stage + (size_t)s * C::STAGE;
-      float kq = 0.f;
-#pragma unroll
-      for (int u = 0; u < EK; ++u) {
-        const int i = tid + u * NT;
-        if (i < DK) {
-          st[i] = rk[s][u];
-          st[DK + i] = rq[s][u];
-          st[2 * DK + i] = expf(rg_[s][u]);
-          kq = fmaf(rk[s][u], rq[s][u], kq);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < EV; ++u) {
-        const int j = tid + u * NT;
-        if (j < DV) st[3 * DK + j] = rv[s][u];
-      }
-      if (tid == 0) st[3 * DK + DV] = rb[s];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-      if (lane == 0) kqw[s * NW + warp] = kq;
-    }
-  }
-  __syncthreads();
-
-  T* out = reinterpret_cast<T*>(a.out);
-  const int mode = a.mode;
-  for (int s = 0; s < n; ++s) {
-    const float* st = stage + (size_t)s * C::STAGE;
-    const float* sk = st;
-    const float* sq = st + DK;
-    const float* se = st + 2 * DK;
-    float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pb = pa;
-#pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-      const int i = rg + RG * m;
-      const float e = se[i];
-      const float w = (mode == KDA_MODE_DECAY_FIRST) ? e * sk[i] : sk[i];
-      pa = f4_fma(w, S[m], pa);
-      pb = f4_fma(e * sq[i], S[m], pb);
-    }
-    // reduce over the lanes of this warp that share the column group
-#pragma unroll
-    for (int off = TPR; off < 32; off <<= 1) {
-      pa.x += __shfl_xor_sync(0xffffffffu, pa.x, off); pa.y += __shfl_xor_sync(0xffffffffu, pa.y, off);
-      pa.z += __shfl_xor_sync(0xffffffffu, pa.z, off); pa.w += __shfl_xor_sync(0xffffffffu, pa.w, off);
-      pb.x += __shfl_xor_sync(0xffffffffu, pb.x, off); pb.y += __shfl_xor_sync(0xffffffffu, pb.y, off);
-      pb.z += __shfl_xor_sync(0xffffffffu, pb.z, off); pb.w += __shfl_xor_sync(0xffffffffu, pb.w, off);
-    }
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f), Bq = A;
-    float kq = 0.f;
-    if constexpr (NW == 1) {
-      // one warp per head: the butterfly above left the full sums in every lane
-      A = pa;
-      Bq = pb;
-      kq = kqw[s];
-    } else {
-      float* rb = red + (size_t)(s & 1) * NW * C::RED;
-      if (lane < TPR) {
-        *reinterpret_cast<float4*>(rb + warp * C::RED + 4 * c4) = pa;
-        *reinterpret_cast<float4*>(rb + warp * C::RED + DV + 4 * c4) = pb;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        float4 x = *reinterpret_cast<const float4*>(rb + w * C::RED + 4 * c4);
-        float4 z = *reinterpret_cast<const float4*>(rb + w * C::RED + DV + 4 * c4);
-        A.x += x.x; A.y += x.y; A.z += x.z; A.w += x.w;
-        Bq.x += z.x; Bq.y += z.y; Bq.z += z.z; Bq.w += z.w;
-        kq += kqw[s * NW + w];
-      }
-    }
-    const float bt = st[3 * DK + DV];
-    const float4 vv = *reinterpret_cast<const float4*>(st + 3 * DK + 4 * c4);
-    float4 d = make_float4(vv.x - A.x, vv.y - A.y, vv.z - A.z, vv.w - A.w);
-    const float bkq = bt * kq;
-    float4 o = make_float4(fmaf(bkq, d.x, Bq.x), fmaf(bkq, d.y, Bq.y),
-                           fmaf(bkq, d.z, Bq.z), fmaf(bkq, d.w, Bq.w));
-    if (active && rg == 0)
-      store4(out + head * a.out_head_stride + s * a.out_step_stride + 4 * c4, o);
-    float4 bd = make_float4(bt * d.x, bt * d.y, bt * d.z, bt * d.w);
-#pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-      const int i = rg + RG * m;
-      const float e = se[i], ki = sk[i];
-      S[m].x = fmaf(e, S[m].x, ki * bd.x);
-      S[m].y = fmaf(e, S[m].y, ki * bd.y);
-      S[m].z = fmaf(e, S[m].z, ki * bd.z);
-      S[m].w = fmaf(e, S[m].w, ki * bd.w);
-    }
-  }
-
-  if (!active) return;
-  // steps past the accepted prefix produce zero output rows
-  if (rg == 0) {
-    for (int s = n; s < a.steps; ++s)
-      store4(out + head * a.out_head_stride + s * a.out_step_stride + 4 * c4,
-             make_float4(0.f, 0.f, 0.f, 0.f));
-  }
-  float* Sout = a.S_out + head * (int64_t)(DK * DV);
-#pragma unroll
-  for (int m = 0; m < RPT; ++m) st_stream(Sout + (rg + RG * m) * DV + 4 * c4, S[m]);
-}
-
-template <int DK, int DV, typename T>
-cudaError_t launch_dims(const StepArgs& a, cudaStream_t s) {
-  // rows per thread 16 where the head is big enough; at least 128 threads per CTA
-  constexpr int TPR = DV / 4;
-  constexpr int NW0 = (DK * TPR) / (16 * 32);
-  constexpr int NW = NW0 < 1 ? 1 : NW0;
-  constexpr int NT = 32 * NW;
-  constexpr int HMAX = NT >= 128 ? 1 : 128 / NT;   // heads per CTA: at least 128 threads
-  const int64_t nheads = (int64_t)a.B * a.H;
-  int hpc = 1;
-  while (hpc < HMAX && (a.H % (hpc * 2)) == 0) hpc *= 2;
-  size_t smem = step_smem_floats<DK, DV, NW>(a.steps) * sizeof(float);
-  auto run = [&](auto kern, int HPCv) -> cudaError_t {
-    size_t total = smem * HPCv;
-    if (total > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)total);
-      if (e != cudaSuccess) return e;
-    }
-    dim3 block(NT, HPCv);
-    int64_t grid = (nheads * a.layers + HPCv - 1) / HPCv;
-    kern<<<(unsigned)grid, block, total, s>>>(a);
-    return cudaGetLastError();
-  };
-  if (a.steps == 1) {
-    if constexpr (HMAX >= 4) {
-      if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, 1, T>, 4);
-    }
-    if constexpr (HMAX >= 2) {
-      if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, 1, T>, 2);
-    }
-    return run(kda_step_kernel<DK, DV, NW, 1, 1, T>, 1);
-  }
-  if constexpr (HMAX >= 4) {
-    if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, KDA_MAX_DRAFT, T>, 4);
-  }
-  if constexpr (HMAX >= 2) {
-    if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, KDA_MAX_DRAFT, T>, 2);
-  }
-  return run(kda_step_kernel<DK, DV, NW, 1, KDA_MAX_DRAFT, T>, 1);
-}
-
-template <typename T>
-cudaError_t launch_t(const StepArgs& a, cudaStream_t s) {
-#define KDA_CASE(DKv, DVv) if (a.dk == DKv && a.dv == DVv) return launch_dims<DKv, DVv, T>(a, s);
-  KDA_CASE(32, 32) KDA_CASE(32, 64) KDA_CASE(32, 128)
-  KDA_CASE(64, 32) KDA_CASE(64, 64) KDA_CASE(64, 128)
-  KDA_CASE(128, 32) KDA_CASE(128, 64) KDA_CASE(128, 128)
-#undef KDA_CASE
-  return cudaErrorInvalidValue;
-}
-
-}  // namespace
 
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
   if ((int64_t)a.B * a.H * a.layers == 0) return cudaSuccess;
-  if (a.dtype == KDA_BF16) return launch_t<__nv_bfloat16>(a, s);
-  return launch_t<float>(a, s);
+  const bool vk = a.layout == KDA_LAYOUT_VK;
+  if (a.dtype == KDA_BF16) return vk ? launch_step_vk_bf16(a, s) : launch_step_kv_bf16(a, s);
+  return vk ? launch_step_vk_f32(a, s) : launch_step_kv_f32(a, s);
 }
 
 }  // namespace kda

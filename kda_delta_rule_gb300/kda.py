@@ -20,6 +20,7 @@ KDA_OK = 0
 KDA_F32, KDA_BF16 = 0, 1
 DECAY_FIRST, UNDECAYED_DELTA = 0, 1
 PAGE_FREE, PAGE_KDA_STATE, PAGE_MLA_KV = 0, 1, 2
+LAYOUT_KV, LAYOUT_VK = 0, 1
 MAX_DRAFT = 16
 
 
@@ -43,6 +44,8 @@ def _load():
         "kda_decode_step": ([P, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
         "kda_verify_replay": ([P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
         "kda_verify_replay_layers": ([I, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
+        "kda_decode_step_slots": ([P, L, P, I, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
+        "kda_verify_replay_slots": ([I, P, P, L, P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
         "kda_num_checkpoints": ([P, I, L, I], L),
         "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, I, P], I),
         "kda_prefill_workspace_bytes": ([P, I, L, I, I, I, I], L),
@@ -191,6 +194,72 @@ def kda_verify_replay_layers(S_committed, q, k, v, g, beta, n_accepted, S_new=No
                                          B, H, dk, dv, code, mode, _stream(stream, S_committed.device)),
            "kda_verify_replay_layers")
     return S_new, out
+
+
+def _state_dims(layout, dk, dv):
+    if layout == LAYOUT_KV:
+        return dk, dv
+    if layout == LAYOUT_VK:
+        return dv, dk
+    raise ValueError(f"layout must be LAYOUT_KV or LAYOUT_VK, got {layout}")
+
+
+def kda_decode_step_slots(S_pool, slot_ids, q, k, v, g, beta, o=None, layout=LAYOUT_KV,
+                          mode=DECAY_FIRST, stream=None):
+    """kda_decode_step on a slot pool, in place.
+
+    S_pool (n_slots,H,dk,dv) for LAYOUT_KV or (n_slots,H,dv,dk) for LAYOUT_VK, fp32;
+    slot_ids int32 (B,): row b updates slot slot_ids[b] (ids outside [0, n_slots) skip the
+    row, whose output is zero). Projections (B,H,D). Returns o (B,H,dv).
+    """
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    n_slots = S_pool.shape[0]
+    _cuda("S_pool", S_pool, torch.float32, (n_slots, H, *_state_dims(layout, dk, dv)))
+    _cuda("slot_ids", slot_ids, torch.int32, (B,))
+    code, _, _ = _projections(q, k, v, g, beta, (B, H))
+    if o is None:
+        o = torch.empty((B, H, dv), device=q.device, dtype=q.dtype)
+    _cuda("o", o, q.dtype, (B, H, dv))
+    _check(_lib.kda_decode_step_slots(_ptr(S_pool), n_slots, _ptr(slot_ids), layout, _ptr(q), _ptr(k),
+                                      _ptr(v), _ptr(g), _ptr(beta), _ptr(o), B, H, dk, dv, code, mode,
+                                      _stream(stream, q.device)),
+           "kda_decode_step_slots")
+    return o
+
+
+def kda_verify_replay_slots(S_pool, q, k, v, g, beta, n_accepted, slot_in, slot_out=None,
+                            S_pool_new=None, out=None, layout=LAYOUT_KV, mode=DECAY_FIRST, stream=None):
+    """kda_verify_replay_layers on slot pools.
+
+    S_pool (L,n_slots,H,<state>) fp32 with <state> (dk,dv) for LAYOUT_KV, (dv,dk) for
+    LAYOUT_VK; projections (L,draft,B,H,D); n_accepted, slot_in, slot_out int32 (B,).
+    Row b of layer l reads slot slot_in[b] of S_pool and writes slot slot_out[b]
+    (slot_in when None) of S_pool_new, which may be S_pool itself when slot_out names
+    other slots. Returns (S_pool_new, out (L,B,H,draft,dv)).
+    """
+    Lr, draft, B, H, dk = q.shape
+    dv = v.shape[-1]
+    n_slots = S_pool.shape[1]
+    shape = (Lr, n_slots, H, *_state_dims(layout, dk, dv))
+    _cuda("S_pool", S_pool, torch.float32, shape)
+    code, _, _ = _projections(q, k, v, g, beta, (Lr, draft, B, H))
+    _cuda("n_accepted", n_accepted, torch.int32, (B,))
+    _cuda("slot_in", slot_in, torch.int32, (B,))
+    if slot_out is not None:
+        _cuda("slot_out", slot_out, torch.int32, (B,))
+    if S_pool_new is None:
+        S_pool_new = torch.zeros_like(S_pool)
+    _cuda("S_pool_new", S_pool_new, torch.float32, shape)
+    if out is None:
+        out = torch.empty((Lr, B, H, draft, dv), device=q.device, dtype=q.dtype)
+    _cuda("out", out, q.dtype, (Lr, B, H, draft, dv))
+    _check(_lib.kda_verify_replay_slots(Lr, _ptr(S_pool), _ptr(S_pool_new), n_slots, _ptr(slot_in),
+                                        _ptr(slot_out), layout, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(n_accepted), _ptr(out), draft, B, H, dk, dv,
+                                        code, mode, _stream(stream, q.device)),
+           "kda_verify_replay_slots")
+    return S_pool_new, out
 
 
 class RawInputRing:

@@ -168,6 +168,37 @@ def test_replay_layers_validation(K):
     assert f(2, *args, 0, 1, 1, 32, 32, 0, 0, None) == -2     # draft 0
 
 
+def test_slot_entries_validation(K):
+    """kda_decode_step_slots / kda_verify_replay_slots reject bad layouts, empty pools,
+    missing slot ids and pool aliasing before any launch."""
+    d = K._lib.kda_decode_step_slots
+    proj = [P(1 << 24), P(2 << 24), P(3 << 24), P(4 << 24), P(5 << 24), P(6 << 24)]
+    # (S_pool, n_slots, slot_ids, layout, q, k, v, g, beta, o, B, H, dk, dv, dtype, mode, stream)
+    assert d(P(0), 8, P(7 << 24), 2, *proj, 4, 2, 32, 32, 0, 0, None) == -1      # layout
+    assert d(P(0), 0, P(7 << 24), 0, *proj, 4, 2, 32, 32, 0, 0, None) == -2      # no slots
+    assert d(P(0), 8, None, 1, *proj, 4, 2, 32, 32, 0, 0, None) == -1            # slot ids NULL
+    assert d(P(8), 8, P(7 << 24), 1, *proj, 4, 2, 32, 32, 0, 0, None) == -4      # unaligned pool
+    o_in_pool = proj[:5] + [P(4096)]
+    assert d(P(0), 8, P(7 << 24), 1, *o_in_pool, 4, 2, 32, 32, 0, 0, None) == -7
+    assert d(P(0), 8, P(7 << 24), 1, *proj, 0, 2, 32, 32, 0, 0, None) == 0       # B = 0: no-op
+    r = K._lib.kda_verify_replay_slots
+    pr = [P(1 << 24), P(2 << 24), P(3 << 24), P(4 << 24), P(5 << 24)]
+
+    def rep(pool, pool_new, s_in, s_out, layout=1, n_slots=8, layers=2, draft=4):
+        # (layers, S_pool, S_pool_new, n_slots, slot_in, slot_out, layout, q, k, v, g, beta,
+        #  n_accepted, out, draft, B, H, dk, dv, dtype, mode, stream)
+        return r(layers, pool, pool_new, n_slots, s_in, s_out, layout, *pr, P(6 << 24), P(9 << 24),
+                 draft, 4, 2, 32, 32, 0, 0, None)
+
+    assert rep(P(0), P(0), P(7 << 24), None) == -7            # same pool, same slots
+    assert rep(P(0), P(0), P(7 << 24), P(7 << 24)) == -7      # same pool, same id array
+    assert rep(P(0), P(4096), P(7 << 24), P(8 << 24)) == -7   # pools partly overlap
+    assert rep(P(0), P(8 << 20), P(7 << 24), None, layout=3) == -1
+    assert rep(P(0), P(8 << 20), None, None) == -1
+    assert rep(P(0), P(8 << 20), P(7 << 24), None, draft=17) == -2
+    assert rep(P(0), P(8 << 20), P(7 << 24), None, layers=0) == 0
+
+
 def test_prefill_validation(K):
     f = K._lib.kda_prefill_chunked
     cu = (ctypes.c_int32 * 3)(0, 100, 228)
