@@ -156,6 +156,34 @@ def prefill_inputs(lengths, H, dk, dv, dtype=torch.bfloat16, seed=0, device="cpu
     return S0, proj, cu_seqlens_of(lengths)
 
 
+def prologue_inputs(lengths, H, dk, dv, w=4, dtype=torch.bfloat16, seed=0, device="cpu",
+                    zero_window=False):
+    """Raw inputs of the input prologue (ShortConv, activation, L2Norm, gates from logits).
+
+    mixed (T, H (2 dk + dv)) ~ N(0, 1), rows [q | k | v] of the packed sequences;
+    conv weight (H (2 dk + dv), w) ~ N(0, 1/w); per-sequence conv windows
+    (N, w - 1, H (2 dk + dv)) ~ N(0, 1) (zeros for fresh sequences); gate logits
+    (T, H, dk) and beta logits (T, H) ~ N(0, 1).  Returns (dict, cu_seqlens).
+    """
+    if isinstance(lengths, int):
+        lengths = [lengths]
+    work = torch.float64 if torch.device(device).type == "cpu" else torch.float32
+    gen = _gen(seed, device)
+    N = len(lengths)
+    T = sum(int(L) for L in lengths)
+    C = H * (2 * dk + dv)
+    out = {
+        "mixed": _normal((T, C), gen, device, work),
+        "weight": _normal((C, w), gen, device, work) / math.sqrt(w),
+        "window": _normal((N, w - 1, C), gen, device, work),
+        "g_logits": _normal((T, H, dk), gen, device, work),
+        "beta_logits": _normal((T, H), gen, device, work),
+    }
+    if zero_window:
+        out["window"].zero_()
+    return {n: t.to(dtype).contiguous() for n, t in out.items()}, cu_seqlens_of(lengths)
+
+
 def to_f64_numpy(t: torch.Tensor):
     """The exact stored values, widened to float64 (for the oracle)."""
     return t.detach().to("cpu").to(torch.float64).numpy()

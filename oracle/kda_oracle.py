@@ -365,6 +365,100 @@ def prefill_recurrent(S0, q, k, v, g, beta, cu_seqlens=None, ckpt_stride=512,
 
 
 # ---------------------------------------------------------------------------
+# Input prologue: ShortConv, activation, L2Norm, gates from logits.
+# [CACHE] "KDA 的递推与充分状态": before the recurrence each layer's input goes
+# through a linear projection, a causal short convolution and an activation, and
+# Q and K are L2-normalised.  [CACHE] "先统一记号：矩阵状态不等于完整检查点": the
+# ShortConv window of a layer at a boundary has kernel size w (the w - 1 most
+# recent inputs); "一个逻辑检查点如何展开": SGLang keeps it as
+# [layers, slots, kernel_size - 1, qkv_width]; "SGLang：从一次较长的 extend
+# 调用中提取检查点": the conv checkpoint is the kernel_size - 1 rows of mixed_qkv
+# just before the boundary.  [SERVE] §1.3: alpha = g_min * sigmoid(.) in
+# [g_min, 0] (read as the log-decay g), beta = sigmoid(.) in [0, 1].
+# Readings where the pages are silent (the equations are stripped): mixed_qkv
+# rows are [q (H dk) | k (H dk) | v (H dv)]; the convolution is depthwise over
+# time with no bias, y[t, c] = sum_j W[c, j] z[t + j, c] over z = [window; x];
+# the activation is none or SiLU; L2Norm is x / sqrt(sum x^2 + eps) over each
+# head's dk channels, after the activation.
+# ---------------------------------------------------------------------------
+
+ACT_NONE = 0
+ACT_SILU = 1
+
+
+def sigmoid(x):
+    x = _f64(x)
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def silu(x):
+    x = _f64(x)
+    return x * sigmoid(x)
+
+
+def l2norm(x, eps=1e-6):
+    """x / sqrt(sum(x^2) + eps) over the last axis."""
+    x = _f64(x)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def short_conv(x, weight, window=None):
+    """Causal depthwise convolution of x (T, C) with weight (C, w).
+
+    window (w - 1, C): the inputs just before x (oldest first); None = zeros.
+    Returns (y (T, C), window_out (w - 1, C)), window_out being the last w - 1
+    rows of [window; x].
+    """
+    x, weight = _f64(x), _f64(weight)
+    T, C = x.shape
+    w = weight.shape[1]
+    if window is None:
+        window = np.zeros((w - 1, C))
+    z = np.concatenate([_f64(window), x], axis=0)          # (w - 1 + T, C)
+    y = np.zeros((T, C))
+    for t in range(T):
+        for j in range(w):                                # tap j reads input t - (w - 1) + j
+            y[t] += weight[:, j] * z[t + j]
+    return y, z[T:].copy()
+
+
+def gates_from_logits(g_logits, beta_logits, g_min):
+    """g = g_min * sigmoid(a) per key channel, beta = sigmoid(b)."""
+    return g_min * sigmoid(g_logits), sigmoid(beta_logits)
+
+
+def input_prep(mixed, weight, window, g_logits, beta_logits, H, dk, dv, g_min,
+               act=ACT_SILU, eps=1e-6):
+    """One sequence of raw inputs -> the recurrence's (q, k, v, g, beta).
+
+    mixed (T, H (2 dk + dv)) rows [q | k | v]; weight (H (2 dk + dv), w);
+    window (w - 1, H (2 dk + dv)) or None; g_logits (T, H, dk); beta_logits (T, H).
+    Returns q, k (T, H, dk), v (T, H, dv), g (T, H, dk), beta (T, H) and the
+    window after the sequence.
+    """
+    mixed = _f64(mixed)
+    T = mixed.shape[0]
+    y, window_out = short_conv(mixed, weight, window)
+    if act == ACT_SILU:
+        y = silu(y)
+    elif act != ACT_NONE:
+        raise ValueError(f"unknown activation {act}")
+    q = l2norm(y[:, :H * dk].reshape(T, H, dk), eps)
+    k = l2norm(y[:, H * dk:2 * H * dk].reshape(T, H, dk), eps)
+    v = y[:, 2 * H * dk:].reshape(T, H, dv)
+    g, beta = gates_from_logits(g_logits, beta_logits, g_min)
+    return q, k, v, g, beta, window_out
+
+
+def conv_window_at(mixed, window, boundary):
+    """The conv checkpoint at `boundary` tokens: the w - 1 rows of [window; mixed]
+    that precede it (oldest first)."""
+    z = np.concatenate([_f64(window), _f64(mixed)], axis=0)
+    wm1 = np.shape(window)[0]
+    return z[boundary:boundary + wm1].copy()
+
+
+# ---------------------------------------------------------------------------
 # Page pool packing ([SERVE] §1.5, Tab 6, Tab 7)
 # ---------------------------------------------------------------------------
 

@@ -117,3 +117,33 @@ def test_ring_mutant_is_caught(name, monkeypatch):
     checks = [pins.test_ring_window_sizes_printed, pins.test_ring_overwrites_oldest_first,
               lambda: pins.test_ring_replay_equals_recurrent(0)]
     assert _caught(checks), f"no pin catches mutant {name}"
+
+
+PROLOGUE_MUTANTS = {
+    "conv_taps_reversed": ("short_conv", "y[t] += weight[:, j] * z[t + j]", "y[t] += weight[:, w - 1 - j] * z[t + j]"),
+    "conv_window_dropped": ("short_conv", "z = np.concatenate([_f64(window), x], axis=0)",
+                            "z = np.concatenate([0.0 * _f64(window), x], axis=0)"),
+    "conv_window_out_stale": ("short_conv", "return y, z[T:].copy()", "return y, z[:w - 1].copy()"),
+    "l2norm_wrong_axis": ("l2norm", "axis=-1", "axis=0"),
+    "gate_sign_flipped": ("gates_from_logits", "g_min * sigmoid(g_logits)", "g_min * sigmoid(-g_logits)"),
+    "silu_without_x": ("silu", "return x * sigmoid(x)", "return sigmoid(x)"),
+    "q_reads_k_columns": ("input_prep", "q = l2norm(y[:, :H * dk]", "q = l2norm(y[:, H * dk:2 * H * dk]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PROLOGUE_MUTANTS))
+def test_prologue_mutant_is_caught(name, monkeypatch):
+    fn, old, new = PROLOGUE_MUTANTS[name]
+    monkeypatch.setattr(O, fn, _mutant(getattr(O, fn), old, new))
+    checks = [lambda: pins.test_short_conv_is_numpy_correlation(4), pins.test_short_conv_newest_and_oldest_taps,
+              pins.test_activation_and_sigmoid_closed_forms, pins.test_l2norm_unit_norm_and_scale_invariance,
+              pins.test_gates_from_logits_values, pins.test_input_prep_channel_layout_by_hand,
+              lambda: pins.test_input_prep_split_equals_one_shot(1)]
+    assert _caught(checks), f"no pin catches mutant {name}"
+
+
+def test_prologue_pins_pass_unmutated():
+    pins.test_short_conv_is_numpy_correlation(4)
+    pins.test_short_conv_newest_and_oldest_taps()
+    pins.test_input_prep_channel_layout_by_hand()
+    pins.test_input_prep_split_equals_one_shot(1)

@@ -388,3 +388,102 @@ def test_snapshot_cost_ratio_properties():
             snap = draft * O.snapshot_bytes_per_step(16, 32, 32, item)
             proj = draft * O.projection_bytes_per_step(16, 32, 32, item)
             assert snap / proj == pytest.approx(O.snapshot_cost_ratio(16, 32, 32))
+
+
+# --------------------------------------------------------------------------
+# Input prologue: ShortConv, activation, L2Norm, gates from logits
+# --------------------------------------------------------------------------
+def _prologue(T, H=2, dk=4, dv=3, w=4, seed=0):
+    p, _ = I.prologue_inputs([T], H, dk, dv, w=w, dtype=torch.float64, seed=seed)
+    return {n: f64(t) for n, t in p.items()}
+
+
+@pytest.mark.parametrize("w", [2, 3, 4])
+def test_short_conv_is_numpy_correlation(w):
+    """A causal depthwise conv over [window; x] is, channel by channel, numpy's valid
+    cross-correlation with the channel's taps (an independent library routine)."""
+    p = _prologue(11, w=w, seed=w)
+    x, W, win = p["mixed"], p["weight"], p["window"][0]
+    y, win_out = O.short_conv(x, W, win)
+    z = np.concatenate([win, x])
+    for c in range(x.shape[1]):
+        assert np.allclose(y[:, c], np.correlate(z[:, c], W[c], mode="valid"), rtol=0, atol=1e-12)
+    assert np.array_equal(win_out, z[-(w - 1):])
+
+
+def test_short_conv_newest_and_oldest_taps():
+    """Only the newest tap set: the input itself. Only the oldest: the input w - 1
+    rows earlier, i.e. the window first."""
+    p = _prologue(7, w=4, seed=3)
+    x, win = p["mixed"], p["window"][0]
+    C = x.shape[1]
+    newest = np.zeros((C, 4)); newest[:, 3] = 1.0
+    oldest = np.zeros((C, 4)); oldest[:, 0] = 1.0
+    assert np.array_equal(O.short_conv(x, newest, win)[0], x)
+    y = O.short_conv(x, oldest, win)[0]
+    assert np.array_equal(y[:3], win) and np.array_equal(y[3:], x[:4])
+    assert np.array_equal(O.short_conv(x, oldest)[0][:3], np.zeros((3, C)))   # fresh sequence
+
+
+def test_activation_and_sigmoid_closed_forms():
+    assert O.sigmoid(0.0) == 0.5
+    assert O.silu(0.0) == 0.0
+    assert O.silu(1.0) == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), abs=1e-15)
+    assert O.silu(-2.0) == pytest.approx(-2.0 / (1.0 + math.exp(2.0)), abs=1e-15)
+    assert O.silu(40.0) == pytest.approx(40.0, abs=1e-12) and abs(O.silu(-40.0)) < 1e-15
+
+
+def test_l2norm_unit_norm_and_scale_invariance():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((5, 3, 8))
+    n = O.l2norm(x, eps=0.0)
+    assert np.allclose(np.linalg.norm(n, axis=-1), 1.0, atol=1e-14)
+    assert np.allclose(O.l2norm(7.5 * x, eps=0.0), n, atol=1e-14)
+    assert np.array_equal(O.l2norm(np.zeros(8)), np.zeros(8))       # eps keeps zero finite
+
+
+def test_gates_from_logits_values():
+    g, b = O.gates_from_logits(np.array([0.0, 60.0, -60.0]), np.array([0.0, 60.0, -60.0]), -5.0)
+    assert g[0] == -2.5 and b[0] == 0.5
+    assert g[1] == pytest.approx(-5.0, abs=1e-20) and b[1] == pytest.approx(1.0, abs=1e-20)
+    assert g[2] == pytest.approx(0.0, abs=1e-20) and b[2] == pytest.approx(0.0, abs=1e-20)
+    a = np.linspace(-6, 6, 101)
+    gg, bb = O.gates_from_logits(a, a, -5.0)
+    assert np.all(np.diff(gg) < 0) and np.all(np.diff(bb) > 0)      # monotone, opposite ways
+    assert gg.min() >= -5.0 and gg.max() <= 0.0 and bb.min() >= 0.0 and bb.max() <= 1.0
+
+
+def test_input_prep_channel_layout_by_hand():
+    """With only the newest tap and no activation the prologue reduces to slicing
+    mixed_qkv rows as [q | k | v] per head and normalising q and k per head."""
+    H, dk, dv, T = 2, 4, 3, 5
+    p = _prologue(T, H, dk, dv, w=3, seed=9)
+    C = H * (2 * dk + dv)
+    W = np.zeros((C, 3)); W[:, 2] = 1.0
+    q, k, v, g, b, _ = O.input_prep(p["mixed"], W, p["window"][0], p["g_logits"], p["beta_logits"],
+                                    H, dk, dv, -5.0, act=O.ACT_NONE, eps=0.0)
+    x = p["mixed"]
+    for t in range(T):
+        for h in range(H):
+            xq = x[t, h * dk:(h + 1) * dk]
+            xk = x[t, H * dk + h * dk:H * dk + (h + 1) * dk]
+            assert np.allclose(q[t, h], xq / math.sqrt(sum(c * c for c in xq)), atol=1e-14)
+            assert np.allclose(k[t, h], xk / math.sqrt(sum(c * c for c in xk)), atol=1e-14)
+            assert np.array_equal(v[t, h], x[t, 2 * H * dk + h * dv:2 * H * dk + (h + 1) * dv])
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_input_prep_split_equals_one_shot(act):
+    """Carrying the conv window across a cut gives the same values as one pass."""
+    H, dk, dv, T = 2, 4, 3, 13
+    p = _prologue(T, H, dk, dv, w=4, seed=11)
+    args = (H, dk, dv, -5.0, act)
+    whole = O.input_prep(p["mixed"], p["weight"], p["window"][0], p["g_logits"], p["beta_logits"], *args)
+    a = O.input_prep(p["mixed"][:6], p["weight"], p["window"][0], p["g_logits"][:6], p["beta_logits"][:6], *args)
+    b = O.input_prep(p["mixed"][6:], p["weight"], a[5], p["g_logits"][6:], p["beta_logits"][6:], *args)
+    for i in range(5):
+        assert np.array_equal(np.concatenate([a[i], b[i]]), whole[i])
+    assert np.array_equal(b[5], whole[5])
+    # the conv checkpoint at a boundary is the window a pass up to it leaves behind
+    assert np.array_equal(O.conv_window_at(p["mixed"], p["window"][0], 6), a[5])
+    assert np.array_equal(O.conv_window_at(p["mixed"], p["window"][0], T), whole[5])
