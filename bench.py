@@ -46,6 +46,7 @@ H, DK, DV, T, STRIDE, CHUNK = 32, 128, 128, 8192, 512, 64
 E2E_SEGMENT = 1024                      # tokens per copy/compute segment of the end-to-end call
 DEC_B, DEC_STEPS = 256, 256
 REP_B, REP_H, REP_D, REP_DRAFT, REP_SETS = 32, 16, 32, 8, 64
+CONV_W = 4                              # ShortConv kernel size of the input-prologue measurements
 WORKLOAD = (f"kda_prefill_chunked long single sequence: B=1 H={H} dk=dv={DK} T={T} bf16 "
             f"fp32-state chunk={CHUNK} ckpt_stride={STRIDE} (16 checkpoint pages)")
 
@@ -297,6 +298,53 @@ def bench_decode(K, dev, warmup=3, runs=3, layout=None):
     return ms_per_step, bytes_step
 
 
+def _timed(fn, stream, warmup, runs):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(runs):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / runs
+
+
+def bench_prologue(K, dev, warmup=3, runs=10):
+    """Input prologue: kda_input_prep at the long-prefill size (T=8192, H=32, d=128, bf16,
+    ShortConv w=4, SiLU) and the fused decode step at the batched-decode size (B=256)."""
+    stream = torch.cuda.current_stream(dev)
+    p, cu = I.prologue_inputs([T], H, DK, DV, w=CONV_W, dtype=torch.bfloat16, seed=3, device=dev)
+    out = K.kda_input_prep(p["mixed"], p["weight"], p["g_logits"], p["beta_logits"], window_in=p["window"],
+                           stream=stream)
+    C = H * (2 * DK + DV)
+    pre_ms = _timed(lambda: K.kda_input_prep(p["mixed"], p["weight"], p["g_logits"], p["beta_logits"],
+                                             window_in=p["window"], out=out, stream=stream), stream, warmup, runs)
+    pre_bytes = 2 * (T * C + T * H * DK + T * H) + 2 * (T * H * (3 * DK + DV) + T * H)
+    del p, out
+    # fused decode: raw rows + conv windows + logits in, state in place
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    S = (0.05 * torch.randn(DEC_B, H, DK, DV, generator=gen, device=dev)).contiguous()
+    steps = 16
+    raws = [I.prologue_inputs([1] * DEC_B, H, DK, DV, w=CONV_W, dtype=torch.bfloat16, seed=400 + t, device=dev)[0]
+            for t in range(steps)]
+    win = raws[0]["window"].clone()
+    o = torch.empty(DEC_B, H, DV, dtype=torch.bfloat16, device=dev)
+
+    def run():
+        for r in raws:
+            K.kda_decode_step_fused(S, win, r["mixed"], r["weight"], r["g_logits"], r["beta_logits"], o=o,
+                                    stream=stream)
+    dec_ms = _timed(run, stream, 2, 3) / steps
+    dec_bytes = (2 * DEC_B * H * DK * DV * 4 + DEC_B * C * 2 + 2 * DEC_B * (CONV_W - 1) * C * 2
+                 + DEC_B * H * (DK + 1) * 2 + DEC_B * H * DV * 2)
+    del S, raws, win
+    torch.cuda.empty_cache()
+    return pre_ms, pre_bytes, dec_ms, dec_bytes
+
+
 def bench_varlen(K, dev, warmup=1, runs=3):
     """Varlen prefix-cache resume prefill: 64 sequences, lengths log-uniform in [512, 32768]
     rounded to multiples of 64, H=32, dk=dv=128, bf16, S0 ~ N(0, 0.05), a checkpoint page
@@ -516,6 +564,17 @@ def main():
                             + ("(dk, dv)" if name == "kv" else "transposed, (dv, dk)")
                             + ", kda_decode_step_slots",
                 "ms_per_step": sms, "state_GBps": sgbs, "hbm_frac": sgbs / hbm}
+        pms, pbytes, fms, fbytes = bench_prologue(K, dev)
+        extras["prologue"] = {
+            "workload": f"kda_input_prep: T={T} H={H} dk=dv={DK} bf16, ShortConv w={CONV_W}, SiLU, L2Norm, "
+                        "gates from logits",
+            "ms_per_call": pms, "algorithmic_bytes": pbytes, "achieved_GBps": pbytes / (pms / 1e3) / 1e9,
+            "hbm_frac": pbytes / (pms / 1e3) / 1e9 / hbm,
+            "decode_fused": {
+                "workload": f"kda_decode_step_fused: B={DEC_B} H={H} dk=dv={DK} bf16 raw rows, w={CONV_W}, "
+                            "fp32 state in place",
+                "ms_per_step": fms, "bytes_per_step": fbytes, "achieved_GBps": fbytes / (fms / 1e3) / 1e9,
+                "hbm_frac": fbytes / (fms / 1e3) / 1e9 / hbm}}
         ams, abytes, single_ms, graph_ms, (layers_ms, layers_bytes) = bench_replay(K, dev)
         agbs = abytes / (ams / 1e3) / 1e9
         extras["replay"] = {"workload": f"B={REP_B} H={REP_H} dk=dv={REP_D} draft={REP_DRAFT} fp32, "

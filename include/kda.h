@@ -66,6 +66,10 @@ extern "C" {
 #define KDA_MODE_DECAY_FIRST      0
 #define KDA_MODE_UNDECAYED_DELTA  1
 
+/* activations of the input prologue */
+#define KDA_ACT_NONE  0
+#define KDA_ACT_SILU  1
+
 /* page kinds of the unified pool ([SERVE] §1.5: one free list, two kinds) */
 #define KDA_PAGE_FREE       0
 #define KDA_PAGE_KDA_STATE  1
@@ -165,6 +169,36 @@ int kda_decode_step_slots(float* S_pool, int64_t n_slots, const int32_t* slot_id
                           const void* q, const void* k, const void* v, const void* g,
                           const void* beta, void* o, int B, int H, int dk, int dv, int dtype,
                           int mode, kda_stream_t stream);
+
+/*
+ * kda_decode_step_fused -- one decode token with the input prologue of
+ * kda_input_prep fused in: the raw mixed_qkv row of each sequence passes
+ * through the causal ShortConv (its window shifted in place), the activation,
+ * per-head L2Norm of q and k and the gates from their logits, then one step of
+ * the recurrence, in one launch.  [CACHE] "KDA 的递推与充分状态" (the prologue
+ * and the recurrence), "一个逻辑检查点如何展开" (SGLang keeps the conv window
+ * [layers, slots, kernel_size - 1, qkv_width] beside the recurrent state);
+ * [SERVE] §1.3.  Same readings of the prologue as kda_input_prep.
+ *   S          device fp32: [B,H,<state>] (slot_ids NULL) or a pool
+ *              [n_slots,H,<state>]; <state> per layout as in the slot entry points
+ *   slot_ids   device int32 [B] or NULL: row b uses slot slot_ids[b] of S and of
+ *              conv_state; ids outside [0, n_slots) give zero output and touch
+ *              nothing; valid ids must be distinct
+ *   conv_state device dtype [B or n_slots, w-1, C], C = H*(2*dk + dv), in/out
+ *   mixed_qkv  device dtype [B, C] in; conv_weight [C, w] in, 2 <= w <= 8
+ *   g_logits   device dtype [B, H, dk]; beta_logits [B, H]   in
+ *   o          device dtype [B, H, dv] out
+ *   q_out, k_out, g_out [B,H,dk], v_out [B,H,dv], beta_out [B,H]: all NULL, or
+ *              all given to receive the prepared projections (for a
+ *              draft-projection cache); rows of skipped ids are left unwritten
+ * Errors: as kda_decode_step and kda_input_prep; KDA_ERR_ALIAS when any two
+ * arguments overlap.
+ */
+int kda_decode_step_fused(float* S, int64_t n_slots, const int32_t* slot_ids, int layout,
+                          void* conv_state, const void* mixed_qkv, const void* conv_weight, int w,
+                          const void* g_logits, const void* beta_logits, float g_min, int act,
+                          void* o, void* q_out, void* k_out, void* v_out, void* g_out, void* beta_out,
+                          int B, int H, int dk, int dv, int dtype, int mode, kda_stream_t stream);
 
 /*
  * kda_verify_replay_slots -- kda_verify_replay_layers on states kept in slot
@@ -367,6 +401,46 @@ int kda_prefill_chunked_host(const float* S0, const void* q, const void* k, cons
                              const int32_t* ckpt_page_ids, int32_t* ckpt_pos,
                              int64_t num_ckpt, void* scratch, int64_t scratch_bytes,
                              int64_t segment_tokens, int mode, kda_stream_t stream);
+
+/*
+ * kda_input_prep -- the input prologue of a KDA layer for prefill: causal
+ * depthwise ShortConv over the rows of mixed_qkv, activation, per-head L2Norm of
+ * q and k, and the gates from their logits, writing the q, k, v, g, beta that
+ * kda_prefill_chunked reads.  [CACHE] "KDA 的递推与充分状态" (projection, causal
+ * short convolution and activation, L2Norm of Q and K), "先统一记号：矩阵状态不等于
+ * 完整检查点" (the ShortConv window: the kernel_size - 1 most recent inputs),
+ * "SGLang：从一次较长的 extend 调用中提取检查点" (the conv checkpoint: the
+ * kernel_size - 1 rows of mixed_qkv before the boundary); [SERVE] §1.3 (alpha =
+ * g_min * sigmoid(.), beta = sigmoid(.)).  Where the pages leave a step open:
+ * rows of mixed_qkv are [q (H*dk) | k (H*dk) | v (H*dv)], the convolution has no
+ * bias, y[t,c] = sum_j weight[c,j] * in[t - (w-1) + j, c], L2Norm is
+ * x / sqrt(sum x^2 + 1e-6) over each head's dk channels after the activation.
+ *   mixed_qkv    device dtype [T, C], C = H*(2*dk + dv)   in (packed sequences)
+ *   conv_weight  device dtype [C, w], 2 <= w <= 8          in
+ *   window_in    device dtype [n_seqs, w-1, C] or NULL     in: each sequence's
+ *                window (the raw rows before it, oldest first); NULL = zeros
+ *   window_out   device dtype [n_seqs, w-1, C] or NULL     out: the window after
+ *                each sequence (carry it into the next call)
+ *   g_logits     device dtype [T, H, dk]; beta_logits [T, H]   in
+ *   g_min        g = g_min * sigmoid(g_logits) (g_min < 0)
+ *   act          KDA_ACT_NONE or KDA_ACT_SILU (applied after the convolution)
+ *   cu_seqlens, n_seqs, T   as kda_prefill_chunked (host)
+ *   q, k, g      device dtype [T, H, dk] out; v [T, H, dv] out; beta [T, H] out
+ *   ckpt_stride, conv_ckpt, num_ckpt  optional conv checkpoints: when conv_ckpt
+ *                is not NULL, checkpoint c (numbered as kda_prefill_chunked
+ *                numbers its states: sequence-major, then position) gets the
+ *                window at its boundary, [num_ckpt, w-1, C] dtype; num_ckpt must
+ *                be >= kda_num_checkpoints()
+ * All tensors of one dtype (KDA_F32 or KDA_BF16); outputs must not overlap
+ * inputs.  Errors: KDA_ERR_SHAPE (w, sizes, cu_seqlens), KDA_ERR_ARG (NULL
+ * required pointer, act, g_min >= 0), KDA_ERR_ALIGN, KDA_ERR_ALIAS.
+ */
+int kda_input_prep(const void* mixed_qkv, const void* conv_weight, int w,
+                   const void* window_in, void* window_out,
+                   const void* g_logits, const void* beta_logits, float g_min, int act,
+                   const int32_t* cu_seqlens, int n_seqs, int64_t T, int H, int dk, int dv,
+                   int dtype, void* q, void* k, void* v, void* g, void* beta,
+                   int ckpt_stride, void* conv_ckpt, int64_t num_ckpt, kda_stream_t stream);
 
 /*
  * kda_pack_heads -- gather (B,H,dk,dv) states into one flat head-contiguous

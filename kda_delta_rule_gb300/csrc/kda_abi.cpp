@@ -187,6 +187,53 @@ int kda_decode_step_slots(float* S_pool, int64_t n_slots, const int32_t* slot_id
   return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_decode_step_slots launch");
 }
 
+int kda_decode_step_fused(float* S, int64_t n_slots, const int32_t* slot_ids, int layout, void* conv_state,
+                          const void* mixed_qkv, const void* conv_weight, int w, const void* g_logits,
+                          const void* beta_logits, float g_min, int act, void* o, void* q_out, void* k_out,
+                          void* v_out, void* g_out, void* beta_out, int B, int H, int dk, int dv, int dtype,
+                          int mode, kda_stream_t stream) {
+  if (int st = check_common(dk, dv, dtype, mode)) return st;
+  if (B < 0 || H < 0) return fail(KDA_ERR_SHAPE, "negative B=%d or H=%d", B, H);
+  const int64_t heads = (int64_t)B * H;
+  if (heads == 0) return ok();
+  if (heads > 0x7fffffffLL) return fail(KDA_ERR_SHAPE, "B*H too large");
+  if (layout != KDA_LAYOUT_KV && layout != KDA_LAYOUT_VK) return fail(KDA_ERR_ARG, "layout=%d is not a KDA_LAYOUT_*", layout);
+  if (slot_ids && (n_slots < 1 || n_slots > ((int64_t)1 << 40)))
+    return fail(KDA_ERR_SHAPE, "n_slots=%lld outside [1, 2^40]", (long long)n_slots);
+  if (w < 2 || w > 8) return fail(KDA_ERR_SHAPE, "conv kernel size w=%d outside [2, 8]", w);
+  if (act != KDA_ACT_NONE && act != KDA_ACT_SILU) return fail(KDA_ERR_ARG, "act=%d is not a KDA_ACT_*", act);
+  if (!(g_min < 0.f)) return fail(KDA_ERR_ARG, "g_min=%g must be negative", (double)g_min);
+  if (!S || !conv_state || !mixed_qkv || !conv_weight || !g_logits || !beta_logits || !o)
+    return fail(KDA_ERR_ARG, "null pointer argument");
+  const int n_keep = (q_out != nullptr) + (k_out != nullptr) + (v_out != nullptr) + (g_out != nullptr) +
+                     (beta_out != nullptr);
+  if (n_keep != 0 && n_keep != 5) return fail(KDA_ERR_ARG, "q_out, k_out, v_out, g_out, beta_out: give all or none");
+  const void* al[] = {S, conv_state, mixed_qkv, conv_weight, g_logits, beta_logits, o, q_out, k_out, v_out, g_out, beta_out};
+  for (const void* ptr : al)
+    if (ptr && !aligned16(ptr)) return fail(KDA_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const size_t es = elem_size(dtype), C = (size_t)H * (2 * dk + dv);
+  const size_t rows = slot_ids ? (size_t)n_slots : (size_t)B;
+  const void* bufs[] = {S, conv_state, mixed_qkv, conv_weight, g_logits, beta_logits, o, q_out, k_out, v_out, g_out, beta_out};
+  const size_t bytes[] = {rows * H * dk * dv * 4, rows * (w - 1) * C * es, (size_t)B * C * es, C * w * es,
+                          (size_t)heads * dk * es, (size_t)heads * es, (size_t)heads * dv * es, (size_t)heads * dk * es,
+                          (size_t)heads * dk * es, (size_t)heads * dv * es, (size_t)heads * dk * es, (size_t)heads * es};
+  for (int i = 0; i < 12; ++i)
+    for (int j = 0; j < i; ++j)
+      if (overlap(bufs[i], bytes[i], bufs[j], bytes[j])) return fail(KDA_ERR_ALIAS, "two arguments overlap");
+  kda::StepArgs a{};
+  a.S_in = S; a.S_out = S;
+  a.out = o;
+  a.B = B; a.H = H; a.dk = dk; a.dv = dv; a.steps = 1; a.dtype = dtype; a.mode = mode;
+  a.layers = 1; a.proj_steps = 1; a.ring_start = 0;
+  a.out_head_stride = dv; a.out_step_stride = 0;
+  a.slot_in = slot_ids; a.slot_out = slot_ids; a.n_slots = n_slots; a.layout = layout;
+  a.mixed = mixed_qkv; a.conv_state = conv_state; a.conv_w = conv_weight;
+  a.g_logits = g_logits; a.beta_logits = beta_logits;
+  a.q_out = q_out; a.k_out = k_out; a.v_out = v_out; a.g_out = g_out; a.beta_out = beta_out;
+  a.conv_size = w; a.act = act; a.g_min = g_min; a.eps = 1e-6f;
+  return cuda_status(kda::launch_step(a, reinterpret_cast<cudaStream_t>(stream)), "kda_decode_step_fused launch");
+}
+
 int kda_verify_replay_slots(int layers, const float* S_pool, float* S_pool_new, int64_t n_slots,
                             const int32_t* slot_in, const int32_t* slot_out, int layout, const void* q,
                             const void* k, const void* v, const void* g, const void* beta,
@@ -385,6 +432,89 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
     status = cuda_status(kda::launch_prefill(a, *sched, max_len, s), "kda_prefill_chunked launch");
   }
   return status;
+}
+
+// ---------------------------------------------------------------------------
+int kda_input_prep(const void* mixed_qkv, const void* conv_weight, int w, const void* window_in, void* window_out,
+                   const void* g_logits, const void* beta_logits, float g_min, int act, const int32_t* cu_seqlens,
+                   int n_seqs, int64_t T, int H, int dk, int dv, int dtype, void* q, void* k, void* v, void* g,
+                   void* beta, int ckpt_stride, void* conv_ckpt, int64_t num_ckpt, kda_stream_t stream) {
+  if (int st = check_common(dk, dv, dtype, KDA_MODE_DECAY_FIRST)) return st;
+  if (w < 2 || w > 8) return fail(KDA_ERR_SHAPE, "conv kernel size w=%d outside [2, 8]", w);
+  if (act != KDA_ACT_NONE && act != KDA_ACT_SILU) return fail(KDA_ERR_ARG, "act=%d is not a KDA_ACT_*", act);
+  if (!(g_min < 0.f)) return fail(KDA_ERR_ARG, "g_min=%g must be negative", (double)g_min);
+  if (H < 0) return fail(KDA_ERR_SHAPE, "negative H");
+  if (int st = check_seqlens(cu_seqlens, n_seqs, T)) return st;
+  if (ckpt_stride < 0) return fail(KDA_ERR_ARG, "negative ckpt_stride");
+  const int N = cu_seqlens ? n_seqs : 1;
+  if (T == 0 || H == 0 || N == 0) return ok();
+  if (!mixed_qkv || !conv_weight || !g_logits || !beta_logits || !q || !k || !v || !g || !beta)
+    return fail(KDA_ERR_ARG, "null pointer argument");
+  const void* al[] = {mixed_qkv, conv_weight, window_in, window_out, g_logits, beta_logits, q, k, v, g, beta, conv_ckpt};
+  for (const void* ptr : al)
+    if (ptr && !aligned16(ptr)) return fail(KDA_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const int64_t need = ckpt_stride > 0 ? kda_num_checkpoints(cu_seqlens, n_seqs, T, ckpt_stride) : 0;
+  if (conv_ckpt && ckpt_stride == 0) return fail(KDA_ERR_ARG, "conv_ckpt given with ckpt_stride 0");
+  if (conv_ckpt && num_ckpt < need)
+    return fail(KDA_ERR_SHAPE, "num_ckpt=%lld < %lld conv checkpoints", (long long)num_ckpt, (long long)need);
+  const size_t es = elem_size(dtype);
+  const size_t C = (size_t)H * (2 * dk + dv);
+  const void* ins[] = {mixed_qkv, conv_weight, window_in, g_logits, beta_logits};
+  const size_t in_bytes[] = {T * C * es, C * w * es, (size_t)N * (w - 1) * C * es, (size_t)T * H * dk * es,
+                             (size_t)T * H * es};
+  const void* outs[] = {q, k, v, g, beta, window_out, conv_ckpt};
+  const size_t out_bytes[] = {(size_t)T * H * dk * es, (size_t)T * H * dk * es, (size_t)T * H * dv * es,
+                              (size_t)T * H * dk * es, (size_t)T * H * es, (size_t)N * (w - 1) * C * es,
+                              (size_t)(conv_ckpt ? num_ckpt : 0) * (w - 1) * C * es};
+  for (int i = 0; i < 7; ++i) {
+    for (int j = 0; j < 5; ++j)
+      if (overlap(outs[i], out_bytes[i], ins[j], in_bytes[j])) return fail(KDA_ERR_ALIAS, "an output overlaps an input");
+    for (int j = 0; j < i; ++j)
+      if (overlap(outs[i], out_bytes[i], outs[j], out_bytes[j])) return fail(KDA_ERR_ALIAS, "two outputs overlap");
+  }
+  static thread_local kda::ProSched sched_storage;
+  kda::ProSched* sched = &sched_storage;
+  kda::ProArgs a{};
+  a.mixed = mixed_qkv; a.weight = conv_weight; a.g_logits = g_logits; a.beta_logits = beta_logits;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+  a.conv_ckpt = conv_ckpt; a.num_ckpt = conv_ckpt ? num_ckpt : 0;
+  a.H = H; a.dk = dk; a.dv = dv; a.w = w; a.dtype = dtype; a.act = act; a.ckpt_stride = ckpt_stride;
+  a.g_min = g_min; a.eps = 1e-6f;
+  int64_t ckb = 0;
+  for (int g0 = 0; g0 < N; g0 += kda::kMaxSeqs) {
+    const int n = std::min(kda::kMaxSeqs, N - g0);
+    sched->n_seqs = n;
+    int32_t tb = 0;
+    for (int i = 0; i < n; ++i) {
+      const int32_t st0 = cu_seqlens ? cu_seqlens[g0 + i] : 0;
+      const int32_t L = cu_seqlens ? cu_seqlens[g0 + i + 1] - st0 : (int32_t)T;
+      sched->start[i] = st0;
+      sched->len[i] = L;
+      sched->ckpt_base[i] = (int32_t)ckb;
+      if (ckpt_stride > 0) ckb += L / ckpt_stride;
+      sched->tile_base[i] = tb;
+      tb += (L + 31) / 32;
+    }
+    sched->tile_base[n] = tb;
+    const size_t woff = (size_t)g0 * (w - 1) * C * es;
+    a.window_in = window_in ? static_cast<const char*>(window_in) + woff : nullptr;
+    a.window_out = window_out ? static_cast<char*>(window_out) + woff : nullptr;
+    cudaError_t e = kda::launch_prologue(a, *sched, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status(e, "kda_input_prep launch");
+    // an empty sequence has no tile: its window passes through unchanged
+    if (window_out) {
+      const size_t wb = (size_t)(w - 1) * C * es;
+      for (int i = 0; i < n && e == cudaSuccess; ++i) {
+        if (sched->len[i] != 0) continue;
+        char* dst = static_cast<char*>(a.window_out) + i * wb;
+        e = window_in ? cudaMemcpyAsync(dst, static_cast<const char*>(a.window_in) + i * wb, wb,
+                                        cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream))
+                      : cudaMemsetAsync(dst, 0, wb, reinterpret_cast<cudaStream_t>(stream));
+      }
+      if (e != cudaSuccess) return cuda_status(e, "kda_input_prep window copy");
+    }
+  }
+  return ok();
 }
 
 // ---------------------------------------------------------------------------

@@ -41,6 +41,16 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// Two consecutive values as fp32 (8 B for fp32, 4 B for bf16), and back.
+__device__ __forceinline__ float2 load2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 load2(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void store2(float* p, float2 x) { *reinterpret_cast<float2*>(p) = x; }
+__device__ __forceinline__ void store2(__nv_bfloat16* p, float2 x) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(x.x, x.y);
+}
+
 // State streams through HBM once per call: evict-first loads and stores.
 __device__ __forceinline__ float4 ld_stream(const float* p) {
   return __ldcs(reinterpret_cast<const float4*>(p));

@@ -26,6 +26,14 @@ struct StepArgs {
   const int32_t* slot_out;     // device [B]: row b writes slot slot_out[b] (used when slot_in is set)
   int64_t n_slots;
   int layout;                  // KDA_LAYOUT_KV: state (dk, dv); KDA_LAYOUT_VK: state (dv, dk)
+  // decode with the input prologue fused in (mixed == nullptr: q, k, v, g, beta given)
+  const void* mixed;           // [B][H (2 dk + dv)] raw rows [q | k | v]
+  void* conv_state;            // [rows][w - 1][H (2 dk + dv)], row b (or slot_in[b]); shifted in place
+  const void* conv_w;          // [H (2 dk + dv)][w]
+  const void *g_logits, *beta_logits;       // [B][H][dk], [B][H]
+  void *q_out, *k_out, *v_out, *g_out, *beta_out;   // prepared projections [B][H][...] or nullptr
+  int conv_size, act;
+  float g_min, eps;
 };
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_step_kv_f32(const StepArgs& a, cudaStream_t s);
@@ -62,6 +70,30 @@ struct PrefillArgs {
 };
 cudaError_t launch_prefill(const PrefillArgs& a, const PrefillSched& sched, int max_len,
                            cudaStream_t s);
+
+// Input prologue (kda_prologue.cu): ShortConv over mixed_qkv rows [q | k | v],
+// activation, per-head L2Norm of q and k, gates from logits.  One launch covers
+// at most kMaxSeqs sequences; tiles of 32 tokens never span two sequences.
+struct ProSched {
+  int32_t n_seqs;
+  int32_t start[kMaxSeqs];       // first token of each sequence (absolute row of mixed)
+  int32_t len[kMaxSeqs];
+  int32_t ckpt_base[kMaxSeqs];   // index of each sequence's first conv checkpoint
+  int32_t tile_base[kMaxSeqs + 1];
+};
+struct ProArgs {
+  const void* mixed;             // [T][C], C = H (2 dk + dv)
+  const void* weight;            // [C][w]
+  const void* window_in;         // [n_seqs][w - 1][C] (offset to this launch) or nullptr
+  void* window_out;              // same shape or nullptr
+  const void *g_logits, *beta_logits;   // [T][H][dk], [T][H]
+  void *q, *k, *v, *g, *beta;    // [T][H][dk] x 2, [T][H][dv], [T][H][dk], [T][H]
+  void* conv_ckpt;               // [num_ckpt][w - 1][C] or nullptr
+  int64_t num_ckpt;
+  int H, dk, dv, w, dtype, act, ckpt_stride;
+  float g_min, eps;
+};
+cudaError_t launch_prologue(const ProArgs& a, const ProSched& sched, cudaStream_t s);
 
 // Tensor-core path (kda_prefill_tc.cu): shapes it takes and workspace bytes per
 // (64-token chunk, head).

@@ -80,7 +80,109 @@ __host__ __device__ constexpr size_t step_smem_floats(int steps) {
 template <int NT_CTA, int MAXS>
 constexpr int step_min_blocks() { return MAXS == 1 && NT_CTA < 512 ? 512 / NT_CTA : 1; }
 
-template <int DK, int DV, int NW, int HPC, int MAXS, typename T, bool TRANS>
+// Decode with the input prologue fused into the staging: raw mixed_qkv channels of
+// this head pass through the causal ShortConv (window read and shifted in place),
+// the activation, per-head L2Norm of q and k, and the gates from their logits.
+template <int DK, int DV, int NW, typename T>
+__device__ __forceinline__ void fused_prologue_stage(const StepArgs& a, int64_t b, int hh, int64_t crow,
+                                                     bool live, int tid, int lane, int warp, float* st,
+                                                     float* kqw, float* red, int64_t head_or_zero) {
+  const int64_t head = head_or_zero;       // 0 for a padding head past the batch (reads stay in bounds)
+  constexpr int NT = 32 * NW, MAXW = 8;
+  const int w = a.conv_size;
+  const int64_t Cw = (int64_t)a.H * (2 * DK + DV);
+  const T* X = reinterpret_cast<const T*>(a.mixed);
+  const T* Wt = reinterpret_cast<const T*>(a.conv_w);
+  T* win = reinterpret_cast<T*>(a.conv_state);
+  // one channel: y = sum_j weight[c, j] * in[j] over the window and the new input;
+  // the window moves up one row and takes the new input
+  auto conv = [&](int64_t col) -> float {
+    const float x = to_f32(X[b * Cw + col]);
+    T* wr = win + crow * (w - 1) * Cw + col;
+    float wv[MAXW - 1];
+#pragma unroll
+    for (int r = 0; r < MAXW - 1; ++r) wv[r] = r < w - 1 ? to_f32(wr[(int64_t)r * Cw]) : 0.f;
+    float y = to_f32(Wt[col * w + (w - 1)]) * x;
+#pragma unroll
+    for (int r = 0; r < MAXW - 1; ++r)
+      if (r < w - 1) y = fmaf(to_f32(Wt[col * w + r]), wv[r], y);
+    if (live) {
+#pragma unroll
+      for (int r = 0; r < MAXW - 1; ++r)
+        if (r < w - 1) wr[(int64_t)r * Cw] = from_f32<T>(r + 1 < w - 1 ? wv[r + 1] : x);
+    }
+    if (a.act == KDA_ACT_SILU) y *= 1.f / (1.f + expf(-y));
+    return y;
+  };
+  constexpr int EK = (DK + NT - 1) / NT, EV = (DV + NT - 1) / NT;
+  float yq[EK], yk[EK], yv[EV];
+  float ssq = 0.f, ssk = 0.f;
+#pragma unroll
+  for (int u = 0; u < EK; ++u) {
+    const int i = tid + u * NT;
+    yq[u] = yk[u] = 0.f;
+    if (i < DK) {
+      yq[u] = conv((int64_t)hh * DK + i);
+      yk[u] = conv((int64_t)a.H * DK + (int64_t)hh * DK + i);
+      ssq = fmaf(yq[u], yq[u], ssq);
+      ssk = fmaf(yk[u], yk[u], ssk);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < EV; ++u) {
+    const int j = tid + u * NT;
+    yv[u] = j < DV ? conv(2 * (int64_t)a.H * DK + (int64_t)hh * DV + j) : 0.f;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    ssq += __shfl_xor_sync(0xffffffffu, ssq, off);
+    ssk += __shfl_xor_sync(0xffffffffu, ssk, off);
+  }
+  if (lane == 0) { red[warp] = ssq; red[NW + warp] = ssk; }
+  __syncthreads();
+  ssq = 0.f; ssk = 0.f;
+#pragma unroll
+  for (int w2 = 0; w2 < NW; ++w2) { ssq += red[w2]; ssk += red[NW + w2]; }
+  const float iq = rsqrtf(ssq + a.eps), ik = rsqrtf(ssk + a.eps);
+  const T* gl = reinterpret_cast<const T*>(a.g_logits);
+  const bool keep = live && a.q_out != nullptr;
+  float kq = 0.f;
+#pragma unroll
+  for (int u = 0; u < EK; ++u) {
+    const int i = tid + u * NT;
+    if (i < DK) {
+      const float qn = yq[u] * iq, kn = yk[u] * ik;
+      const float gi = a.g_min / (1.f + expf(-to_f32(gl[head * DK + i])));
+      st[i] = kn;
+      st[DK + i] = qn;
+      st[2 * DK + i] = expf(gi);
+      kq = fmaf(kn, qn, kq);
+      if (keep) {
+        reinterpret_cast<T*>(a.q_out)[head * DK + i] = from_f32<T>(qn);
+        reinterpret_cast<T*>(a.k_out)[head * DK + i] = from_f32<T>(kn);
+        reinterpret_cast<T*>(a.g_out)[head * DK + i] = from_f32<T>(gi);
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < EV; ++u) {
+    const int j = tid + u * NT;
+    if (j < DV) {
+      st[3 * DK + j] = yv[u];
+      if (keep) reinterpret_cast<T*>(a.v_out)[head * DV + j] = from_f32<T>(yv[u]);
+    }
+  }
+  if (tid == 0) {
+    const float bt = 1.f / (1.f + expf(-to_f32(reinterpret_cast<const T*>(a.beta_logits)[head])));
+    st[3 * DK + DV] = bt;
+    if (keep) reinterpret_cast<T*>(a.beta_out)[head] = from_f32<T>(bt);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+  if (lane == 0) kqw[warp] = kq;
+}
+
+template <int DK, int DV, int NW, int HPC, int MAXS, typename T, bool TRANS, bool FUSED>
 __global__ void __launch_bounds__(32 * NW * HPC, (step_min_blocks<32 * NW * HPC, MAXS>()))
 kda_step_kernel(const StepArgs a) {
   using C = StepCfg<DK, DV, NW>;
@@ -145,6 +247,14 @@ kda_step_kernel(const StepArgs a) {
   const T* v = reinterpret_cast<const T*>(a.v);
   const T* g = reinterpret_cast<const T*>(a.g);
   const T* beta = reinterpret_cast<const T*>(a.beta);
+  if constexpr (FUSED) {
+    static_assert(MAXS == 1, "the fused prologue is a decode path");
+    // conv window row: the batch row, or its slot (row 0 stands in for a skipped
+    // slot; nothing is written there)
+    const int64_t crow = a.slot_in == nullptr ? (int64_t)b : live_state ? (int64_t)a.slot_in[b] : 0;
+    fused_prologue_stage<DK, DV, NW, T>(a, b, (int)(hl % a.H), crow, active && live_state, tid, lane, warp, stage,
+                                        kqw, red, active ? head : 0);
+  } else {
   // All steps' loads are issued before any is used (MAXS is 1 for decode, the
   // draft bound for replay), so staging costs one memory round trip, not one
   // per step.
@@ -195,6 +305,7 @@ kda_step_kernel(const StepArgs a) {
       for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
       if (lane == 0) kqw[s * NW + warp] = kq;
     }
+  }
   }
   __syncthreads();
 
@@ -350,7 +461,7 @@ kda_step_kernel(const StepArgs a) {
   for (int m = 0; m < RPT; ++m) st_stream(Sout + (rg + RG * m) * ROWLEN + 4 * c4, S[m]);
 }
 
-template <int DK, int DV, typename T, bool TRANS>
+template <int DK, int DV, typename T, bool TRANS, bool FUSED>
 cudaError_t launch_dims(const StepArgs& a, cudaStream_t s) {
   // rows per thread 16 where the head is big enough; at least 128 threads per CTA
   constexpr int TPR = DV / 4;
@@ -373,28 +484,30 @@ cudaError_t launch_dims(const StepArgs& a, cudaStream_t s) {
     kern<<<(unsigned)grid, block, total, s>>>(a);
     return cudaGetLastError();
   };
-  if (a.steps == 1) {
+  if (FUSED || a.steps == 1) {
     if constexpr (HMAX >= 4) {
-      if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, 1, T, TRANS>, 4);
+      if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, 1, T, TRANS, FUSED>, 4);
     }
     if constexpr (HMAX >= 2) {
-      if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, 1, T, TRANS>, 2);
+      if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, 1, T, TRANS, FUSED>, 2);
     }
-    return run(kda_step_kernel<DK, DV, NW, 1, 1, T, TRANS>, 1);
+    return run(kda_step_kernel<DK, DV, NW, 1, 1, T, TRANS, FUSED>, 1);
   }
   if constexpr (HMAX >= 4) {
-    if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, KDA_MAX_DRAFT, T, TRANS>, 4);
+    if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, KDA_MAX_DRAFT, T, TRANS, false>, 4);
   }
   if constexpr (HMAX >= 2) {
-    if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, KDA_MAX_DRAFT, T, TRANS>, 2);
+    if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, KDA_MAX_DRAFT, T, TRANS, false>, 2);
   }
-  return run(kda_step_kernel<DK, DV, NW, 1, KDA_MAX_DRAFT, T, TRANS>, 1);
+  return run(kda_step_kernel<DK, DV, NW, 1, KDA_MAX_DRAFT, T, TRANS, false>, 1);
 }
 
 template <typename T, bool TRANS>
 cudaError_t launch_layout(const StepArgs& a, cudaStream_t s) {
 #define KDA_CASE(DKv, DVv) \
-  if (a.dk == DKv && a.dv == DVv) return launch_dims<DKv, DVv, T, TRANS>(a, s);
+  if (a.dk == DKv && a.dv == DVv)                                     \
+    return a.mixed != nullptr ? launch_dims<DKv, DVv, T, TRANS, true>(a, s) \
+                              : launch_dims<DKv, DVv, T, TRANS, false>(a, s);
   KDA_CASE(32, 32) KDA_CASE(32, 64) KDA_CASE(32, 128)
   KDA_CASE(64, 32) KDA_CASE(64, 64) KDA_CASE(64, 128)
   KDA_CASE(128, 32) KDA_CASE(128, 64) KDA_CASE(128, 128)

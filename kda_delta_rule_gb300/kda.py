@@ -21,6 +21,7 @@ KDA_F32, KDA_BF16 = 0, 1
 DECAY_FIRST, UNDECAYED_DELTA = 0, 1
 PAGE_FREE, PAGE_KDA_STATE, PAGE_MLA_KV = 0, 1, 2
 LAYOUT_KV, LAYOUT_VK = 0, 1
+ACT_NONE, ACT_SILU = 0, 1
 MAX_DRAFT = 16
 
 
@@ -36,7 +37,7 @@ def _load():
             f"KDA CUDA library not found at {_LIB_PATH}; build it with "
             "`python -m kda_delta_rule_gb300.build` (needs nvcc for sm_103a)")
     lib = ctypes.CDLL(_LIB_PATH)
-    P, I, L, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    P, I, L, D, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_float
     sig = {
         "kda_version": ([], I),
         "kda_status_string": ([I], ctypes.c_char_p),
@@ -46,6 +47,8 @@ def _load():
         "kda_verify_replay_layers": ([I, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
         "kda_decode_step_slots": ([P, L, P, I, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
         "kda_verify_replay_slots": ([I, P, P, L, P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
+        "kda_decode_step_fused": ([P, L, P, I, P, P, P, I, P, P, F, I, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
+        "kda_input_prep": ([P, P, I, P, P, P, P, F, I, P, I, L, I, I, I, I, P, P, P, P, P, I, P, L, P], I),
         "kda_num_checkpoints": ([P, I, L, I], L),
         "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, I, P], I),
         "kda_prefill_workspace_bytes": ([P, I, L, I, I, I, I], L),
@@ -358,6 +361,96 @@ def kda_device_errors() -> int:
     flags = ctypes.c_int(0)
     _check(_lib.kda_device_errors(ctypes.byref(flags)), "kda_device_errors")
     return int(flags.value)
+
+
+def kda_input_prep(mixed, conv_weight, g_logits, beta_logits, cu_seqlens=None, window_in=None,
+                   window_out=None, g_min=-5.0, act=ACT_SILU, ckpt_stride=0, conv_ckpt=None, out=None,
+                   stream=None):
+    """Input prologue for prefill: ShortConv + activation + L2Norm of q, k + gates from logits.
+
+    mixed (T, H*(2dk+dv)) rows [q | k | v]; conv_weight (C, w); g_logits (T,H,dk);
+    beta_logits (T,H); window_in / window_out (N, w-1, C) or None; conv_ckpt
+    (num_ckpt, w-1, C) or None (needs ckpt_stride). out: optional dict of q,k,v,g,beta.
+    Returns dict q, k, g (T,H,dk), v (T,H,dv), beta (T,H) in mixed's dtype.
+    """
+    T, C = mixed.shape
+    H, dk = g_logits.shape[1], g_logits.shape[2]
+    dv = C // H - 2 * dk
+    if dv <= 0 or H * (2 * dk + dv) != C:
+        raise ValueError(f"mixed width {C} does not split as H*(2*dk+dv) with H={H}, dk={dk}")
+    dt = mixed.dtype
+    code = _dtype_code(mixed)
+    w = conv_weight.shape[1]
+    arr, N = _cu_array(cu_seqlens)
+    _cuda("mixed", mixed, dt)
+    _cuda("conv_weight", conv_weight, dt, (C, w))
+    _cuda("g_logits", g_logits, dt, (T, H, dk))
+    _cuda("beta_logits", beta_logits, dt, (T, H))
+    for name, t in (("window_in", window_in), ("window_out", window_out)):
+        if t is not None:
+            _cuda(name, t, dt, (N, w - 1, C))
+    n_ck = 0
+    if conv_ckpt is not None:
+        n_ck = conv_ckpt.shape[0]
+        _cuda("conv_ckpt", conv_ckpt, dt, (n_ck, w - 1, C))
+    if out is None:
+        dev = mixed.device
+        out = {"q": torch.empty(T, H, dk, dtype=dt, device=dev), "k": torch.empty(T, H, dk, dtype=dt, device=dev),
+               "v": torch.empty(T, H, dv, dtype=dt, device=dev), "g": torch.empty(T, H, dk, dtype=dt, device=dev),
+               "beta": torch.empty(T, H, dtype=dt, device=dev)}
+    for n, shp in (("q", (T, H, dk)), ("k", (T, H, dk)), ("v", (T, H, dv)), ("g", (T, H, dk)), ("beta", (T, H))):
+        _cuda(n, out[n], dt, shp)
+    _check(_lib.kda_input_prep(_ptr(mixed), _ptr(conv_weight), w, _ptr(window_in), _ptr(window_out),
+                               _ptr(g_logits), _ptr(beta_logits), float(g_min), act, arr, N, T, H, dk, dv, code,
+                               _ptr(out["q"]), _ptr(out["k"]), _ptr(out["v"]), _ptr(out["g"]), _ptr(out["beta"]),
+                               int(ckpt_stride), _ptr(conv_ckpt), n_ck, _stream(stream, mixed.device)),
+           "kda_input_prep")
+    return out
+
+
+def kda_decode_step_fused(S, conv_state, mixed, conv_weight, g_logits, beta_logits, o=None, slot_ids=None,
+                          layout=LAYOUT_KV, g_min=-5.0, act=ACT_SILU, keep_projections=False,
+                          mode=DECAY_FIRST, stream=None):
+    """One decode token with the input prologue fused in; S and conv_state updated in place.
+
+    S (B or n_slots, H, <state>) fp32; conv_state (B or n_slots, w-1, C); mixed (B, C);
+    conv_weight (C, w); g_logits (B,H,dk); beta_logits (B,H); slot_ids int32 (B,) or None.
+    Returns o (B,H,dv), or (o, dict of the prepared q,k,v,g,beta) with keep_projections.
+    """
+    B, H, dk = g_logits.shape
+    C = mixed.shape[1]
+    dv = C // H - 2 * dk
+    dt = mixed.dtype
+    code = _dtype_code(mixed)
+    w = conv_weight.shape[1]
+    rows = S.shape[0]
+    _cuda("S", S, torch.float32, (rows, H, *_state_dims(layout, dk, dv)))
+    _cuda("conv_state", conv_state, dt, (rows, w - 1, C))
+    _cuda("mixed", mixed, dt, (B, C))
+    _cuda("conv_weight", conv_weight, dt, (C, w))
+    _cuda("g_logits", g_logits, dt, (B, H, dk))
+    _cuda("beta_logits", beta_logits, dt, (B, H))
+    if slot_ids is not None:
+        _cuda("slot_ids", slot_ids, torch.int32, (B,))
+    elif rows != B:
+        raise ValueError(f"S has {rows} rows for a batch of {B} and no slot_ids")
+    if o is None:
+        o = torch.empty(B, H, dv, dtype=dt, device=mixed.device)
+    _cuda("o", o, dt, (B, H, dv))
+    kept = None
+    if keep_projections:
+        dev = mixed.device
+        kept = {"q": torch.zeros(B, H, dk, dtype=dt, device=dev), "k": torch.zeros(B, H, dk, dtype=dt, device=dev),
+                "v": torch.zeros(B, H, dv, dtype=dt, device=dev), "g": torch.zeros(B, H, dk, dtype=dt, device=dev),
+                "beta": torch.zeros(B, H, dtype=dt, device=dev)}
+    kp = kept or {}
+    _check(_lib.kda_decode_step_fused(_ptr(S), rows, _ptr(slot_ids), layout, _ptr(conv_state), _ptr(mixed),
+                                      _ptr(conv_weight), w, _ptr(g_logits), _ptr(beta_logits), float(g_min), act,
+                                      _ptr(o), _ptr(kp.get("q")), _ptr(kp.get("k")), _ptr(kp.get("v")),
+                                      _ptr(kp.get("g")), _ptr(kp.get("beta")), B, H, dk, dv, code, mode,
+                                      _stream(stream, mixed.device)),
+           "kda_decode_step_fused")
+    return (o, kept) if keep_projections else o
 
 
 def kda_prefill_chunked(S0, q, k, v, g, beta, cu_seqlens=None, chunk=64, ckpt_stride=512,

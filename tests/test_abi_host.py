@@ -199,6 +199,51 @@ def test_slot_entries_validation(K):
     assert rep(P(0), P(8 << 20), P(7 << 24), None, layers=0) == 0
 
 
+def test_prologue_entries_validation(K):
+    """kda_input_prep / kda_decode_step_fused: kernel size, activation, g_min, partial
+    projection outputs and aliasing are rejected before any launch."""
+    f = K._lib.kda_input_prep
+    cu = (ctypes.c_int32 * 3)(0, 40, 100)
+
+    def prep(**kw):
+        a = dict(mixed=P(1 << 24), wt=P(2 << 24), w=4, win_in=None, win_out=None, gl=P(3 << 24), bl=P(4 << 24),
+                 g_min=-5.0, act=1, cu=cu, n=2, T=100, H=2, dk=32, dv=32, dtype=0, q=P(5 << 24), k=P(6 << 24),
+                 v=P(7 << 24), g=P(8 << 24), beta=P(9 << 24), stride=0, ck=None, nck=0)
+        a.update(kw)
+        return f(a["mixed"], a["wt"], a["w"], a["win_in"], a["win_out"], a["gl"], a["bl"], a["g_min"], a["act"],
+                 a["cu"], a["n"], a["T"], a["H"], a["dk"], a["dv"], a["dtype"], a["q"], a["k"], a["v"], a["g"],
+                 a["beta"], a["stride"], a["ck"], a["nck"], None)
+
+    assert prep(w=1) == -2 and prep(w=9) == -2
+    assert prep(act=2) == -1
+    assert prep(g_min=0.0) == -1
+    assert prep(q=None) == -1
+    assert prep(q=P((1 << 24) + 64)) == -7                      # q inside mixed
+    assert prep(k=P((5 << 24) + 16)) == -7                      # k overlaps q
+    assert prep(ck=P(10 << 24), stride=0) == -1
+    assert prep(ck=P(10 << 24), stride=32, nck=1) == -2         # 1 + 1 checkpoints needed
+    assert prep(T=101) == -2                                   # cu_seqlens does not end at T
+    assert prep(H=0) == 0
+    d = K._lib.kda_decode_step_fused
+
+    def dec(**kw):
+        a = dict(S=P(0), n_slots=0, slots=None, layout=0, conv=P(1 << 24), mixed=P(2 << 24), wt=P(3 << 24), w=4,
+                 gl=P(4 << 24), bl=P(5 << 24), g_min=-5.0, act=1, o=P(6 << 24), qo=None, ko=None, vo=None,
+                 go=None, bo=None, B=2, H=2, dk=32, dv=32, dtype=0, mode=0)
+        a.update(kw)
+        return d(a["S"], a["n_slots"], a["slots"], a["layout"], a["conv"], a["mixed"], a["wt"], a["w"], a["gl"],
+                 a["bl"], a["g_min"], a["act"], a["o"], a["qo"], a["ko"], a["vo"], a["go"], a["bo"], a["B"], a["H"],
+                 a["dk"], a["dv"], a["dtype"], a["mode"], None)
+
+    assert dec(qo=P(7 << 24)) == -1                            # only some projection outputs
+    assert dec(layout=5) == -1
+    assert dec(slots=P(8 << 24), n_slots=0) == -2
+    assert dec(conv=P(64)) == -7                                # conv window inside S
+    assert dec(w=9) == -2
+    assert dec(conv=None) == -1
+    assert dec(B=0) == 0
+
+
 def test_prefill_validation(K):
     f = K._lib.kda_prefill_chunked
     cu = (ctypes.c_int32 * 3)(0, 100, 228)
