@@ -185,7 +185,8 @@ int kda_decode_step_slots(float* S_pool, int64_t n_slots, const int32_t* slot_id
  *              conv_state; ids outside [0, n_slots) give zero output and touch
  *              nothing; valid ids must be distinct
  *   conv_state device dtype [B or n_slots, w-1, C], C = H*(2*dk + dv), in/out
- *   mixed_qkv  device dtype [B, C] in; conv_weight [C, w] in, 2 <= w <= 8
+ *   mixed_qkv  device dtype [B, C] in; conv_weight [C, w] in, 2 <= w <= 4 (the
+ *              window sits in registers; kda_input_prep takes up to 8)
  *   g_logits   device dtype [B, H, dk]; beta_logits [B, H]   in
  *   o          device dtype [B, H, dv] out
  *   q_out, k_out, g_out [B,H,dk], v_out [B,H,dv], beta_out [B,H]: all NULL, or

@@ -5,6 +5,10 @@
     python -m kda_delta_rule_gb300.cases prefill  [--reps N]   # T=8192 H=32 d=128 bf16, 16 checkpoints
     python -m kda_delta_rule_gb300.cases varlen   [--reps N]   # 64 seqs, ~0.5M tokens, H=32 d=128 bf16
     python -m kda_delta_rule_gb300.cases pack     [--reps N]   # pack+unpack of a (256,32,128,128) state
+    python -m kda_delta_rule_gb300.cases layer    [--reps N]   # kda_input_prep then prefill, T=8192 H=32 d=128
+    python -m kda_delta_rule_gb300.cases prologue [--reps N]   # kda_input_prep alone, T=8192 H=32 d=128 bf16
+    python -m kda_delta_rule_gb300.cases decode_vk    [--reps N]   # decode on 256 of 512 transposed pool slots
+    python -m kda_delta_rule_gb300.cases decode_fused [--reps N]   # decode with the input prologue, B=256
 
 Each case prints the mean device time per call measured with CUDA events.
 """
@@ -80,8 +84,55 @@ def case_pack(reps):
     return _time(run, reps)
 
 
+def case_layer(reps, T=8192, H=32, d=128, w=4):
+    raw, cu = I.prologue_inputs([T], H, d, d, w=w, dtype=torch.bfloat16, seed=0, device="cuda")
+    S0, _, _ = I.prefill_inputs([T], H, d, d, dtype=torch.bfloat16, seed=1, device="cuda")
+    p = K.kda_input_prep(raw["mixed"], raw["weight"], raw["g_logits"], raw["beta_logits"], window_in=raw["window"])
+    pool = K.PagePool(H * d * d * 4, T // 512)
+    ids = torch.tensor(pool.alloc(T // 512), dtype=torch.int32, device="cuda")
+    o = torch.empty(T, H, d, dtype=torch.bfloat16, device="cuda")
+    Sf = torch.empty_like(S0)
+    ws = torch.empty(K.kda_prefill_workspace_bytes(cu, T, H, d, d, torch.bfloat16), dtype=torch.uint8, device="cuda")
+
+    def run():
+        K.kda_input_prep(raw["mixed"], raw["weight"], raw["g_logits"], raw["beta_logits"], window_in=raw["window"],
+                         out=p)
+        K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu, ckpt_stride=512,
+                              page_pool=pool, ckpt_page_ids=ids, o=o, S_final=Sf, workspace=ws)
+    return _time(run, reps)
+
+
+def case_prologue(reps, T=8192, H=32, d=128, w=4):
+    raw, _ = I.prologue_inputs([T], H, d, d, w=w, dtype=torch.bfloat16, seed=0, device="cuda")
+    p = K.kda_input_prep(raw["mixed"], raw["weight"], raw["g_logits"], raw["beta_logits"], window_in=raw["window"])
+    return _time(lambda: K.kda_input_prep(raw["mixed"], raw["weight"], raw["g_logits"], raw["beta_logits"],
+                                          window_in=raw["window"], out=p), reps)
+
+
+def case_decode_vk(reps, H=32, d=128, B=256):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    pool = (0.05 * torch.randn(2 * B, H, d, d, generator=gen, device="cuda")).contiguous()
+    slots = torch.randperm(2 * B, generator=gen, device="cuda")[:B].to(torch.int32)
+    p = I.decode_step_projections(B, H, d, d, dtype=torch.bfloat16, seed=1, device="cuda")
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+    return _time(lambda: K.kda_decode_step_slots(pool, slots, p["q"], p["k"], p["v"], p["g"], p["beta"], o=o,
+                                                 layout=K.LAYOUT_VK), reps)
+
+
+def case_decode_fused(reps, H=32, d=128, B=256, w=4):
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    S = (0.05 * torch.randn(B, H, d, d, generator=gen, device="cuda")).contiguous()
+    raw, _ = I.prologue_inputs([1] * B, H, d, d, w=w, dtype=torch.bfloat16, seed=2, device="cuda")
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+    return _time(lambda: K.kda_decode_step_fused(S, raw["window"], raw["mixed"], raw["weight"], raw["g_logits"],
+                                                 raw["beta_logits"], o=o), reps)
+
+
 CASES = {"decode": case_decode, "replay": case_replay, "prefill": case_prefill,
-         "varlen": case_varlen, "pack": case_pack}
+         "varlen": case_varlen, "pack": case_pack, "layer": case_layer, "prologue": case_prologue, "decode_vk": case_decode_vk,
+         "decode_fused": case_decode_fused}
 
 
 def main():

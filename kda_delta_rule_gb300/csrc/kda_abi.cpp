@@ -200,7 +200,7 @@ int kda_decode_step_fused(float* S, int64_t n_slots, const int32_t* slot_ids, in
   if (layout != KDA_LAYOUT_KV && layout != KDA_LAYOUT_VK) return fail(KDA_ERR_ARG, "layout=%d is not a KDA_LAYOUT_*", layout);
   if (slot_ids && (n_slots < 1 || n_slots > ((int64_t)1 << 40)))
     return fail(KDA_ERR_SHAPE, "n_slots=%lld outside [1, 2^40]", (long long)n_slots);
-  if (w < 2 || w > 8) return fail(KDA_ERR_SHAPE, "conv kernel size w=%d outside [2, 8]", w);
+  if (w < 2 || w > 4) return fail(KDA_ERR_SHAPE, "conv kernel size w=%d outside [2, 4] (fused decode)", w);
   if (act != KDA_ACT_NONE && act != KDA_ACT_SILU) return fail(KDA_ERR_ARG, "act=%d is not a KDA_ACT_*", act);
   if (!(g_min < 0.f)) return fail(KDA_ERR_ARG, "g_min=%g must be negative", (double)g_min);
   if (!S || !conv_state || !mixed_qkv || !conv_weight || !g_logits || !beta_logits || !o)
@@ -329,6 +329,7 @@ int64_t kda_prefill_workspace_bytes(const int32_t* cu_seqlens, int n_seqs, int64
 int kda_device_errors(int* flags) {
   if (!flags) return fail(KDA_ERR_ARG, "flags is NULL");
   int e = kda::read_and_clear_device_errors(flags);
+  if (e == 0) e = kda::read_and_clear_prologue_errors(flags);
   if (e != 0) return cuda_status((cudaError_t)e, "kda_device_errors");
   return ok();
 }
@@ -480,6 +481,7 @@ int kda_input_prep(const void* mixed_qkv, const void* conv_weight, int w, const 
   a.conv_ckpt = conv_ckpt; a.num_ckpt = conv_ckpt ? num_ckpt : 0;
   a.H = H; a.dk = dk; a.dv = dv; a.w = w; a.dtype = dtype; a.act = act; a.ckpt_stride = ckpt_stride;
   a.g_min = g_min; a.eps = 1e-6f;
+  a.T = T;
   int64_t ckb = 0;
   for (int g0 = 0; g0 < N; g0 += kda::kMaxSeqs) {
     const int n = std::min(kda::kMaxSeqs, N - g0);
@@ -493,7 +495,7 @@ int kda_input_prep(const void* mixed_qkv, const void* conv_weight, int w, const 
       sched->ckpt_base[i] = (int32_t)ckb;
       if (ckpt_stride > 0) ckb += L / ckpt_stride;
       sched->tile_base[i] = tb;
-      tb += (L + 31) / 32;
+      tb += (L + kda::kPrologueTile - 1) / kda::kPrologueTile;
     }
     sched->tile_base[n] = tb;
     const size_t woff = (size_t)g0 * (w - 1) * C * es;

@@ -73,7 +73,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, const PrefillSched& sched, int 
 
 // Input prologue (kda_prologue.cu): ShortConv over mixed_qkv rows [q | k | v],
 // activation, per-head L2Norm of q and k, gates from logits.  One launch covers
-// at most kMaxSeqs sequences; tiles of 32 tokens never span two sequences.
+// at most kMaxSeqs sequences; tiles of kPrologueTile tokens never span two sequences.
+constexpr int kPrologueTile = 32;
 struct ProSched {
   int32_t n_seqs;
   int32_t start[kMaxSeqs];       // first token of each sequence (absolute row of mixed)
@@ -90,10 +91,13 @@ struct ProArgs {
   void *q, *k, *v, *g, *beta;    // [T][H][dk] x 2, [T][H][dv], [T][H][dk], [T][H]
   void* conv_ckpt;               // [num_ckpt][w - 1][C] or nullptr
   int64_t num_ckpt;
+  int64_t T;                     // rows of mixed and of the logits
   int H, dk, dv, w, dtype, act, ckpt_stride;
   float g_min, eps;
 };
 cudaError_t launch_prologue(const ProArgs& a, const ProSched& sched, cudaStream_t s);
+// Copy the prologue kernel's device error word to *flags (OR) and clear it.
+int read_and_clear_prologue_errors(int* flags);
 
 // Tensor-core path (kda_prefill_tc.cu): shapes it takes and workspace bytes per
 // (64-token chunk, head).

@@ -31,6 +31,7 @@
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "kda_tc.cuh"
+#include "kda_tmap.h"
 #include "../../include/kda.h"
 
 #include <cstdio>
@@ -109,13 +110,6 @@ __device__ __forceinline__ int find_seq(const PrefillSched& s, int chunk) {
 __device__ __forceinline__ bool cta_wait(uint32_t mbar, uint32_t parity) {
   const bool ok = mbar_wait(mbar, parity);
   return __syncthreads_and(ok) != 0;
-}
-
-// 2-D tiled TMA load (tile mode) into shared memory, completion on mbar.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(mbar) : "memory");
 }
 
 // Tensor maps of one prefill launch: k and q as [T][H*128] with a 64 x 64 box
@@ -915,33 +909,9 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   if (warp == ISSUER) tmem_dealloc(tmem, 256);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
 // [T][cols] bf16 tensor map with a box of box_x columns x 64 rows
 bool make_map(CUtensorMap* m, const void* base, int64_t T, int64_t cols, int box_x, bool swizzle128) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)T};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)box_x, 64};
-  cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_map_2d(m, base, T, cols, 2, box_x, 64, swizzle128);
 }
 
 template <int DV>

@@ -8,26 +8,43 @@
 // raw rows before the boundary (same page, section "SGLang：从一次较长的 extend
 // 调用中提取检查点").
 //
-// One CTA per (32-token tile of one sequence, head); each thread owns two
-// adjacent channels of the head's q, k or v columns, so every row access of a
-// warp is one contiguous 64- or 128-byte piece.  The tile's raw inputs and the
-// w - 1 rows before it sit in registers; the convolution runs from the newest
-// token down so each output overwrites an input no later output needs.  The sum
-// of squares of a token's q (k) is reduced with shuffles inside the lanes of the
-// group and across its warps through shared memory.  HBM-bound: every input
-// element is read once (plus the w - 1 halo rows per tile) and every output
-// written once.
+// One CTA per (32-token tile of one sequence, head), the CTAs of one tile
+// adjacent in the grid.  One thread issues four TMA copies: the head's q, k and v
+// columns of mixed_qkv for the tile plus the w - 1 rows before it, and the tile's
+// gate logits, all into shared memory, completion on one mbarrier (bounded wait).
+// The first tile of a sequence then overwrites its halo rows with the carried
+// window.  Each lane owns eight adjacent channels (one 16-byte shared-memory read
+// and one 16-byte global store per token) of q, k, v or the gate logits and walks
+// the tile's tokens in order with the conv window rolling through registers:
+// convolution, activation, for q and k the L2Norm (its sum of squares reduced
+// over the row's lanes with shuffles), store.  Window and conv-checkpoint rows
+// are copied raw from shared memory.  HBM-bound: every input element is read once
+// (plus the halo rows, mostly from L2) and every output written once.
+#include <climits>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
+#include "kda_tc.cuh"
+#include "kda_tmap.h"
 #include "../../include/kda.h"
 
 namespace kda {
 namespace {
 
-constexpr int TT = 32;     // tokens per tile
-constexpr int MAXW = 8;    // largest conv kernel size (the window lives in registers)
+using tc::mbar_init;
+using tc::mbar_init_fence;
+using tc::mbar_expect_tx;
+using tc::mbar_wait;
+using tc::smem_u32;
+using tc::tma_load_2d;
 
-__device__ __forceinline__ float sigm(float x) { return 1.f / (1.f + expf(-x)); }
+constexpr int TT = kPrologueTile;  // tokens per tile
+constexpr int VEC = 8;             // channels per lane
+constexpr int MAXW = 8;            // largest conv kernel size
+
+// sigmoid through the hardware exp2 and reciprocal (about 2 ulp; 0 for very
+// negative x, where 1 + e^-x overflows)
+__device__ __forceinline__ float sigm(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 __device__ __forceinline__ int find_tile_seq(const ProSched& s, int tile) {
   int lo = 0, hi = s.n_seqs - 1;
@@ -38,22 +55,43 @@ __device__ __forceinline__ int find_tile_seq(const ProSched& s, int tile) {
   return lo;
 }
 
-template <int DK, int DV>
-struct ProCfg {
-  static constexpr int NCH2 = DK + DV / 2;                  // channel pairs of one head
-  static constexpr int NT = (NCH2 + 31) / 32 * 32;
-  static constexpr int SEG = DK / 2 < 32 ? DK / 2 : 32;     // lanes of one reduction segment
-  static constexpr int NSEG = DK / 2 / SEG;                 // segments per q (or k) group
+struct ProMaps {
+  CUtensorMap qk;   // mixed [T][C], box DK x (TT + W - 1)
+  CUtensorMap v;    // mixed [T][C], box DV x (TT + W - 1)
+  CUtensorMap g;    // g_logits [T][H * DK], box DK x TT
 };
 
-template <int DK, int DV, typename T>
-__global__ void __launch_bounds__(ProCfg<DK, DV>::NT)
-kda_prologue_kernel(const ProArgs a, const ProSched sched) {
-  using Cfg = ProCfg<DK, DV>;
-  __shared__ float red[2 * Cfg::NSEG][TT];
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int h = blockIdx.y, H = a.H, w = a.w;
-  const int tile = blockIdx.x;
+__host__ __device__ constexpr int up128(int x) { return (x + 127) / 128 * 128; }
+
+// lanes of one head: q [0, NQ), k [NQ, 2 NQ), v [2 NQ, 2 NQ + NV), gate logits after
+template <int DK, int DV, int W, typename T>
+struct ProCfg {
+  static constexpr int NQ = DK / VEC, NV = DV / VEC;
+  static constexpr int LH = 3 * NQ + NV;
+  static constexpr int NT = (LH + 31) / 32 * 32;
+  static constexpr int HALO = W - 1, ROWS = TT + HALO;
+  static constexpr int ES = (int)sizeof(T);
+  static constexpr int QB = ROWS * DK * ES, VB = ROWS * DV * ES, GB = TT * DK * ES;
+  static constexpr int OQ = 0, OK = up128(QB), OV = OK + up128(QB), OG = OV + up128(VB);
+  static constexpr int SMEM = OG + up128(GB) + 128;           // + alignment slack
+  static constexpr uint32_t TX = 2 * QB + VB + GB;            // bytes the four copies deliver
+  static_assert(2 * NQ <= 32, "q and k rows of a head share one warp");
+};
+
+// W: the conv kernel size, or MAXW for any size up to MAXW (taps past w are zero)
+template <int DK, int DV, int W, typename T>
+__global__ void __launch_bounds__(ProCfg<DK, DV, W, T>::NT)
+kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant__ ProMaps maps) {
+  using Cfg = ProCfg<DK, DV, W, T>;
+  constexpr int NQ = Cfg::NQ, NV = Cfg::NV, HALO = Cfg::HALO;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+  __shared__ uint64_t bar_word;
+  const uint32_t bar = smem_u32(&bar_word);
+
+  const int l = threadIdx.x;
+  const int H = a.H, w = W == MAXW ? a.w : W;
+  const int h = (int)(blockIdx.x % (unsigned)H), tile = (int)(blockIdx.x / (unsigned)H);
   const int n = find_tile_seq(sched, tile);
   const int64_t s0 = sched.start[n];
   const int len = sched.len[n];
@@ -62,128 +100,185 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched) {
   const int64_t t0 = s0 + pos0;
   const int64_t C = (int64_t)H * (2 * DK + DV);
 
-  // this thread's column pair: group 0 = q, 1 = k, 2 = v, 3 = none
-  int grp, c;
-  if (tid < DK / 2) { grp = 0; c = 2 * tid; }
-  else if (tid < DK) { grp = 1; c = 2 * (tid - DK / 2); }
-  else if (tid < Cfg::NCH2) { grp = 2; c = 2 * (tid - DK); }
-  else { grp = 3; c = 0; }
-  const int64_t col = grp == 0 ? (int64_t)h * DK + c
-                    : grp == 1 ? (int64_t)H * DK + (int64_t)h * DK + c
-                               : 2 * (int64_t)H * DK + (int64_t)h * DV + c;
-  const bool mine = grp < 3;
-  const T* x = reinterpret_cast<const T*>(a.mixed);
-  const T* win = reinterpret_cast<const T*>(a.window_in);
-  const T* wt = reinterpret_cast<const T*>(a.weight);
-
-  // raw input of position p (< 0: the carried window, zeros without one)
-  auto raw = [&](int p) -> float2 {
-    if (p >= 0) return load2(x + (s0 + p) * C + col);
-    if (win == nullptr) return make_float2(0.f, 0.f);
-    const T* r = win + ((int64_t)n * (w - 1) + (w - 1 + p)) * C + col;
-    return load2(r);
-  };
-
-  // taps by distance back from the newest input: wr[d] = weight[:, w - 1 - d]
-  float2 wr[MAXW];
-  float2 z[TT + MAXW - 1];                 // z[MAXW - 1 + t] = input of tile token t
-  if (mine) {
-#pragma unroll
-    for (int d = 0; d < MAXW; ++d)
-      wr[d] = d < w ? make_float2(to_f32(wt[col * w + (w - 1 - d)]), to_f32(wt[(col + 1) * w + (w - 1 - d)]))
-                    : make_float2(0.f, 0.f);
-#pragma unroll
-    for (int t = 0; t < TT; ++t) z[MAXW - 1 + t] = t < L ? load2(x + (t0 + t) * C + col) : make_float2(0.f, 0.f);
-#pragma unroll
-    for (int r = 1; r < MAXW; ++r) z[MAXW - 1 - r] = r < w ? raw(pos0 - r) : make_float2(0.f, 0.f);
-    // newest token first: output t overwrites input t, which no earlier token reads
-#pragma unroll
-    for (int t = TT - 1; t >= 0; --t) {
-      float2 y = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int d = 0; d < MAXW; ++d) {
-        y.x = fmaf(wr[d].x, z[MAXW - 1 + t - d].x, y.x);
-        y.y = fmaf(wr[d].y, z[MAXW - 1 + t - d].y, y.y);
-      }
-      if (a.act == KDA_ACT_SILU) { y.x *= sigm(y.x); y.y *= sigm(y.y); }
-      z[MAXW - 1 + t] = y;
-    }
-  } else {
-#pragma unroll
-    for (int t = 0; t < TT + MAXW - 1; ++t) z[t] = make_float2(0.f, 0.f);
-  }
-
-  // per-token sums of squares of q and k over the head
-  const int gi = tid % (DK / 2), seg = gi / Cfg::SEG;
-#pragma unroll
-  for (int t = 0; t < TT; ++t) {
-    const float2 y = z[MAXW - 1 + t];
-    float ss = grp < 2 ? fmaf(y.x, y.x, y.y * y.y) : 0.f;
-#pragma unroll
-    for (int off = Cfg::SEG / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if (grp < 2 && (lane % Cfg::SEG) == 0) red[grp * Cfg::NSEG + seg][t] = ss;
+  if (l == 0) {
+    mbar_init(bar, 1);
+    mbar_init_fence();
   }
   __syncthreads();
-
-  if (grp < 2) {
-    T* out = reinterpret_cast<T*>(grp == 0 ? a.q : a.k);
-    const T* gl = reinterpret_cast<const T*>(a.g_logits);
-    T* gout = reinterpret_cast<T*>(a.g);
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      if (t >= L) break;
-      float ss = 0.f;
-#pragma unroll
-      for (int sgi = 0; sgi < Cfg::NSEG; ++sgi) ss += red[grp * Cfg::NSEG + sgi][t];
-      const float inv = rsqrtf(ss + a.eps);
-      const float2 y = z[MAXW - 1 + t];
-      const int64_t o = ((t0 + t) * H + h) * DK + c;
-      store2(out + o, make_float2(y.x * inv, y.y * inv));
-      if (grp == 0) {
-        const float2 lg = load2(gl + o);
-        store2(gout + o, make_float2(a.g_min * sigm(lg.x), a.g_min * sigm(lg.y)));
-      }
-    }
-  } else if (grp == 2) {
-    T* out = reinterpret_cast<T*>(a.v);
-#pragma unroll
-    for (int t = 0; t < TT; ++t)
-      if (t < L) store2(out + ((t0 + t) * H + h) * DV + c, z[MAXW - 1 + t]);
+  if (l == 0) {
+    mbar_expect_tx(bar, Cfg::TX);
+    const int y0 = (int)(t0 - HALO);                       // may be negative: rows there read as zero
+    tma_load_2d(smem_u32(sm + Cfg::OQ), &maps.qk, h * DK, y0, bar);
+    tma_load_2d(smem_u32(sm + Cfg::OK), &maps.qk, H * DK + h * DK, y0, bar);
+    tma_load_2d(smem_u32(sm + Cfg::OV), &maps.v, 2 * H * DK + h * DV, y0, bar);
+    tma_load_2d(smem_u32(sm + Cfg::OG), &maps.g, h * DK, (int)t0, bar);
   }
-  if (tid < L) {
+
+  // role: 0 q, 1 k, 2 v (conv lanes), 3 gate logits, 4 none
+  int role, c;
+  if (l < NQ) { role = 0; c = VEC * l; }
+  else if (l < 2 * NQ) { role = 1; c = VEC * (l - NQ); }
+  else if (l < 2 * NQ + NV) { role = 2; c = VEC * (l - 2 * NQ); }
+  else if (l < 3 * NQ + NV) { role = 3; c = VEC * (l - 2 * NQ - NV); }
+  else { role = 4; c = 0; }
+  const bool conv_lane = role < 3;
+  const int64_t col = role == 0 ? (int64_t)h * DK + c
+                    : role == 1 ? (int64_t)H * DK + (int64_t)h * DK + c
+                                : 2 * (int64_t)H * DK + (int64_t)h * DV + c;
+  const int width = role == 2 ? DV : DK;                   // elements per shared-memory row of this lane's tile
+  const T* tile_s = reinterpret_cast<const T*>(sm + (role == 0 ? Cfg::OQ : role == 1 ? Cfg::OK
+                                                     : role == 2 ? Cfg::OV : Cfg::OG)) + c;
+  T* dst = nullptr;
+  int64_t dstride = 0;
+  if (conv_lane) {
+    const int64_t dcol = role == 2 ? (int64_t)h * DV + c : (int64_t)h * DK + c;
+    dstride = role == 2 ? (int64_t)H * DV : (int64_t)H * DK;
+    dst = reinterpret_cast<T*>(role == 0 ? a.q : role == 1 ? a.k : a.v) + t0 * dstride + dcol;
+  } else if (role == 3) {
+    dstride = (int64_t)H * DK;
+    dst = reinterpret_cast<T*>(a.g) + (t0 * H + h) * DK + c;
+  }
+
+  // while the copies run: taps by distance back (tap[0] multiplies the newest input), beta
+  float tap[W][VEC];
+  if (conv_lane) {
+    const T* wt = reinterpret_cast<const T*>(a.weight);
+#pragma unroll
+    for (int d = 0; d < W; ++d)
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) tap[d][e] = d < w ? to_f32(wt[(col + e) * w + (w - 1 - d)]) : 0.f;
+  }
+  for (int t = l; t < L; t += Cfg::NT) {
     const T* bl = reinterpret_cast<const T*>(a.beta_logits);
-    T* bo = reinterpret_cast<T*>(a.beta);
-    bo[(t0 + tid) * H + h] = from_f32<T>(sigm(to_f32(bl[(t0 + tid) * H + h])));
+    reinterpret_cast<T*>(a.beta)[(t0 + t) * H + h] = from_f32<T>(sigm(to_f32(bl[(t0 + t) * H + h])));
   }
 
-  // raw windows: after the sequence (its last tile) and at every checkpoint
-  // boundary b inside this tile (b - 1 in the tile); rows are positions b - w + 1 .. b - 1
-  if (!mine) return;
-  auto put_window = [&](T* dst, int b) {
-    for (int r = 0; r < w - 1; ++r) store2(dst + (int64_t)r * C + col, raw(b - (w - 1) + r));
-  };
-  if (a.window_out != nullptr && pos0 + L == len)
-    put_window(reinterpret_cast<T*>(a.window_out) + (int64_t)n * (w - 1) * C, len);
-  if (a.conv_ckpt != nullptr && a.ckpt_stride > 0) {
-    for (int b = (pos0 / a.ckpt_stride + 1) * a.ckpt_stride; b <= pos0 + L; b += a.ckpt_stride) {
-      const int64_t idx = (int64_t)sched.ckpt_base[n] + b / a.ckpt_stride - 1;
-      if (idx < a.num_ckpt) put_window(reinterpret_cast<T*>(a.conv_ckpt) + idx * (w - 1) * C, b);
+  if (!mbar_wait(bar, 0)) {
+    mbar_wait(bar, 0);     // the copies may still be landing: wait once more before leaving
+    return;
+  }
+  // a sequence's first tile: the halo rows before it are the carried window (or zeros)
+  if (pos0 == 0 && conv_lane) {
+    const T* win = reinterpret_cast<const T*>(a.window_in);
+#pragma unroll
+    for (int d = 1; d < W; ++d) {
+      if (d >= w) continue;
+      float v8[VEC];
+      if (win != nullptr) load8(win + ((int64_t)n * (w - 1) + (w - 1 - d)) * C + col, v8);
+      else {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) v8[e] = 0.f;
+      }
+      store8(const_cast<T*>(tile_s) + (HALO - d) * width, v8);
+    }
+  }
+
+  float wnd[W - 1][VEC];                                   // newest first
+  if (conv_lane) {
+#pragma unroll
+    for (int d = 1; d < W; ++d) load8(tile_s + (HALO - d) * width, wnd[d - 1]);
+  }
+  const int row0 = role == 3 ? 0 : HALO;                   // shared-memory row of tile token 0
+  int next_ck = (a.conv_ckpt != nullptr && a.ckpt_stride > 0) ? (pos0 / a.ckpt_stride + 1) * a.ckpt_stride : INT_MAX;
+#pragma unroll 2
+  for (int t = 0; t < L; ++t) {
+    float y[VEC], xs[VEC];
+    if (role < 4) load8(tile_s + (row0 + t) * width, xs);
+    if (conv_lane) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        float acc = tap[0][e] * xs[e];
+#pragma unroll
+        for (int d = 1; d < W; ++d) acc = fmaf(tap[d][e], wnd[d - 1][e], acc);
+        if (a.act == KDA_ACT_SILU) acc = __fdividef(acc, 1.f + __expf(-acc));
+        y[e] = acc;
+      }
+#pragma unroll
+      for (int d = W - 2; d > 0; --d)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) wnd[d][e] = wnd[d - 1][e];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) wnd[0][e] = xs[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) y[e] = a.g_min * sigm(xs[e]);
+    }
+    // L2Norm of q and k: the row's lanes are NQ consecutive lanes of one warp
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) ss = fmaf(y[e], y[e], ss);
+#pragma unroll
+    for (int off = NQ / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (role < 2) {
+      const float inv = rsqrtf(ss + a.eps);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) y[e] *= inv;
+    }
+    if (role < 4) store8(dst + (int64_t)t * dstride, y);
+
+    // raw windows after position b = pos0 + t + 1 (the end of the sequence, every
+    // conv checkpoint boundary): rows b - w + 1 .. b - 1, oldest first
+    const int b = pos0 + t + 1;
+    const bool at_end = a.window_out != nullptr && b == len;
+    const bool at_ck = b == next_ck;
+    if (at_ck) next_ck += a.ckpt_stride;
+    if (conv_lane && (at_end || at_ck)) {
+      const int64_t idx = at_ck ? (int64_t)sched.ckpt_base[n] + b / a.ckpt_stride - 1 : 0;
+      for (int r = 0; r < w - 1; ++r) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(tile_s + (HALO + t + 1 - (w - 1) + r) * width);
+        if (at_end)
+          *reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.window_out) + ((int64_t)n * (w - 1) + r) * C + col) = raw;
+        if (at_ck && idx < a.num_ckpt)
+          *reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.conv_ckpt) + (idx * (w - 1) + r) * C + col) = raw;
+        if (sizeof(T) == 4) {                              // fp32: the second half of the eight channels
+          const uint4 raw2 = *reinterpret_cast<const uint4*>(tile_s + (HALO + t + 1 - (w - 1) + r) * width + 4);
+          if (at_end)
+            *reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.window_out) + ((int64_t)n * (w - 1) + r) * C + col + 4) = raw2;
+          if (at_ck && idx < a.num_ckpt)
+            *reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.conv_ckpt) + (idx * (w - 1) + r) * C + col + 4) = raw2;
+        }
+      }
     }
   }
 }
 
+template <int DK, int DV, int W, typename T>
+cudaError_t launch_w(const ProArgs& a, const ProSched& sched, const ProMaps& maps, unsigned grid, cudaStream_t s) {
+  using Cfg = ProCfg<DK, DV, W, T>;
+  auto kern = kda_prologue_kernel<DK, DV, W, T>;
+  if (Cfg::SMEM > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<grid, Cfg::NT, Cfg::SMEM, s>>>(a, sched, maps);
+  return cudaGetLastError();
+}
+
 template <int DK, int DV, typename T>
-cudaError_t launch_dims(const ProArgs& a, const ProSched& sched, cudaStream_t s) {
+cudaError_t launch_dims(const ProArgs& a, const ProSched& sched, int64_t T_rows, cudaStream_t s) {
   const int tiles = sched.tile_base[sched.n_seqs];
   if (tiles == 0) return cudaSuccess;
-  kda_prologue_kernel<DK, DV, T><<<dim3((unsigned)tiles, (unsigned)a.H), ProCfg<DK, DV>::NT, 0, s>>>(a, sched);
-  return cudaGetLastError();
+  const unsigned grid = (unsigned)((int64_t)a.H * tiles);
+  const int W = a.w <= 4 ? a.w : MAXW;
+  const int64_t C = (int64_t)a.H * (2 * DK + DV);
+  ProMaps maps;
+  const int es = (int)sizeof(T);
+  if (!make_map_2d(&maps.qk, a.mixed, T_rows, C, es, DK, TT + W - 1, false) ||
+      !make_map_2d(&maps.v, a.mixed, T_rows, C, es, DV, TT + W - 1, false) ||
+      !make_map_2d(&maps.g, a.g_logits, T_rows, (int64_t)a.H * DK, es, DK, TT, false))
+    return cudaErrorInvalidValue;
+  switch (W) {
+    case 2: return launch_w<DK, DV, 2, T>(a, sched, maps, grid, s);
+    case 3: return launch_w<DK, DV, 3, T>(a, sched, maps, grid, s);
+    case 4: return launch_w<DK, DV, 4, T>(a, sched, maps, grid, s);
+    default: return launch_w<DK, DV, MAXW, T>(a, sched, maps, grid, s);
+  }
 }
 
 template <typename T>
 cudaError_t launch_t(const ProArgs& a, const ProSched& sched, cudaStream_t s) {
 #define KDA_CASE(DKv, DVv) \
-  if (a.dk == DKv && a.dv == DVv) return launch_dims<DKv, DVv, T>(a, sched, s);
+  if (a.dk == DKv && a.dv == DVv) return launch_dims<DKv, DVv, T>(a, sched, a.T, s);
   KDA_CASE(32, 32) KDA_CASE(32, 64) KDA_CASE(32, 128)
   KDA_CASE(64, 32) KDA_CASE(64, 64) KDA_CASE(64, 128)
   KDA_CASE(128, 32) KDA_CASE(128, 64) KDA_CASE(128, 128)
@@ -192,6 +287,14 @@ cudaError_t launch_t(const ProArgs& a, const ProSched& sched, cudaStream_t s) {
 }
 
 }  // namespace
+
+int read_and_clear_prologue_errors(int* flags) {
+  int word = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&word, tc::g_kda_device_error, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(tc::g_kda_device_error, &zero, sizeof(int));
+  *flags |= word;
+  return (int)e;
+}
 
 cudaError_t launch_prologue(const ProArgs& a, const ProSched& sched, cudaStream_t s) {
   if (a.w < 2 || a.w > MAXW) return cudaErrorInvalidValue;

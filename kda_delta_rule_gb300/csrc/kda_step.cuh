@@ -83,55 +83,82 @@ constexpr int step_min_blocks() { return MAXS == 1 && NT_CTA < 512 ? 512 / NT_CT
 // Decode with the input prologue fused into the staging: raw mixed_qkv channels of
 // this head pass through the causal ShortConv (window read and shifted in place),
 // the activation, per-head L2Norm of q and k, and the gates from their logits.
+constexpr int kFusedMaxW = 4;   // largest conv kernel size of the fused decode (window in registers)
+
 template <int DK, int DV, int NW, typename T>
 __device__ __forceinline__ void fused_prologue_stage(const StepArgs& a, int64_t b, int hh, int64_t crow,
                                                      bool live, int tid, int lane, int warp, float* st,
                                                      float* kqw, float* red, int64_t head_or_zero) {
+  constexpr int NT = 32 * NW, FW = kFusedMaxW;
+  constexpr int EK = (DK + NT - 1) / NT, EV = (DV + NT - 1) / NT;
   const int64_t head = head_or_zero;       // 0 for a padding head past the batch (reads stay in bounds)
-  constexpr int NT = 32 * NW, MAXW = 8;
   const int w = a.conv_size;
   const int64_t Cw = (int64_t)a.H * (2 * DK + DV);
   const T* X = reinterpret_cast<const T*>(a.mixed);
   const T* Wt = reinterpret_cast<const T*>(a.conv_w);
-  T* win = reinterpret_cast<T*>(a.conv_state);
-  // one channel: y = sum_j weight[c, j] * in[j] over the window and the new input;
-  // the window moves up one row and takes the new input
-  auto conv = [&](int64_t col) -> float {
-    const float x = to_f32(X[b * Cw + col]);
-    T* wr = win + crow * (w - 1) * Cw + col;
-    float wv[MAXW - 1];
-#pragma unroll
-    for (int r = 0; r < MAXW - 1; ++r) wv[r] = r < w - 1 ? to_f32(wr[(int64_t)r * Cw]) : 0.f;
-    float y = to_f32(Wt[col * w + (w - 1)]) * x;
-#pragma unroll
-    for (int r = 0; r < MAXW - 1; ++r)
-      if (r < w - 1) y = fmaf(to_f32(Wt[col * w + r]), wv[r], y);
-    if (live) {
-#pragma unroll
-      for (int r = 0; r < MAXW - 1; ++r)
-        if (r < w - 1) wr[(int64_t)r * Cw] = from_f32<T>(r + 1 < w - 1 ? wv[r + 1] : x);
-    }
-    if (a.act == KDA_ACT_SILU) y *= 1.f / (1.f + expf(-y));
-    return y;
-  };
-  constexpr int EK = (DK + NT - 1) / NT, EV = (DV + NT - 1) / NT;
-  float yq[EK], yk[EK], yv[EV];
-  float ssq = 0.f, ssk = 0.f;
+  T* win = reinterpret_cast<T*>(a.conv_state) + crow * (w - 1) * Cw;
+  const T* gl = reinterpret_cast<const T*>(a.g_logits);
+
+  // ---- every load first: new inputs, windows, taps and logits in one round trip ----
+  // channel slot e: 2u = q of key channel tid + u NT, 2u + 1 = k of it, 2 EK + u = v channel
+  constexpr int NE = 2 * EK + EV;
+  float xin[NE], wv[NE][FW - 1], tap[NE][FW], glg[EK];
+  int64_t cols[NE];
+  bool has[NE];
 #pragma unroll
   for (int u = 0; u < EK; ++u) {
     const int i = tid + u * NT;
-    yq[u] = yk[u] = 0.f;
-    if (i < DK) {
-      yq[u] = conv((int64_t)hh * DK + i);
-      yk[u] = conv((int64_t)a.H * DK + (int64_t)hh * DK + i);
-      ssq = fmaf(yq[u], yq[u], ssq);
-      ssk = fmaf(yk[u], yk[u], ssk);
-    }
+    cols[2 * u] = (int64_t)hh * DK + i;
+    cols[2 * u + 1] = (int64_t)a.H * DK + (int64_t)hh * DK + i;
+    has[2 * u] = has[2 * u + 1] = i < DK;
+    glg[u] = i < DK ? to_f32(gl[head * DK + i]) : 0.f;
   }
 #pragma unroll
   for (int u = 0; u < EV; ++u) {
     const int j = tid + u * NT;
-    yv[u] = j < DV ? conv(2 * (int64_t)a.H * DK + (int64_t)hh * DV + j) : 0.f;
+    cols[2 * EK + u] = 2 * (int64_t)a.H * DK + (int64_t)hh * DV + j;
+    has[2 * EK + u] = j < DV;
+  }
+#pragma unroll
+  for (int e = 0; e < NE; ++e) {
+    xin[e] = has[e] ? to_f32(X[b * Cw + cols[e]]) : 0.f;
+#pragma unroll
+    for (int r = 0; r < FW - 1; ++r) wv[e][r] = has[e] && r < w - 1 ? to_f32(win[(int64_t)r * Cw + cols[e]]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < FW; ++j) tap[e][j] = has[e] && j < w ? to_f32(Wt[cols[e] * w + j]) : 0.f;
+  }
+  const float blg = tid == 0 ? to_f32(reinterpret_cast<const T*>(a.beta_logits)[head]) : 0.f;
+
+  // ---- ShortConv (tap j reads the input w - 1 - j steps back) and activation ----
+  float y[NE];
+#pragma unroll
+  for (int e = 0; e < NE; ++e) {
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < FW; ++j) {
+      if (j < w - 1) acc = fmaf(tap[e][j], wv[e][j], acc);
+      else if (j == w - 1) acc = fmaf(tap[e][j], xin[e], acc);
+    }
+    if (a.act == KDA_ACT_SILU) acc *= 1.f / (1.f + expf(-acc));
+    y[e] = acc;
+  }
+  // ---- the window moves up one row and takes the new input ----
+  if (live) {
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+      if (!has[e]) continue;
+#pragma unroll
+      for (int r = 0; r < FW - 1; ++r)
+        if (r < w - 1) win[(int64_t)r * Cw + cols[e]] = from_f32<T>(r + 1 < w - 1 ? wv[e][r + 1] : xin[e]);
+    }
+  }
+
+  // ---- per-head L2Norm of q and k ----
+  float ssq = 0.f, ssk = 0.f;
+#pragma unroll
+  for (int u = 0; u < EK; ++u) {
+    ssq = fmaf(y[2 * u], y[2 * u], ssq);
+    ssk = fmaf(y[2 * u + 1], y[2 * u + 1], ssk);
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -144,15 +171,16 @@ __device__ __forceinline__ void fused_prologue_stage(const StepArgs& a, int64_t 
 #pragma unroll
   for (int w2 = 0; w2 < NW; ++w2) { ssq += red[w2]; ssk += red[NW + w2]; }
   const float iq = rsqrtf(ssq + a.eps), ik = rsqrtf(ssk + a.eps);
-  const T* gl = reinterpret_cast<const T*>(a.g_logits);
+
+  // ---- stage k, q, e^g, v, beta (and keep the prepared projections if asked) ----
   const bool keep = live && a.q_out != nullptr;
   float kq = 0.f;
 #pragma unroll
   for (int u = 0; u < EK; ++u) {
     const int i = tid + u * NT;
     if (i < DK) {
-      const float qn = yq[u] * iq, kn = yk[u] * ik;
-      const float gi = a.g_min / (1.f + expf(-to_f32(gl[head * DK + i])));
+      const float qn = y[2 * u] * iq, kn = y[2 * u + 1] * ik;
+      const float gi = a.g_min / (1.f + expf(-glg[u]));
       st[i] = kn;
       st[DK + i] = qn;
       st[2 * DK + i] = expf(gi);
@@ -168,12 +196,12 @@ __device__ __forceinline__ void fused_prologue_stage(const StepArgs& a, int64_t 
   for (int u = 0; u < EV; ++u) {
     const int j = tid + u * NT;
     if (j < DV) {
-      st[3 * DK + j] = yv[u];
-      if (keep) reinterpret_cast<T*>(a.v_out)[head * DV + j] = from_f32<T>(yv[u]);
+      st[3 * DK + j] = y[2 * EK + u];
+      if (keep) reinterpret_cast<T*>(a.v_out)[head * DV + j] = from_f32<T>(y[2 * EK + u]);
     }
   }
   if (tid == 0) {
-    const float bt = 1.f / (1.f + expf(-to_f32(reinterpret_cast<const T*>(a.beta_logits)[head])));
+    const float bt = 1.f / (1.f + expf(-blg));
     st[3 * DK + DV] = bt;
     if (keep) reinterpret_cast<T*>(a.beta_out)[head] = from_f32<T>(bt);
   }

@@ -14,6 +14,7 @@
 //    (chunk from the MN offset, row from K).  Descriptor: LBO = K*128, SBO = 1024.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -184,6 +185,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(mbar) : "memory");
+}
+
+// 2-D tiled TMA load (tile mode) into shared memory, completion on mbar; x (the
+// innermost coordinate) times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(mbar) : "memory");
 }
 
 // shared -> global bulk copy tracked by bulk groups (16-byte aligned ends, size a multiple of 16)

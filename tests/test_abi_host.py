@@ -239,7 +239,7 @@ def test_prologue_entries_validation(K):
     assert dec(layout=5) == -1
     assert dec(slots=P(8 << 24), n_slots=0) == -2
     assert dec(conv=P(64)) == -7                                # conv window inside S
-    assert dec(w=9) == -2
+    assert dec(w=5) == -2                                       # fused decode keeps w <= 4
     assert dec(conv=None) == -1
     assert dec(B=0) == 0
 
