@@ -74,7 +74,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, const PrefillSched& sched, int 
 // Input prologue (kda_prologue.cu): ShortConv over mixed_qkv rows [q | k | v],
 // activation, per-head L2Norm of q and k, gates from logits.  One launch covers
 // at most kMaxSeqs sequences; tiles of kPrologueTile tokens never span two sequences.
-constexpr int kPrologueTile = 32;
+constexpr int kPrologueTile = 16;
 struct ProSched {
   int32_t n_seqs;
   int32_t start[kMaxSeqs];       // first token of each sequence (absolute row of mixed)
@@ -96,8 +96,12 @@ struct ProArgs {
   float g_min, eps;
 };
 cudaError_t launch_prologue(const ProArgs& a, const ProSched& sched, cudaStream_t s);
-// Copy the prologue kernel's device error word to *flags (OR) and clear it.
+cudaError_t launch_prologue_f32(const ProArgs& a, const ProSched& sched, cudaStream_t s);
+cudaError_t launch_prologue_bf16(const ProArgs& a, const ProSched& sched, cudaStream_t s);
+// OR the prologue kernels' device error words into *flags and clear them.
 int read_and_clear_prologue_errors(int* flags);
+int read_and_clear_prologue_errors_f32(int* flags);
+int read_and_clear_prologue_errors_bf16(int* flags);
 
 // Tensor-core path (kda_prefill_tc.cu): shapes it takes and workspace bytes per
 // (64-token chunk, head).
