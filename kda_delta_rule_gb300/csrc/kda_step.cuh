@@ -85,75 +85,97 @@ constexpr int step_min_blocks() { return MAXS == 1 && NT_CTA < 512 ? 512 / NT_CT
 // the activation, per-head L2Norm of q and k, and the gates from their logits.
 constexpr int kFusedMaxW = 4;   // largest conv kernel size of the fused decode (window in registers)
 
+// Raw inputs of one head's prologue, per thread: channel slot e = 2u (q of key
+// channel tid + u NT), 2u + 1 (k of it), 2 EK + u (v channel tid + u NT).
+template <int DK, int DV, int NW>
+struct FusedIn {
+  static constexpr int NT = 32 * NW, FW = kFusedMaxW;
+  static constexpr int EK = (DK + NT - 1) / NT, EV = (DV + NT - 1) / NT, NE = 2 * EK + EV;
+  float xin[NE], wv[NE][FW - 1], tap[NE][FW], glg[EK], blg;
+};
+
+template <int DK, int DV, int NW>
+__device__ __forceinline__ int64_t fused_col(const StepArgs& a, int hh, int tid, int e) {
+  using F = FusedIn<DK, DV, NW>;
+  if (e < 2 * F::EK) {
+    const int i = tid + (e >> 1) * F::NT;
+    return (e & 1) ? (int64_t)a.H * DK + (int64_t)hh * DK + i : (int64_t)hh * DK + i;
+  }
+  return 2 * (int64_t)a.H * DK + (int64_t)hh * DV + tid + (e - 2 * F::EK) * F::NT;
+}
+template <int DK, int DV, int NW>
+__device__ __forceinline__ bool fused_has(int tid, int e) {
+  using F = FusedIn<DK, DV, NW>;
+  return e < 2 * F::EK ? tid + (e >> 1) * F::NT < DK : tid + (e - 2 * F::EK) * F::NT < DV;
+}
+
+// Every load of the prologue: new inputs, windows, taps and logits, issued before
+// the state loads so that its arithmetic overlaps them.
 template <int DK, int DV, int NW, typename T>
-__device__ __forceinline__ void fused_prologue_stage(const StepArgs& a, int64_t b, int hh, int64_t crow,
-                                                     bool live, int tid, int lane, int warp, float* st,
-                                                     float* kqw, float* red, int64_t head_or_zero) {
-  constexpr int NT = 32 * NW, FW = kFusedMaxW;
-  constexpr int EK = (DK + NT - 1) / NT, EV = (DV + NT - 1) / NT;
-  const int64_t head = head_or_zero;       // 0 for a padding head past the batch (reads stay in bounds)
+__device__ __forceinline__ void fused_load(const StepArgs& a, int64_t b, int hh, int64_t crow, int tid,
+                                           int64_t head, FusedIn<DK, DV, NW>& f) {
+  using F = FusedIn<DK, DV, NW>;
   const int w = a.conv_size;
   const int64_t Cw = (int64_t)a.H * (2 * DK + DV);
   const T* X = reinterpret_cast<const T*>(a.mixed);
   const T* Wt = reinterpret_cast<const T*>(a.conv_w);
-  T* win = reinterpret_cast<T*>(a.conv_state) + crow * (w - 1) * Cw;
+  const T* win = reinterpret_cast<const T*>(a.conv_state) + crow * (w - 1) * Cw;
   const T* gl = reinterpret_cast<const T*>(a.g_logits);
+#pragma unroll
+  for (int u = 0; u < F::EK; ++u) {
+    const int i = tid + u * F::NT;
+    f.glg[u] = i < DK ? to_f32(gl[head * DK + i]) : 0.f;
+  }
+#pragma unroll
+  for (int e = 0; e < F::NE; ++e) {
+    const bool has = fused_has<DK, DV, NW>(tid, e);
+    const int64_t col = fused_col<DK, DV, NW>(a, hh, tid, e);
+    f.xin[e] = has ? to_f32(X[b * Cw + col]) : 0.f;
+#pragma unroll
+    for (int r = 0; r < F::FW - 1; ++r) f.wv[e][r] = has && r < w - 1 ? to_f32(win[(int64_t)r * Cw + col]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < F::FW; ++j) f.tap[e][j] = has && j < w ? to_f32(Wt[col * w + j]) : 0.f;
+  }
+  f.blg = tid == 0 ? to_f32(reinterpret_cast<const T*>(a.beta_logits)[head]) : 0.f;
+}
 
-  // ---- every load first: new inputs, windows, taps and logits in one round trip ----
-  // channel slot e: 2u = q of key channel tid + u NT, 2u + 1 = k of it, 2 EK + u = v channel
-  constexpr int NE = 2 * EK + EV;
-  float xin[NE], wv[NE][FW - 1], tap[NE][FW], glg[EK];
-  int64_t cols[NE];
-  bool has[NE];
-#pragma unroll
-  for (int u = 0; u < EK; ++u) {
-    const int i = tid + u * NT;
-    cols[2 * u] = (int64_t)hh * DK + i;
-    cols[2 * u + 1] = (int64_t)a.H * DK + (int64_t)hh * DK + i;
-    has[2 * u] = has[2 * u + 1] = i < DK;
-    glg[u] = i < DK ? to_f32(gl[head * DK + i]) : 0.f;
-  }
-#pragma unroll
-  for (int u = 0; u < EV; ++u) {
-    const int j = tid + u * NT;
-    cols[2 * EK + u] = 2 * (int64_t)a.H * DK + (int64_t)hh * DV + j;
-    has[2 * EK + u] = j < DV;
-  }
-#pragma unroll
-  for (int e = 0; e < NE; ++e) {
-    xin[e] = has[e] ? to_f32(X[b * Cw + cols[e]]) : 0.f;
-#pragma unroll
-    for (int r = 0; r < FW - 1; ++r) wv[e][r] = has[e] && r < w - 1 ? to_f32(win[(int64_t)r * Cw + cols[e]]) : 0.f;
-#pragma unroll
-    for (int j = 0; j < FW; ++j) tap[e][j] = has[e] && j < w ? to_f32(Wt[cols[e] * w + j]) : 0.f;
-  }
-  const float blg = tid == 0 ? to_f32(reinterpret_cast<const T*>(a.beta_logits)[head]) : 0.f;
-
-  // ---- ShortConv (tap j reads the input w - 1 - j steps back) and activation ----
+// The prologue's arithmetic: ShortConv (tap j reads the input w - 1 - j steps back),
+// activation, window shift in place, per-head L2Norm of q and k, gates; then the
+// step's staging (k, q, e^g, v, beta) and the k.q partials.
+template <int DK, int DV, int NW, typename T>
+__device__ __forceinline__ void fused_compute(const StepArgs& a, const FusedIn<DK, DV, NW>& f, int hh, int64_t crow,
+                                              bool live, int tid, int lane, int warp, float* st, float* kqw,
+                                              float* red, int64_t head) {
+  using F = FusedIn<DK, DV, NW>;
+  constexpr int EK = F::EK, EV = F::EV, NE = F::NE, FW = F::FW;
+  const int w = a.conv_size;
+  const int64_t Cw = (int64_t)a.H * (2 * DK + DV);
   float y[NE];
 #pragma unroll
   for (int e = 0; e < NE; ++e) {
     float acc = 0.f;
 #pragma unroll
     for (int j = 0; j < FW; ++j) {
-      if (j < w - 1) acc = fmaf(tap[e][j], wv[e][j], acc);
-      else if (j == w - 1) acc = fmaf(tap[e][j], xin[e], acc);
+      if (j < w - 1) acc = fmaf(f.tap[e][j], f.wv[e][j], acc);
+      else if (j == w - 1) acc = fmaf(f.tap[e][j], f.xin[e], acc);
     }
-    if (a.act == KDA_ACT_SILU) acc *= 1.f / (1.f + expf(-acc));
+    if (a.act == KDA_ACT_SILU) acc = __fdividef(acc, 1.f + __expf(-acc));   // about 2 ulp
     y[e] = acc;
   }
-  // ---- the window moves up one row and takes the new input ----
+  // the window moves up one row and takes the new input
   if (live) {
+    T* win = reinterpret_cast<T*>(a.conv_state) + crow * (w - 1) * Cw;
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
-      if (!has[e]) continue;
+      if (!fused_has<DK, DV, NW>(tid, e)) continue;
+      const int64_t col = fused_col<DK, DV, NW>(a, hh, tid, e);
 #pragma unroll
       for (int r = 0; r < FW - 1; ++r)
-        if (r < w - 1) win[(int64_t)r * Cw + cols[e]] = from_f32<T>(r + 1 < w - 1 ? wv[e][r + 1] : xin[e]);
+        if (r < w - 1) win[(int64_t)r * Cw + col] = from_f32<T>(r + 1 < w - 1 ? f.wv[e][r + 1] : f.xin[e]);
     }
   }
 
-  // ---- per-head L2Norm of q and k ----
+  // per-head L2Norm of q and k
   float ssq = 0.f, ssk = 0.f;
 #pragma unroll
   for (int u = 0; u < EK; ++u) {
@@ -172,15 +194,15 @@ __device__ __forceinline__ void fused_prologue_stage(const StepArgs& a, int64_t 
   for (int w2 = 0; w2 < NW; ++w2) { ssq += red[w2]; ssk += red[NW + w2]; }
   const float iq = rsqrtf(ssq + a.eps), ik = rsqrtf(ssk + a.eps);
 
-  // ---- stage k, q, e^g, v, beta (and keep the prepared projections if asked) ----
+  // stage k, q, e^g, v, beta (and keep the prepared projections if asked)
   const bool keep = live && a.q_out != nullptr;
   float kq = 0.f;
 #pragma unroll
   for (int u = 0; u < EK; ++u) {
-    const int i = tid + u * NT;
+    const int i = tid + u * F::NT;
     if (i < DK) {
       const float qn = y[2 * u] * iq, kn = y[2 * u + 1] * ik;
-      const float gi = a.g_min / (1.f + expf(-glg[u]));
+      const float gi = __fdividef(a.g_min, 1.f + __expf(-f.glg[u]));
       st[i] = kn;
       st[DK + i] = qn;
       st[2 * DK + i] = expf(gi);
@@ -194,14 +216,14 @@ __device__ __forceinline__ void fused_prologue_stage(const StepArgs& a, int64_t 
   }
 #pragma unroll
   for (int u = 0; u < EV; ++u) {
-    const int j = tid + u * NT;
+    const int j = tid + u * F::NT;
     if (j < DV) {
       st[3 * DK + j] = y[2 * EK + u];
       if (keep) reinterpret_cast<T*>(a.v_out)[head * DV + j] = from_f32<T>(y[2 * EK + u]);
     }
   }
   if (tid == 0) {
-    const float bt = 1.f / (1.f + expf(-blg));
+    const float bt = __fdividef(1.f, 1.f + __expf(-f.blg));
     st[3 * DK + DV] = bt;
     if (keep) reinterpret_cast<T*>(a.beta_out)[head] = from_f32<T>(bt);
   }
@@ -253,7 +275,14 @@ kda_step_kernel(const StepArgs a) {
   }
   constexpr int ROWLEN = TRANS ? DK : DV;          // floats per stored row
 
-  // ---- issue all state loads first ----
+  // ---- fused prologue: its loads go out first, its arithmetic overlaps the state loads ----
+  // conv window row: the batch row, or its slot (row 0 stands in for a skipped
+  // slot; nothing is written there); head 0 stands in for a padding head
+  FusedIn<DK, DV, NW> fin;
+  const int64_t crow = a.slot_in == nullptr ? (int64_t)b : live_state ? (int64_t)a.slot_in[b] : 0;
+  if constexpr (FUSED) fused_load<DK, DV, NW, T>(a, b, (int)(hl % a.H), crow, tid, active ? head : 0, fin);
+
+  // ---- issue all state loads ----
   float4 S[RPT];
   const float* Sin = a.S_in + srow_in * (int64_t)(DK * DV);
   if (live_state) {
@@ -277,11 +306,8 @@ kda_step_kernel(const StepArgs a) {
   const T* beta = reinterpret_cast<const T*>(a.beta);
   if constexpr (FUSED) {
     static_assert(MAXS == 1, "the fused prologue is a decode path");
-    // conv window row: the batch row, or its slot (row 0 stands in for a skipped
-    // slot; nothing is written there)
-    const int64_t crow = a.slot_in == nullptr ? (int64_t)b : live_state ? (int64_t)a.slot_in[b] : 0;
-    fused_prologue_stage<DK, DV, NW, T>(a, b, (int)(hl % a.H), crow, active && live_state, tid, lane, warp, stage,
-                                        kqw, red, active ? head : 0);
+    fused_compute<DK, DV, NW, T>(a, fin, (int)(hl % a.H), crow, active && live_state, tid, lane, warp, stage, kqw,
+                                 red, active ? head : 0);
   } else {
   // All steps' loads are issued before any is used (MAXS is 1 for decode, the
   // draft bound for replay), so staging costs one memory round trip, not one
