@@ -76,9 +76,12 @@ __host__ __device__ constexpr size_t step_smem_floats(int steps) {
 }
 
 // Decode keeps at least 16 warps resident per SM (128 registers a thread), so that
-// enough state loads are in flight to cover HBM latency.
-template <int NT_CTA, int MAXS>
-constexpr int step_min_blocks() { return MAXS == 1 && NT_CTA < 512 ? 512 / NT_CTA : 1; }
+// enough state loads are in flight to cover HBM latency; replay of 32 x 32 heads
+// (a warp per head, four heads per CTA) keeps four CTAs per SM the same way.
+template <int NT_CTA, int MAXS, int HEAD_ELEMS>
+constexpr int step_min_blocks() {
+  return MAXS == 1 ? (NT_CTA < 512 ? 512 / NT_CTA : 1) : (HEAD_ELEMS <= 1024 && NT_CTA <= 128 ? 4 : 1);
+}
 
 // Decode with the input prologue fused into the staging: raw mixed_qkv channels of
 // this head pass through the causal ShortConv (window read and shifted in place),
@@ -233,7 +236,7 @@ __device__ __forceinline__ void fused_compute(const StepArgs& a, const FusedIn<D
 }
 
 template <int DK, int DV, int NW, int HPC, int MAXS, typename T, bool TRANS, bool FUSED>
-__global__ void __launch_bounds__(32 * NW * HPC, (step_min_blocks<32 * NW * HPC, MAXS>()))
+__global__ void __launch_bounds__(32 * NW * HPC, (step_min_blocks<32 * NW * HPC, MAXS, DK * DV>()))
 kda_step_kernel(const StepArgs a) {
   using C = StepCfg<DK, DV, NW>;
   using CT = StepCfgT<DK, DV, NW>;
@@ -279,8 +282,11 @@ kda_step_kernel(const StepArgs a) {
   // conv window row: the batch row, or its slot (row 0 stands in for a skipped
   // slot; nothing is written there); head 0 stands in for a padding head
   FusedIn<DK, DV, NW> fin;
-  const int64_t crow = a.slot_in == nullptr ? (int64_t)b : live_state ? (int64_t)a.slot_in[b] : 0;
-  if constexpr (FUSED) fused_load<DK, DV, NW, T>(a, b, (int)(hl % a.H), crow, tid, active ? head : 0, fin);
+  int64_t crow = 0;
+  if constexpr (FUSED) {
+    crow = a.slot_in == nullptr ? (int64_t)b : live_state ? (int64_t)a.slot_in[b] : 0;
+    fused_load<DK, DV, NW, T>(a, b, (int)(hl % a.H), crow, tid, active ? head : 0, fin);
+  }
 
   // ---- issue all state loads ----
   float4 S[RPT];
