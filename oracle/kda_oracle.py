@@ -225,6 +225,41 @@ def unrolled_products(S0, q, k, v, g, beta, mode=DECAY_FIRST):
     return np.stack(outs), S_t
 
 
+def segment_transition(k, g, beta, mode=DECAY_FIRST):
+    """Product of the transition matrices of a run of tokens, later tokens on the left:
+    the state after the run is segment_transition @ S_before + (the run's state from zero)."""
+    k = _f64(k)
+    M = np.eye(k.shape[-1])
+    for t in range(k.shape[0]):
+        M = transition_matrix(k[t], g[t], beta[t], mode) @ M
+    return M
+
+
+def prefill_segment_scan(S0, q, k, v, g, beta, seg_len, mode=DECAY_FIRST):
+    """Sequence-parallel form of one head's prefill (context-parallel prefix scan).
+
+    [CACHE] "预填充为什么能分块并行": every token transition is a diagonal matrix minus a
+    rank-one matrix, so the state after a segment is affine in the state before it,
+    S_end = M S_start + L with M the product of the segment's transitions and L the
+    segment's state from zero.  The serve-module page's KCP passes one (H, dk, dv) state
+    per rank, independent of length.  Segment starts come from the scan
+    X_{j+1} = M_j X_j + L_j, X_0 = S0; each segment's outputs from its own start state.
+    Returns (o (T, dv), S_T).
+    """
+    X = _f64(S0).copy()
+    T = int(np.shape(q)[0])
+    outs = []
+    for a in range(0, T, seg_len):
+        b = min(T, a + seg_len)
+        o_seg, _ = kda_recurrent(X, q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b], mode)
+        M = segment_transition(k[a:b], g[a:b], beta[a:b], mode)
+        _, L = kda_recurrent(np.zeros_like(X), q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b], mode)
+        X = M @ X + L
+        outs.append(o_seg)
+    dv = X.shape[-1]
+    return (np.concatenate(outs) if outs else np.zeros((0, dv))), X
+
+
 # ---------------------------------------------------------------------------
 # Chunked WY / UT form ([CACHE] "预填充为什么能分块并行")
 # ---------------------------------------------------------------------------

@@ -147,3 +147,19 @@ def test_prologue_pins_pass_unmutated():
     pins.test_short_conv_newest_and_oldest_taps()
     pins.test_input_prep_channel_layout_by_hand()
     pins.test_input_prep_split_equals_one_shot(1)
+
+
+SCAN_MUTANTS = {
+    "transition_product_reversed": ("segment_transition", "M = transition_matrix(k[t], g[t], beta[t], mode) @ M",
+                                    "M = M @ transition_matrix(k[t], g[t], beta[t], mode)"),
+    "local_state_from_start": ("prefill_segment_scan", "kda_recurrent(np.zeros_like(X),", "kda_recurrent(X,"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SCAN_MUTANTS))
+def test_scan_mutant_is_caught(name, monkeypatch):
+    fn, old, new = SCAN_MUTANTS[name]
+    monkeypatch.setattr(O, fn, _mutant(getattr(O, fn), old, new))
+    checks = [lambda: pins.test_segment_scan_equals_recurrent(0, 7),
+              pins.test_segment_transition_is_the_homogeneous_recurrence]
+    assert _caught(checks), f"no pin catches mutant {name}"

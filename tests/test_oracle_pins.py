@@ -487,3 +487,24 @@ def test_input_prep_split_equals_one_shot(act):
     # the conv checkpoint at a boundary is the window a pass up to it leaves behind
     assert np.array_equal(O.conv_window_at(p["mixed"], p["window"][0], 6), a[5])
     assert np.array_equal(O.conv_window_at(p["mixed"], p["window"][0], T), whole[5])
+
+
+# --------------------------------------------------------------------------
+# Sequence-parallel (segment scan) form
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("seg_len", [1, 3, 7, 40])
+def test_segment_scan_equals_recurrent(mode, seg_len):
+    """Starts from the affine scan, outputs from each segment's start: the full recurrence."""
+    S0, a = _rand_head(23, 5, 4, seed=seg_len + 10 * mode)
+    o_ref, S_ref = O.kda_recurrent(S0, a["q"], a["k"], a["v"], a["g"], a["beta"], mode)
+    o, S = O.prefill_segment_scan(S0, a["q"], a["k"], a["v"], a["g"], a["beta"], seg_len, mode)
+    assert np.abs(o - o_ref).max() < 1e-12 and np.abs(S - S_ref).max() < 1e-12
+
+
+def test_segment_transition_is_the_homogeneous_recurrence():
+    """M applied to a state equals the recurrence run with v = 0 from that state."""
+    S0, a = _rand_head(9, 4, 6, seed=77)
+    M = O.segment_transition(a["k"], a["g"], a["beta"])
+    _, S_h = O.kda_recurrent(S0, a["q"], a["k"], np.zeros_like(a["v"]), a["g"], a["beta"])
+    assert np.abs(M @ S0 - S_h).max() < 1e-13
