@@ -345,6 +345,37 @@ def bench_prologue(K, dev, warmup=3, runs=10):
     return pre_ms, pre_bytes, dec_ms, dec_bytes
 
 
+def bench_scan(K, dev, warmup=2, runs=5, T_long=65536, H_few=4):
+    """One long sequence with few heads (T=65536, H=4, d=128, bf16, a checkpoint every 512
+    tokens): the serial chain (kda_prefill_chunked) against the sequence-parallel prefill
+    (kda_prefill_scan, pieces chosen from the SM count)."""
+    S0, p, cu = I.prefill_inputs([T_long], H_few, DK, DV, dtype=torch.bfloat16, seed=9, device=dev)
+    n_ck = T_long // STRIDE
+    page_bytes = H_few * DK * DV * 4
+    pool = K.PagePool(page_bytes, n_ck, device=dev)
+    ids = torch.tensor(pool.alloc(n_ck), dtype=torch.int32, device=dev)
+    o = torch.empty(T_long, H_few, DV, dtype=torch.bfloat16, device=dev)
+    S_fin = torch.empty_like(S0)
+    ws = torch.empty(K.kda_prefill_workspace_bytes(cu, T_long, H_few, DK, DV, torch.bfloat16), dtype=torch.uint8,
+                     device=dev)
+    ws_scan = torch.empty(K.kda_prefill_scan_workspace_bytes(T_long, H_few, DK, DV, torch.bfloat16, STRIDE, 0),
+                          dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def serial():
+        K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu, ckpt_stride=STRIDE,
+                              page_pool=pool, ckpt_page_ids=ids, o=o, S_final=S_fin, stream=stream, workspace=ws)
+
+    def scan():
+        K.kda_prefill_scan(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], ckpt_stride=STRIDE, o=o, S_final=S_fin,
+                           page_pool=pool, ckpt_page_ids=ids, segments=0, workspace=ws_scan, stream=stream)
+    ms_serial = _timed(serial, stream, warmup, runs)
+    ms_scan = _timed(scan, stream, warmup, runs)
+    del S0, p, o, S_fin, ws, ws_scan, pool
+    torch.cuda.empty_cache()
+    return T_long, H_few, ms_serial, ms_scan
+
+
 def bench_varlen(K, dev, warmup=1, runs=3):
     """Varlen prefix-cache resume prefill: 64 sequences, lengths log-uniform in [512, 32768]
     rounded to multiples of 64, H=32, dk=dv=128, bf16, S0 ~ N(0, 0.05), a checkpoint page
@@ -592,6 +623,12 @@ def main():
                             "one kda_verify_replay_layers launch",
                 "ms_per_launch": layers_ms, "ms_per_layer": layers_ms / REP_SETS,
                 "bytes_per_launch": layers_bytes, "state_GBps": lgbs, "hbm_frac": lgbs / hbm}
+        sT, sH, s_serial, s_scan = bench_scan(K, dev)
+        extras["scan"] = {
+            "workload": f"one sequence T={sT} H={sH} dk=dv={DK} bf16, ckpt every {STRIDE}: serial chain "
+                        "(kda_prefill_chunked) vs sequence-parallel (kda_prefill_scan, pieces from the SM count)",
+            "ms_serial": s_serial, "ms_scan": s_scan, "speedup": s_serial / s_scan,
+            "tokens_per_s_scan": sT / (s_scan / 1e3)}
         vms, vtok, vseq, vck, vbytes = bench_varlen(K, dev)
         vgbs = vbytes / (vms / 1e3) / 1e9
         extras["varlen"] = {"workload": f"{vseq} sequences, lengths log-uniform in [512, 32768] rounded to 64 "

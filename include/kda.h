@@ -320,6 +320,37 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k,
                         int mode, kda_stream_t stream);
 
 /*
+ * kda_prefill_scan -- kda_prefill_chunked for one long sequence, sequence-parallel
+ * inside the GPU (the context-parallel prefix scan: [CACHE] "预填充为什么能分块并行",
+ * every token transition is a diagonal matrix minus a rank-one matrix, so the
+ * state after a segment is affine in the state before it, S_end = M S_start + L;
+ * [SERVE] §1.7, KCP passes one state per rank whatever the length).  The sequence
+ * is cut into about `segments` pieces of whole checkpoint strides (whole 64-token
+ * chunks without checkpoints); the chunk images are built once; one chain launch
+ * runs the first piece from S0 and, for each middle piece, its state from zero and
+ * its transition (dk/dv pseudo-sequences from identity columns with the beta U
+ * term dropped); an fp32 scan gives every piece's start state; a second chain
+ * launch runs the pieces from their starts with outputs and checkpoints.  Worth
+ * it when H * dv / 64 chains leave most SMs idle (few heads, long sequence);
+ * results match kda_prefill_chunked within the bf16 tolerances, not bitwise.
+ *   Arguments as kda_prefill_chunked for one sequence (no cu_seqlens), plus
+ *   segments   0 = choose: the most pieces whose first chain launch fits one CTA
+ *              per SM; 1 or 2 = the plain chain; at most 256; the count is
+ *              rounded so pieces are whole strides
+ *   workspace  device, 256-byte aligned, >= kda_prefill_scan_workspace_bytes(...)
+ *              for the same T, H, dk, dv, dtype, ckpt_stride, segments
+ * Tensor-core shapes only (bf16, dk = 128, dv in {64, 128}): others KDA_ERR_SHAPE.
+ */
+int kda_prefill_scan(const float* S0, const void* q, const void* k, const void* v,
+                     const void* g, const void* beta, int64_t T, int H, int dk, int dv,
+                     int dtype, int chunk, int ckpt_stride, void* o, float* S_final,
+                     void* page_pool, int64_t page_bytes, const int32_t* ckpt_page_ids,
+                     int32_t* ckpt_pos, int64_t num_ckpt, void* workspace,
+                     int64_t workspace_bytes, int segments, int mode, kda_stream_t stream);
+int64_t kda_prefill_scan_workspace_bytes(int64_t T, int H, int dk, int dv, int dtype,
+                                         int ckpt_stride, int segments);
+
+/*
  * kda_prefill_workspace_bytes -- device scratch the tensor-core prefill needs
  * for these sequences (0 when the shape runs on the CUDA-core kernel). The
  * scratch holds, per 64-token chunk and head, the chunk's WY/UT operands in

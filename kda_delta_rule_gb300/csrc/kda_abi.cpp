@@ -334,13 +334,15 @@ int kda_device_errors(int* flags) {
   return ok();
 }
 
-int kda_prefill_chunked(const float* S0, const void* q, const void* k, const void* v,
-                        const void* g, const void* beta, const int32_t* cu_seqlens, int n_seqs,
-                        int64_t T, int H, int dk, int dv, int dtype, int chunk, int ckpt_stride,
-                        void* o, float* S_final, void* page_pool, int64_t page_bytes,
-                        const int32_t* ckpt_page_ids, int32_t* ckpt_pos, int64_t num_ckpt,
-                        void* workspace, int64_t workspace_bytes,
-                        int mode, kda_stream_t stream) {
+// Checks shared by the prefill entry points; *need gets the checkpoint count and
+// *done is set when there is nothing to launch.
+static int check_prefill(const float* S0, const void* q, const void* k, const void* v, const void* g,
+                         const void* beta, const int32_t* cu_seqlens, int n_seqs, int64_t T, int H, int dk,
+                         int dv, int dtype, int chunk, int ckpt_stride, const void* o, const float* S_final,
+                         const void* page_pool, int64_t page_bytes, const int32_t* ckpt_page_ids,
+                         int64_t num_ckpt, int mode, int64_t* need, bool* done) {
+  *need = 0;
+  *done = false;
   if (int st = check_common(dk, dv, dtype, mode)) return st;
   if (chunk != 64) return fail(KDA_ERR_ARG, "chunk=%d: the kernels use 64-token chunks", chunk);
   if (ckpt_stride < 0 || (ckpt_stride % chunk) != 0)
@@ -348,7 +350,10 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
   if (H < 0) return fail(KDA_ERR_SHAPE, "negative H");
   if (int st = check_seqlens(cu_seqlens, n_seqs, T)) return st;
   const int N = cu_seqlens ? n_seqs : 1;
-  if (N == 0 || H == 0) return ok();
+  if (N == 0 || H == 0) {
+    *done = true;
+    return KDA_OK;
+  }
   const size_t es = elem_size(dtype);
   const size_t state_bytes = (size_t)N * H * dk * dv * 4;
   if (!S_final) return fail(KDA_ERR_ARG, "S_final is NULL");
@@ -364,17 +369,35 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
       overlap(o, obytes, v, obytes) || overlap(o, obytes, S0, state_bytes) ||
       overlap(o, obytes, S_final, state_bytes))
     return fail(KDA_ERR_ALIAS, "o overlaps an input or the final state");
-  const int64_t need = kda_num_checkpoints(cu_seqlens, n_seqs, T, ckpt_stride);
-  if (need < 0) return (int)need;
-  if (need > 0) {
+  *need = kda_num_checkpoints(cu_seqlens, n_seqs, T, ckpt_stride);
+  if (*need < 0) return (int)*need;
+  if (*need > 0) {
     if (!page_pool || !ckpt_page_ids) return fail(KDA_ERR_ARG, "checkpoints requested but page_pool or ckpt_page_ids is NULL");
-    if (num_ckpt < need)
-      return fail(KDA_ERR_SHAPE, "num_ckpt=%lld < %lld checkpoints this prefill emits", (long long)num_ckpt, (long long)need);
+    if (num_ckpt < *need)
+      return fail(KDA_ERR_SHAPE, "num_ckpt=%lld < %lld checkpoints this prefill emits", (long long)num_ckpt,
+                  (long long)*need);
     if (page_bytes < (int64_t)H * dk * dv * 4 || (page_bytes % 16) != 0)
       return fail(KDA_ERR_SHAPE, "page_bytes=%lld must be a multiple of 16 and >= H*dk*dv*4=%lld",
                   (long long)page_bytes, (long long)H * dk * dv * 4);
     if (!aligned16(page_pool)) return fail(KDA_ERR_ALIGN, "page_pool must be 16-byte aligned");
   }
+  return KDA_OK;
+}
+
+int kda_prefill_chunked(const float* S0, const void* q, const void* k, const void* v,
+                        const void* g, const void* beta, const int32_t* cu_seqlens, int n_seqs,
+                        int64_t T, int H, int dk, int dv, int dtype, int chunk, int ckpt_stride,
+                        void* o, float* S_final, void* page_pool, int64_t page_bytes,
+                        const int32_t* ckpt_page_ids, int32_t* ckpt_pos, int64_t num_ckpt,
+                        void* workspace, int64_t workspace_bytes,
+                        int mode, kda_stream_t stream) {
+  int64_t need = 0;
+  bool done = false;
+  if (int st = check_prefill(S0, q, k, v, g, beta, cu_seqlens, n_seqs, T, H, dk, dv, dtype, chunk, ckpt_stride, o,
+                             S_final, page_pool, page_bytes, ckpt_page_ids, num_ckpt, mode, &need, &done))
+    return st;
+  if (done) return ok();
+  const int N = cu_seqlens ? n_seqs : 1;
   if (workspace) {
     const int64_t ws_need = kda_prefill_workspace_bytes(cu_seqlens, n_seqs, T, H, dk, dv, dtype);
     if (ws_need < 0) return (int)ws_need;
@@ -412,6 +435,8 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
       sched->len[i] = lens[g0 + i];
       sched->ckpt_base[i] = bases[g0 + i];
       sched->chunk_base[i] = cbase;
+      sched->flags[i] = kda::kSeqEmit;
+      sched->pos_base[i] = 0;
       cbase += (lens[g0 + i] + 63) / 64;
       max_len = std::max(max_len, lens[g0 + i]);
     }
@@ -433,6 +458,75 @@ int kda_prefill_chunked(const float* S0, const void* q, const void* k, const voi
     status = cuda_status(kda::launch_prefill(a, *sched, max_len, s), "kda_prefill_chunked launch");
   }
   return status;
+}
+
+// ---------------------------------------------------------------------------
+static int scan_segments(int64_t T, int H, int dk, int dv, int ckpt_stride, int segments) {
+  if (segments > 0) return segments;
+  int dev = 0, n_sm = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) n_sm = v;
+  }
+  cudaGetLastError();                      // no device here: size for the GB300's 152 SMs
+  return kda::prefill_scan_segments(T, H, dk, dv, ckpt_stride, n_sm);
+}
+
+int64_t kda_prefill_scan_workspace_bytes(int64_t T, int H, int dk, int dv, int dtype, int ckpt_stride, int segments) {
+  if (int st = check_common(dk, dv, dtype, KDA_MODE_DECAY_FIRST)) return st;
+  if (T < 0 || T > 0x7fffffffLL || H < 0) return fail(KDA_ERR_SHAPE, "T=%lld or H=%d out of range", (long long)T, H);
+  if (ckpt_stride < 0 || ckpt_stride % 64 != 0) return fail(KDA_ERR_ARG, "ckpt_stride must be a multiple of 64");
+  // (at most 1 + 254 * 3 pseudo-sequences in the first chain launch: within one launch group)
+  if (segments < 0 || segments > 256) return fail(KDA_ERR_ARG, "segments=%d outside [0, 256]", segments);
+  if (!kda::prefill_tc_supported(dk, dv, dtype))
+    return fail(KDA_ERR_SHAPE, "the sequence-parallel prefill runs the tensor-core kernels: bf16, dk=128, dv 64 or 128");
+  ok();
+  const int64_t images = (T + 63) / 64 * H * kda::prefill_tc_image_bytes(dv);
+  const int P = scan_segments(T, H, dk, dv, ckpt_stride, segments);
+  return (images + 255) / 256 * 256 + kda::prefill_scan_scratch_bytes(T, H, dk, dv, ckpt_stride, P);
+}
+
+int kda_prefill_scan(const float* S0, const void* q, const void* k, const void* v, const void* g, const void* beta,
+                     int64_t T, int H, int dk, int dv, int dtype, int chunk, int ckpt_stride, void* o, float* S_final,
+                     void* page_pool, int64_t page_bytes, const int32_t* ckpt_page_ids, int32_t* ckpt_pos,
+                     int64_t num_ckpt, void* workspace, int64_t workspace_bytes, int segments, int mode,
+                     kda_stream_t stream) {
+  int64_t need = 0;
+  bool done = false;
+  if (int st = check_prefill(S0, q, k, v, g, beta, nullptr, 1, T, H, dk, dv, dtype, chunk, ckpt_stride, o, S_final,
+                             page_pool, page_bytes, ckpt_page_ids, num_ckpt, mode, &need, &done))
+    return st;
+  if (done) return ok();
+  const int64_t ws_need = kda_prefill_scan_workspace_bytes(T, H, dk, dv, dtype, ckpt_stride, segments);
+  if (ws_need < 0) return (int)ws_need;
+  if (!workspace || workspace_bytes < ws_need)
+    return fail(KDA_ERR_SHAPE, "workspace_bytes=%lld < %lld needed (kda_prefill_scan_workspace_bytes)",
+                (long long)workspace_bytes, (long long)ws_need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return fail(KDA_ERR_ALIGN, "workspace must be 256-byte aligned");
+  if (T == 0) {
+    if (S0) return cuda_status(cudaMemcpyAsync(S_final, S0, (size_t)H * dk * dv * 4, cudaMemcpyDeviceToDevice,
+                                               reinterpret_cast<cudaStream_t>(stream)), "kda_prefill_scan copy");
+    return cuda_status(cudaMemsetAsync(S_final, 0, (size_t)H * dk * dv * 4, reinterpret_cast<cudaStream_t>(stream)),
+                       "kda_prefill_scan zero");
+  }
+  const int P = scan_segments(T, H, dk, dv, ckpt_stride, segments);
+  const int64_t images = ((T + 63) / 64 * H * kda::prefill_tc_image_bytes(dv) + 255) / 256 * 256;
+  kda::PrefillArgs a{};
+  a.S0 = S0;
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.o = o;
+  a.S_final = S_final;
+  a.page_pool = static_cast<char*>(page_pool);
+  a.page_bytes = page_bytes;
+  a.ckpt_page_ids = ckpt_page_ids;
+  a.ckpt_pos = ckpt_pos;
+  a.num_ckpt = need > 0 ? num_ckpt : 0;
+  a.H = H; a.dk = dk; a.dv = dv; a.dtype = dtype; a.chunk = chunk;
+  a.ckpt_stride = ckpt_stride; a.mode = mode;
+  a.workspace = workspace; a.workspace_bytes = images;
+  a.T = T;
+  return cuda_status(kda::launch_prefill_tc_scan(a, T, P, static_cast<char*>(workspace) + images,
+                                                 reinterpret_cast<cudaStream_t>(stream)),
+                     "kda_prefill_scan launch");
 }
 
 // ---------------------------------------------------------------------------

@@ -51,7 +51,13 @@ struct PrefillSched {
   int32_t len[kMaxSeqs];         // tokens of each sequence
   int32_t ckpt_base[kMaxSeqs];   // index of each sequence's first checkpoint
   int32_t chunk_base[kMaxSeqs + 1];  // index of each sequence's first 64-token chunk; [n_seqs] = total
+  // tensor-core chain only: per (pseudo-)sequence flags and the position of its first
+  // token within the sequence it is a segment of (added to checkpoint positions)
+  uint8_t flags[kMaxSeqs];
+  int32_t pos_base[kMaxSeqs];
 };
+constexpr uint8_t kSeqEmit = 1;      // write outputs and checkpoints
+constexpr uint8_t kSeqNoU = 2;       // drop the beta U term: the homogeneous (transition) recurrence
 
 struct PrefillArgs {
   const float* S0;               // [n,H,dk,dv] (already offset to this launch) or nullptr
@@ -107,6 +113,16 @@ int read_and_clear_prologue_errors_bf16(int* flags);
 // (64-token chunk, head).
 bool prefill_tc_supported(int dk, int dv, int dtype);
 int64_t prefill_tc_image_bytes(int dv);
+// The two tensor-core kernels separately: chunk images of every chunk of `sched`
+// into a.workspace, then the chain over `sched`'s (pseudo-)sequences.
+cudaError_t launch_prefill_tc_prep(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s);
+cudaError_t launch_prefill_tc_chain(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s);
+// Sequence-parallel prefill of one sequence (kda_scan.cu): the sequence cut into
+// about `segments` pieces of whole checkpoint strides (fewer than 3 runs the plain
+// chain); scratch of prefill_scan_scratch_bytes() for the same arguments.
+int prefill_scan_segments(int64_t len, int H, int dk, int dv, int ckpt_stride, int n_sm);
+int64_t prefill_scan_scratch_bytes(int64_t len, int H, int dk, int dv, int ckpt_stride, int segments);
+cudaError_t launch_prefill_tc_scan(const PrefillArgs& a, int64_t len, int segments, void* scratch, cudaStream_t s);
 // Copy the device error word to *flags and clear it (synchronises the device).
 int read_and_clear_device_errors(int* flags);
 // Record a failure message for kda_last_error() and return `status`.

@@ -757,7 +757,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     }
   } else if (warp == 8) {
     // ---- checkpoint writer: each staged checkpoint, 128 rows of 256 bytes --------
-    const int ck_every = a.ckpt_stride > 0 ? a.ckpt_stride / C : 0;
+    const int ck_every = a.ckpt_stride > 0 && (sched.flags[n] & kSeqEmit) ? a.ckpt_stride / C : 0;
     int k = 0;
     if (ck_every > 0) {
       for (int c = ck_every - 1; c < nch; c += ck_every) {
@@ -787,7 +787,8 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     // ---- row warps -------------------------------------------------------------
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
     const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
-    const int ck_every = a.ckpt_stride > 0 ? a.ckpt_stride / C : 0;
+    const bool emit = (sched.flags[n] & kSeqEmit) != 0, use_u = (sched.flags[n] & kSeqNoU) == 0;
+    const int ck_every = a.ckpt_stride > 0 && emit ? a.ckpt_stride / C : 0;
     int ck_left = ck_every;
     int n_ck = 0;                          // checkpoints staged so far
     auto row_step = [&](auto stage_tag, int c) -> bool {
@@ -807,7 +808,8 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
         const uint4* urow = reinterpret_cast<const uint4*>(st + S_U + r * 128);
         uint4 u[4];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) u[cc] = urow[(4 * hh + cc) ^ (r & 7)];   // all loads before any store
+        for (int cc = 0; cc < 4; ++cc)                     // all loads before any store
+          u[cc] = use_u ? urow[(4 * hh + cc) ^ (r & 7)] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u[cc]);
@@ -862,7 +864,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
             float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
             const int64_t used = (int64_t)H * DKT * DV, total = a.page_bytes / 4;
             for (int64_t e = used + tid; e < total; e += CRW) page[e] = 0.f;   // pad past the state
-            if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = pos;
+            if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = sched.pos_base[n] + pos;
           }
         }
       }
@@ -879,7 +881,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       if (lane == 0) mbar_arrive(sready);
       if (qd >= 2) {
         const int r = i - 64;
-        if (r < L) {
+        if (emit && r < L) {
           __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0 + jc;
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(ov + 8 * cc);
@@ -915,27 +917,37 @@ bool make_map(CUtensorMap* m, const void* base, int64_t T, int64_t cols, int box
 }
 
 template <int DV>
-cudaError_t launch_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned char* ws, int total_chunks,
-                      cudaStream_t s) {
-  cudaError_t e;
-  if (total_chunks > 0) {
-    PrepMaps maps;
-    if (!make_map(&maps.k, a.k, a.T, (int64_t)a.H * DKT, 64, true) ||
-        !make_map(&maps.q, a.q, a.T, (int64_t)a.H * DKT, 64, true) ||
-        !make_map(&maps.g, a.g, a.T, (int64_t)a.H * DKT, DKT, false) ||
-        !make_map(&maps.v, a.v, a.T, (int64_t)a.H * DV, 64, true))
-      return cudaErrorInvalidValue;
-    auto prep = a.mode == KDA_MODE_DECAY_FIRST ? kda_chunk_prep_kernel<DV, true> : kda_chunk_prep_kernel<DV, false>;
-    e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
-    if (e != cudaSuccess) return e;
-    prep<<<(unsigned)((int64_t)a.H * total_chunks), PNT, P_SMEM, s>>>(a, sched, ws, maps);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+cudaError_t launch_prep_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned char* ws, int total_chunks,
+                           cudaStream_t s) {
+  if (total_chunks <= 0) return cudaSuccess;
+  PrepMaps maps;
+  if (!make_map(&maps.k, a.k, a.T, (int64_t)a.H * DKT, 64, true) ||
+      !make_map(&maps.q, a.q, a.T, (int64_t)a.H * DKT, 64, true) ||
+      !make_map(&maps.g, a.g, a.T, (int64_t)a.H * DKT, DKT, false) ||
+      !make_map(&maps.v, a.v, a.T, (int64_t)a.H * DV, 64, true))
+    return cudaErrorInvalidValue;
+  auto prep = a.mode == KDA_MODE_DECAY_FIRST ? kda_chunk_prep_kernel<DV, true> : kda_chunk_prep_kernel<DV, false>;
+  cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
+  if (e != cudaSuccess) return e;
+  prep<<<(unsigned)((int64_t)a.H * total_chunks), PNT, P_SMEM, s>>>(a, sched, ws, maps);
+  return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t launch_chain_dv(const PrefillArgs& a, const PrefillSched& sched, const unsigned char* ws, cudaStream_t s) {
   auto chain = kda_chain_kernel<DV>;
-  e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
   chain<<<dim3(DV / DVS, a.H, sched.n_seqs), CNT, C_SMEM, s>>>(a, sched, ws);
   return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t launch_dv(const PrefillArgs& a, const PrefillSched& sched, unsigned char* ws, int total_chunks,
+                      cudaStream_t s) {
+  cudaError_t e = launch_prep_dv<DV>(a, sched, ws, total_chunks, s);
+  if (e != cudaSuccess) return e;
+  return launch_chain_dv<DV>(a, sched, ws, s);
 }
 
 }  // namespace
@@ -954,6 +966,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const PrefillSched& sched, c
   unsigned char* ws = static_cast<unsigned char*>(a.workspace);
   return a.dv == 128 ? launch_dv<128>(a, sched, ws, total_chunks, s)
                      : launch_dv<64>(a, sched, ws, total_chunks, s);
+}
+
+cudaError_t launch_prefill_tc_prep(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s) {
+  unsigned char* ws = static_cast<unsigned char*>(a.workspace);
+  const int total = sched.chunk_base[sched.n_seqs];
+  return a.dv == 128 ? launch_prep_dv<128>(a, sched, ws, total, s) : launch_prep_dv<64>(a, sched, ws, total, s);
+}
+
+cudaError_t launch_prefill_tc_chain(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s) {
+  if (sched.n_seqs == 0 || a.H == 0) return cudaSuccess;
+  const unsigned char* ws = static_cast<const unsigned char*>(a.workspace);
+  return a.dv == 128 ? launch_chain_dv<128>(a, sched, ws, s) : launch_chain_dv<64>(a, sched, ws, s);
 }
 
 int read_and_clear_device_errors(int* flags) {

@@ -48,6 +48,8 @@ def _load():
         "kda_decode_step_slots": ([P, L, P, I, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
         "kda_verify_replay_slots": ([I, P, P, L, P, P, I, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P], I),
         "kda_decode_step_fused": ([P, L, P, I, P, P, P, I, P, P, F, I, P, P, P, P, P, P, I, I, I, I, I, I, P], I),
+        "kda_prefill_scan": ([P, P, P, P, P, P, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, I, I, P], I),
+        "kda_prefill_scan_workspace_bytes": ([L, I, I, I, I, I, I], L),
         "kda_input_prep": ([P, P, I, P, P, P, P, F, I, P, I, L, I, I, I, I, P, P, P, P, P, I, P, L, P], I),
         "kda_num_checkpoints": ([P, I, L, I], L),
         "kda_prefill_chunked": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, I, P], I),
@@ -498,6 +500,56 @@ def kda_prefill_chunked(S0, q, k, v, g, beta, cu_seqlens=None, chunk=64, ckpt_st
                                     _ptr(ckpt_page_ids), _ptr(ckpt_pos), n_ck,
                                     _ptr(workspace), ws_bytes, mode, _stream(stream, dev)),
            "kda_prefill_chunked")
+    return o, S_final
+
+
+def kda_prefill_scan_workspace_bytes(T, H, dk, dv, dtype=torch.bfloat16, ckpt_stride=512, segments=0) -> int:
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    r = _lib.kda_prefill_scan_workspace_bytes(int(T), int(H), int(dk), int(dv), code, int(ckpt_stride),
+                                              int(segments))
+    if r < 0:
+        _check(int(r), "kda_prefill_scan_workspace_bytes")
+    return int(r)
+
+
+def kda_prefill_scan(S0, q, k, v, g, beta, chunk=64, ckpt_stride=512, o=None, S_final=None, page_pool=None,
+                     ckpt_page_ids=None, ckpt_pos=None, segments=0, workspace=None, mode=DECAY_FIRST,
+                     stream=None):
+    """Sequence-parallel prefill of one sequence (q,k,g (T,H,dk); v (T,H,dv); beta (T,H); bf16).
+
+    S0 (1,H,dk,dv) fp32 or None. segments: 0 = chosen from the SM count. workspace: None
+    (allocated) or a CUDA uint8 tensor of kda_prefill_scan_workspace_bytes(...). Returns (o, S_final).
+    """
+    T, Hq, dk = q.shape
+    code, _, dv = _projections(q, k, v, g, beta, (T, Hq))
+    dev = q.device
+    if S0 is not None:
+        _cuda("S0", S0, torch.float32, (1, Hq, dk, dv))
+    if o is None:
+        o = torch.empty((T, Hq, dv), device=dev, dtype=q.dtype)
+    if S_final is None:
+        S_final = torch.empty((1, Hq, dk, dv), device=dev, dtype=torch.float32)
+    _cuda("o", o, q.dtype, (T, Hq, dv))
+    _cuda("S_final", S_final, torch.float32, (1, Hq, dk, dv))
+    stride = ckpt_stride if page_pool is not None else 0       # no pool: no checkpoints
+    n_ck = 0
+    if page_pool is not None and ckpt_page_ids is not None:
+        _cuda("ckpt_page_ids", ckpt_page_ids, torch.int32)
+        n_ck = ckpt_page_ids.numel()
+        if ckpt_pos is not None:
+            _cuda("ckpt_pos", ckpt_pos, torch.int32)
+    need = kda_prefill_scan_workspace_bytes(T, Hq, dk, dv, q.dtype, stride, segments)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _cuda("workspace", workspace, torch.uint8)
+    _check(_lib.kda_prefill_scan(_ptr(S0), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), T, Hq, dk, dv, code,
+                                 chunk, stride, _ptr(o), _ptr(S_final),
+                                 ctypes.c_void_p(page_pool.arena.data_ptr()) if page_pool is not None else None,
+                                 page_pool.page_bytes if page_pool is not None else 0,
+                                 _ptr(ckpt_page_ids) if n_ck else None, _ptr(ckpt_pos) if n_ck else None,
+                                 n_ck, _ptr(workspace), workspace.numel(), int(segments), mode,
+                                 _stream(stream, dev)),
+           "kda_prefill_scan")
     return o, S_final
 
 
