@@ -77,7 +77,7 @@ __host__ __device__ constexpr size_t step_smem_floats(int steps) {
 
 // Decode keeps at least 16 warps resident per SM (128 registers a thread), so that
 // enough state loads are in flight to cover HBM latency; replay of 32 x 32 heads
-// (a warp per head, four heads per CTA) keeps four CTAs per SM the same way.
+// (a warp per head, four heads per CTA) keeps at least four CTAs per SM the same way.
 template <int NT_CTA, int MAXS, int HEAD_ELEMS>
 constexpr int step_min_blocks() {
   return MAXS == 1 ? (NT_CTA < 512 ? 512 / NT_CTA : 1) : (HEAD_ELEMS <= 1024 && NT_CTA <= 128 ? 4 : 1);
@@ -552,6 +552,16 @@ cudaError_t launch_dims(const StepArgs& a, cudaStream_t s) {
       if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, 1, T, TRANS, FUSED>, 2);
     }
     return run(kda_step_kernel<DK, DV, NW, 1, 1, T, TRANS, FUSED>, 1);
+  }
+  // drafts of up to 8 steps (the common case) keep half the staging registers
+  if (a.steps <= 8) {
+    if constexpr (HMAX >= 4) {
+      if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, 8, T, TRANS, false>, 4);
+    }
+    if constexpr (HMAX >= 2) {
+      if (hpc >= 2) return run(kda_step_kernel<DK, DV, NW, 2, 8, T, TRANS, false>, 2);
+    }
+    return run(kda_step_kernel<DK, DV, NW, 1, 8, T, TRANS, false>, 1);
   }
   if constexpr (HMAX >= 4) {
     if (hpc >= 4) return run(kda_step_kernel<DK, DV, NW, 4, KDA_MAX_DRAFT, T, TRANS, false>, 4);
