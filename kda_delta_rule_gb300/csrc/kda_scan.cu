@@ -72,19 +72,22 @@ __global__ void scan_init_kernel(const float* __restrict__ S0, float* __restrict
 }
 
 // X_1 = segment 0's final state; X_{j+1} = M_j X_j + L_j for j = 1 .. P-2.
-// One CTA per (head, 32 state columns): X block and M_j in shared memory, each
-// thread DK / 8 rows of one column.
+// One CTA of 256 threads per (head, 32 state columns); X block [DK][32] and M_j
+// transposed, [k][i], in shared memory; each thread a 4 x 4 block (rows 4 ti ..,
+// columns 4 tc ..): per k one 16-byte read of X's row k and one of M_j's column k
+// feed 16 FMAs.
+constexpr int SCAN_NT = 256;
 template <int DK>
-__global__ void __launch_bounds__(256) scan_kernel(const float* __restrict__ SfA, float* __restrict__ XC, int H,
-                                                   int dv, int P, int nb) {
+__global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float* __restrict__ SfA, float* __restrict__ XC, int H,
+                                                       int dv, int P, int nb) {
+  static_assert(DK / 4 * 8 == SCAN_NT, "one thread per 4 x 4 block of a DK x 32 tile");
   extern __shared__ float4 scan_smem4[];
   float* Xs = reinterpret_cast<float*>(scan_smem4);        // [DK][32]
-  float* Ms = Xs + DK * 32;                                // [DK][DK]
-  constexpr int RPT = DK / 8;
+  float* MT = Xs + DK * 32;                                // [DK (k)][DK (i)]
   const int h = blockIdx.x, c0 = blockIdx.y * 32, tid = threadIdx.x;
-  const int c = tid & 31, i0 = tid >> 5;
+  const int tc = tid & 7, ti = tid >> 3;                   // column group, row group
   const int64_t HS = (int64_t)H * DK * dv;
-  for (int e = tid; e < DK * 32; e += 256) {
+  for (int e = tid; e < DK * 32; e += SCAN_NT) {
     const int i = e >> 5, cc = e & 31;
     const int64_t off = ((int64_t)h * DK + i) * dv + c0 + cc;
     const float x = SfA[off];
@@ -92,29 +95,55 @@ __global__ void __launch_bounds__(256) scan_kernel(const float* __restrict__ SfA
     XC[off] = x;
   }
   __syncthreads();
+  // M_j as float4s along k (row i, columns k .. k + 3), consecutive threads on
+  // consecutive rows so that the transposed stores hit distinct banks; the loads of
+  // M_{j+1} are in flight while step j computes
+  constexpr int NM = DK * DK / 4 / SCAN_NT;
+  float4 mv[NM];
+  auto load_m = [&](int j) {
+    const int64_t ls = 1 + (int64_t)(j - 1) * (1 + nb);
+#pragma unroll
+    for (int u = 0; u < NM; ++u) {
+      const int e = tid + SCAN_NT * u, i = e % DK, k = 4 * (e / DK), b = k / dv;
+      mv[u] = *reinterpret_cast<const float4*>(SfA + (ls + 1 + b) * HS + ((int64_t)h * DK + i) * dv + (k - b * dv));
+    }
+  };
+  if (P >= 3) load_m(1);
   for (int j = 1; j <= P - 2; ++j) {
     const int64_t ls = 1 + (int64_t)(j - 1) * (1 + nb);    // slot of L_j; M_j's column blocks follow
-    for (int e = tid; e < DK * DK; e += 256) {
-      const int i = e / DK, k = e % DK, b = k / dv;
-      Ms[e] = SfA[(ls + 1 + b) * HS + ((int64_t)h * DK + i) * dv + (k - b * dv)];
+#pragma unroll
+    for (int u = 0; u < NM; ++u) {
+      const int e = tid + SCAN_NT * u, i = e % DK, k = 4 * (e / DK);
+      MT[(k + 0) * DK + i] = mv[u].x;
+      MT[(k + 1) * DK + i] = mv[u].y;
+      MT[(k + 2) * DK + i] = mv[u].z;
+      MT[(k + 3) * DK + i] = mv[u].w;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float4 l4 = *reinterpret_cast<const float4*>(SfA + ls * HS + ((int64_t)h * DK + 4 * ti + r) * dv + c0 +
+                                                         4 * tc);
+      acc[r][0] = l4.x; acc[r][1] = l4.y; acc[r][2] = l4.z; acc[r][3] = l4.w;
     }
     __syncthreads();
-    float acc[RPT];
+    if (j + 1 <= P - 2) load_m(j + 1);
+#pragma unroll 8
+    for (int k = 0; k < DK; ++k) {
+      const float4 x4 = *reinterpret_cast<const float4*>(Xs + k * 32 + 4 * tc);
+      const float4 m4 = *reinterpret_cast<const float4*>(MT + k * DK + 4 * ti);
+      const float mr[4] = {m4.x, m4.y, m4.z, m4.w}, xc[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) acc[m] = SfA[ls * HS + ((int64_t)h * DK + i0 + 8 * m) * dv + c0 + c];
-    for (int k = 0; k < DK; k += 4) {
-      const float x0 = Xs[k * 32 + c], x1 = Xs[(k + 1) * 32 + c], x2 = Xs[(k + 2) * 32 + c], x3 = Xs[(k + 3) * 32 + c];
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int m = 0; m < RPT; ++m) {
-        const float4 mr = *reinterpret_cast<const float4*>(Ms + (i0 + 8 * m) * DK + k);
-        acc[m] = fmaf(mr.x, x0, fmaf(mr.y, x1, fmaf(mr.z, x2, fmaf(mr.w, x3, acc[m]))));
-      }
+        for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(mr[r], xc[q], acc[r][q]);
     }
     __syncthreads();
 #pragma unroll
-    for (int m = 0; m < RPT; ++m) {
-      Xs[(i0 + 8 * m) * 32 + c] = acc[m];
-      XC[(int64_t)j * HS + ((int64_t)h * DK + i0 + 8 * m) * dv + c0 + c] = acc[m];
+    for (int r = 0; r < 4; ++r) {
+      const float4 o4 = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      *reinterpret_cast<float4*>(Xs + (4 * ti + r) * 32 + 4 * tc) = o4;
+      *reinterpret_cast<float4*>(XC + (int64_t)j * HS + ((int64_t)h * DK + 4 * ti + r) * dv + c0 + 4 * tc) = o4;
     }
     __syncthreads();
   }
@@ -192,7 +221,7 @@ cudaError_t launch_prefill_tc_scan(const PrefillArgs& a, int64_t len, int segmen
   const int smem = (a.dk * 32 + a.dk * a.dk) * 4;
   if (smem > 48 * 1024 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
-  kern<<<dim3(a.H, a.dv / 32), 256, smem, s>>>(SfA, XC, a.H, a.dv, p.P, p.nb);
+  kern<<<dim3(a.H, a.dv / 32), SCAN_NT, smem, s>>>(SfA, XC, a.H, a.dv, p.P, p.nb);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // ---- second chain launch: segments 1 .. P-1 from their starts ----
