@@ -162,7 +162,10 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant
     dst = reinterpret_cast<T*>(a.g) + (t0 * H + h) * DK + c;
   }
 
-  // while the copies run: taps by distance back (tap[0] multiplies the newest input), beta
+  // while the copies run: taps by distance back (tap[0] multiplies the newest input), beta.
+  // For bf16 outputs with SiLU the taps are halved (exact): the convolution then
+  // yields x / 2, the argument SiLU(x) = x/2 + x/2 tanh(x/2) starts from.
+  constexpr bool HALF_TAPS = SILU && sizeof(T) == 2;
   float tap[W][VEC];
   if (conv_lane) {
     const T* wt = reinterpret_cast<const T*>(a.weight);
@@ -179,12 +182,13 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant
 #pragma unroll
       for (int d = 0; d < W; ++d)
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) tap[d][e] = wv[e * W + (W - 1 - d)];
+        for (int e = 0; e < VEC; ++e) tap[d][e] = (HALF_TAPS ? 0.5f : 1.f) * wv[e * W + (W - 1 - d)];
     } else {
 #pragma unroll
       for (int d = 0; d < W; ++d)
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) tap[d][e] = d < w ? to_f32(wt[(col + e) * w + (w - 1 - d)]) : 0.f;
+        for (int e = 0; e < VEC; ++e)
+          tap[d][e] = d < w ? (HALF_TAPS ? 0.5f : 1.f) * to_f32(wt[(col + e) * w + (w - 1 - d)]) : 0.f;
     }
   }
   for (int t = l; t < L; t += Cfg::NT) {
@@ -222,6 +226,10 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant
   }
   const int row0 = role == 3 ? 0 : HALO;                   // shared-memory row of tile token 0
   int next_ck = (a.conv_ckpt != nullptr && a.ckpt_stride > 0) ? (pos0 / a.ckpt_stride + 1) * a.ckpt_stride : INT_MAX;
+  // A sequence end is always a tile's last token, and so is every checkpoint
+  // boundary when the stride is a multiple of the tile; only other strides need
+  // the boundary test at every token.
+  const bool ck_inside = a.conv_ckpt != nullptr && a.ckpt_stride > 0 && (a.ckpt_stride % TT) != 0;
   T* dptr = dst;
   for (int tb = 0; tb < L; tb += R) {
 #pragma unroll
@@ -236,24 +244,35 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant
           float acc = tap[0][e] * xs[e];
 #pragma unroll
           for (int d = 1; d < W; ++d) acc = fmaf(tap[d][e], ring[((u - d) % R + R) % R][e], acc);
-          y[e] = SILU ? silu_out<T>(acc) : acc;
+          if constexpr (HALF_TAPS) y[e] = fmaf(acc, tanh_hw(acc), acc);   // acc = x / 2
+          else y[e] = SILU ? silu_out<T>(acc) : acc;
         }
 #pragma unroll
         for (int e = 0; e < VEC; ++e) ring[u][e] = xs[e];   // the oldest row leaves, token t enters
       } else {
+        if constexpr (sizeof(T) == 2) {
+          // g_min sigmoid(x) = g_min/2 + g_min/2 tanh(x/2) in one rounding
+          const float hg = 0.5f * a.g_min;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) y[e] = a.g_min * sigm_out<T>(xs[e]);
+          for (int e = 0; e < VEC; ++e) y[e] = fmaf(hg, tanh_hw(0.5f * xs[e]), hg);
+        } else {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) y[e] = a.g_min * sigm_out<T>(xs[e]);
+        }
       }
-      // L2Norm of q and k: the row's lanes are NQ consecutive lanes of one warp
-      float ss = 0.f;
+      // L2Norm of q and k: the row's lanes are NQ consecutive lanes of warp 0 (the
+      // other warps hold only v and gate lanes and skip it)
+      if (l < 32) {
+        float ss = 0.f;
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) ss = fmaf(y[e], y[e], ss);
+        for (int e = 0; e < VEC; ++e) ss = fmaf(y[e], y[e], ss);
 #pragma unroll
-      for (int off = NQ / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      if (role < 2) {
-        const float inv = rsqrtf(ss + a.eps);
+        for (int off = NQ / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if (role < 2) {
+          const float inv = rsqrtf(ss + a.eps);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) y[e] *= inv;
+          for (int e = 0; e < VEC; ++e) y[e] *= inv;
+        }
       }
       if (role < 4) store8(dptr, y);
       dptr += dstride;
@@ -261,6 +280,7 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant
       // raw windows after position b = pos0 + t + 1 (the end of the sequence, every
       // conv checkpoint boundary): rows b - w + 1 .. b - 1, oldest first
       const int b = pos0 + t + 1;
+      if (!ck_inside && t != L - 1) continue;
       const bool at_end = a.window_out != nullptr && b == len;
       const bool at_ck = b == next_ck;
       if (at_ck) next_ck += a.ckpt_stride;
