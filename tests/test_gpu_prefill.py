@@ -213,6 +213,14 @@ def test_tc_strong_decay(K):
     _tc_case(K, [256, 100], 128, seed=4, g_min=-10.0)
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+def test_tc_weak_decay_long_memory(K, mode):
+    """g = -0.01 sigmoid(.): the state keeps nearly all of its past over 2048 tokens (32
+    chunks), so the bf16 operand copies of S feed 32 chained updates; outputs, final state
+    and every checkpoint page must still meet the bf16 tolerances."""
+    _tc_case(K, [2048], 128, mode=mode, seed=9, stride=512, g_min=-0.01)
+
+
 def test_tc_cold_start_and_single_chunk(K):
     _tc_case(K, [64], 128, seed=5, state_std=0.0)
     _tc_case(K, [7], 64, seed=6)
