@@ -163,3 +163,44 @@ def test_scan_mutant_is_caught(name, monkeypatch):
     checks = [lambda: pins.test_segment_scan_equals_recurrent(0, 7),
               pins.test_segment_transition_is_the_homogeneous_recurrence]
     assert _caught(checks), f"no pin catches mutant {name}"
+
+
+BOOKKEEPING_MUTANTS = {
+    "pack_transposes_heads": ("pack_heads", "np.ascontiguousarray(S).reshape(-1)",
+                              "np.ascontiguousarray(np.swapaxes(S, -1, -2)).reshape(-1)"),
+    "unpack_reads_value_major": ("unpack_heads", ".reshape(B, H, dk, dv)", ".reshape(B, H, dv, dk).swapaxes(-1, -2)"),
+    "page_tail_not_zeroed": ("store_kda", "page = np.zeros(page_elems, dtype=flat.dtype)",
+                             "page = np.ones(page_elems, dtype=flat.dtype)"),
+    "checkpoint_includes_start": ("checkpoint_positions", "range(1, int(L) // int(ckpt_stride) + 1)",
+                                  "range(0, int(L) // int(ckpt_stride) + 1)"),
+    "checkpoint_drops_end": ("checkpoint_positions", "range(1, int(L) // int(ckpt_stride) + 1)",
+                             "range(1, int(L) // int(ckpt_stride))"),
+    "chunked_checkpoint_before_chunk": ("prefill_chunked", "ckpts.append((n, pos, S.copy()))",
+                                        "ckpts.append((n, pos - L, S.copy()))"),
+    "replay_count_not_clamped": ("verify_and_replay_batched", "n_b = int(min(max(int(n_accepted[b]), 0), draft))",
+                                 "n_b = int(n_accepted[b])"),
+    "ratio_counts_two_key_vectors": ("snapshot_cost_ratio", "(3 * dk + dv + 1)", "(2 * dk + dv + 1)"),
+    "ratio_drops_beta": ("snapshot_cost_ratio", "(3 * dk + dv + 1)", "(3 * dk + dv)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BOOKKEEPING_MUTANTS))
+def test_bookkeeping_mutant_is_caught(name, monkeypatch):
+    fn, old, new = BOOKKEEPING_MUTANTS[name]
+    monkeypatch.setattr(O, fn, _mutant(getattr(O, fn), old, new))
+    checks = [pins.test_pack_layout_and_roundtrip, pins.test_store_load_zero_padded_page,
+              pins.test_checkpoint_positions_long_prefill, pins.test_last_checkpoint_is_final_state_bitwise,
+              pins.test_batched_replay_zero_pads_and_matches_per_sequence,
+              pins.test_replay_counts_clamp_to_the_draft,
+              pins.test_snapshot_cost_ratio_printed_values, pins.test_snapshot_cost_ratio_properties,
+              pins.test_varlen_is_independent_sequences]
+    assert _caught(checks), f"no pin catches mutant {name}"
+
+
+def test_bookkeeping_pins_pass_unmutated():
+    assert not _caught([pins.test_pack_layout_and_roundtrip, pins.test_store_load_zero_padded_page,
+                        pins.test_checkpoint_positions_long_prefill, pins.test_last_checkpoint_is_final_state_bitwise,
+                        pins.test_batched_replay_zero_pads_and_matches_per_sequence,
+                        pins.test_replay_counts_clamp_to_the_draft,
+                        pins.test_snapshot_cost_ratio_printed_values, pins.test_snapshot_cost_ratio_properties,
+                        pins.test_varlen_is_independent_sequences])

@@ -262,6 +262,23 @@ def test_batched_replay_zero_pads_and_matches_per_sequence():
         np.testing.assert_allclose(S_new[b], Sb, atol=1e-15)
 
 
+def test_replay_counts_clamp_to_the_draft():
+    """An accepted count counts draft tokens, so it lies in [0, draft] ([SERVE] §1.2); counts
+    outside are clamped: a negative count replays nothing (state unchanged, zero rows), a count
+    past the draft replays all of it (the recurrence over the whole draft)."""
+    B, H, dk, dv, draft = 3, 2, 4, 3, 5
+    S, proj, _ = I.replay_inputs(B, H, dk, dv, draft, dtype=torch.float64, seed=9)
+    S = f64(S)
+    P = {n: f64(getattr(proj, n)) for n in ("q", "k", "v", "g", "beta")}
+    S_new, out = O.verify_and_replay_batched(S, P["q"], P["k"], P["v"], P["g"], P["beta"],
+                                             np.array([-2, draft + 3, draft]))
+    assert np.array_equal(S_new[0], S[0]) and np.all(out[0] == 0.0)
+    for b in (1, 2):
+        o, Sb = O.kda_recurrent(S[b], P["q"][:, b], P["k"][:, b], P["v"][:, b], P["g"][:, b], P["beta"][:, b])
+        np.testing.assert_allclose(out[b], np.moveaxis(o, 0, 1), atol=1e-15)
+        np.testing.assert_allclose(S_new[b], Sb, atol=1e-15)
+
+
 def test_draft_window_layout():
     # Tab 4 panel b: (draft=3, B=1, H=2, D=3), step i filled with i.
     lay = _golden()["draft_window_layout"]
