@@ -204,3 +204,37 @@ def test_bookkeeping_pins_pass_unmutated():
                         pins.test_replay_counts_clamp_to_the_draft,
                         pins.test_snapshot_cost_ratio_printed_values, pins.test_snapshot_cost_ratio_properties,
                         pins.test_varlen_is_independent_sequences])
+
+
+FORM_MUTANTS = {
+    "ut_inverse_sign": ("ut_inverse", "T[r] -= A[r, s] * T[s]", "T[r] += A[r, s] * T[s]"),
+    "ut_inverse_transposed": ("ut_inverse", "T[r] -= A[r, s] * T[s]", "T[r] -= A[s, r] * T[s]"),
+    "transition_decay_applied_after": ("transition_matrix", "return (np.eye(k.shape[0]) - kkT) @ D",
+                                       "return D @ (np.eye(k.shape[0]) - kkT)"),
+    "transition_page1_as_decay_first": ("transition_matrix", "return D - kkT", "return (np.eye(k.shape[0]) - kkT) @ D"),
+    "conv_window_one_late": ("conv_window_at", "z[boundary:boundary + wm1]", "z[boundary + 1:boundary + 1 + wm1]"),
+    "recurrent_checkpoint_one_early": ("prefill_recurrent", "(t + 1 - a) % ckpt_stride == 0", "(t - a) % ckpt_stride == 0"),
+}
+
+
+def _form_pins():
+    yield lambda: pins.test_ut_inverse_is_the_inverse()
+    for mode in (O.DECAY_FIRST, O.UNDECAYED_DELTA):
+        for a in [(2, 4, 3, 1), (3, 5, 5, 2)]:
+            yield lambda m=mode, a=a: pins.test_recurrent_equals_unrolled_products(m, *a)
+        yield lambda m=mode: pins.test_chunked_equals_recurrent(m, 200, 64)
+    yield pins.test_checkpoint_positions_long_prefill
+    yield pins.test_last_checkpoint_is_final_state_bitwise
+    yield lambda: pins.test_input_prep_split_equals_one_shot(1)
+    yield pins.test_input_prep_channel_layout_by_hand
+
+
+@pytest.mark.parametrize("name", sorted(FORM_MUTANTS))
+def test_form_mutant_is_caught(name, monkeypatch):
+    fn, old, new = FORM_MUTANTS[name]
+    monkeypatch.setattr(O, fn, _mutant(getattr(O, fn), old, new))
+    assert _caught(_form_pins()), f"no pin catches mutant {name}"
+
+
+def test_form_pins_pass_unmutated():
+    assert not _caught(_form_pins())
