@@ -318,3 +318,49 @@ def test_pack_validation(K):
     assert f(P(0), 4096, 1024, P(1 << 20), 100, 2, 2, 32, 32, None) == -2   # flat too small
     assert f(P(0), 4098, 1024, P(1 << 20), 8192, 2, 2, 32, 32, None) == -4  # stride % 4
     assert f(P(8), 4096, 1024, P(1 << 20), 8192, 2, 2, 32, 32, None) == -4  # misaligned
+
+
+def test_prefill_scan_validation(K):
+    # every call below carries one defect, so it is refused before any launch
+    lib = K._lib
+    T, H, d = 4096, 2, 128
+    need = lib.kda_prefill_scan_workspace_bytes(T, H, d, d, 1, 512, 4)
+    cu = (ctypes.c_int32 * 2)(0, T)
+    assert need > lib.kda_prefill_workspace_bytes(cu, 1, T, H, d, d, 1) > 0   # images, then the piece states
+    assert lib.kda_prefill_scan_workspace_bytes(T, H, d, d, 1, 96, 4) == -1     # stride not a multiple of 64
+    assert lib.kda_prefill_scan_workspace_bytes(T, H, d, d, 1, 512, 257) == -1  # more than 256 pieces
+    assert lib.kda_prefill_scan_workspace_bytes(T, H, d, d, 1, 512, -1) == -1
+    assert lib.kda_prefill_scan_workspace_bytes(T, H, 32, 32, 1, 512, 4) == -2  # no tensor-core kernels there
+    assert lib.kda_prefill_scan_workspace_bytes(T, H, d, d, 0, 512, 4) == -2    # fp32: the CUDA-core path only
+    f = lib.kda_prefill_scan
+
+    def call(**kw):
+        a = dict(S0=P(0), q=P(1 << 24), k=P(2 << 24), v=P(3 << 24), g=P(4 << 24), beta=P(5 << 24), T=T, H=H,
+                 dk=d, dv=d, dtype=1, chunk=64, stride=512, o=P(6 << 24), Sf=P(7 << 24), pool=P(8 << 24),
+                 page_bytes=H * d * d * 4, ids=P(9 << 24), pos=None, nck=8, ws=P(10 << 24), ws_bytes=need,
+                 segments=4, mode=0)
+        a.update(kw)
+        return f(a["S0"], a["q"], a["k"], a["v"], a["g"], a["beta"], a["T"], a["H"], a["dk"], a["dv"],
+                 a["dtype"], a["chunk"], a["stride"], a["o"], a["Sf"], a["pool"], a["page_bytes"], a["ids"],
+                 a["pos"], a["nck"], a["ws"], a["ws_bytes"], a["segments"], a["mode"], None)
+
+    assert call(ws_bytes=need - 256) == -2                     # workspace too small
+    assert call(ws=None) == -2
+    assert call(ws=ctypes.c_void_p(A + (10 << 24) + 16)) == -4  # not 256-byte aligned
+    assert call(chunk=32) == -1
+    assert call(nck=7) == -2                                   # 8 checkpoints at 512 .. 4096
+    assert call(ids=None) == -1
+    assert call(Sf=P(64)) == -7                                # S_final overlaps S0
+    assert call(segments=300) == -1
+
+
+def test_noalloc_refuses_calls_past_its_scratch_before_any_device_call(K):
+    lib = K._lib
+    T, H, d = 2048, 32, 128                                    # 32 chunks x 32 heads of chunk images
+    cu = (ctypes.c_int32 * 2)(0, T)
+    assert lib.kda_prefill_workspace_bytes(cu, 1, T, H, d, d, 1) > (64 << 20)
+    st = lib.kda_prefill_chunked_noalloc(P(0), P(1 << 26), P(2 << 26), P(3 << 26), P(4 << 26), P(5 << 26), cu, 1,
+                                         T, H, d, d, 1, 64, 512, P(6 << 26), P(7 << 26), P(8 << 26),
+                                         H * d * d * 4, P(9 << 26), None, 4, 0, None)
+    assert st == -2
+    assert b"scratch" in lib.kda_last_error()
