@@ -369,6 +369,20 @@ int64_t kda_prefill_workspace_bytes(const int32_t* cu_seqlens, int n_seqs, int64
 int kda_device_errors(int* flags);
 
 /*
+ * kda_set_prefill_chain_columns -- a tuning knob of the tensor-core prefill
+ * (kda_prefill_chunked, kda_prefill_scan and the variants built on them):
+ * how many columns of each head's state one CTA of the sequential chunk
+ * chain owns ([CACHE] "预填充为什么能分块并行": the chunks of a sequence
+ * are walked in order; the dv columns of the state evolve independently).
+ *   cols  32 or 64; 0 (the default) chooses per call: 32 while twice the
+ *         number of 64-column CTAs still fits the device's SMs, else 64.
+ * Results agree to rounding either way. Process-wide; applies to calls
+ * issued after it returns. Errors: KDA_ERR_ARG for any other value (the
+ * setting is left as it was).
+ */
+int kda_set_prefill_chain_columns(int cols);
+
+/*
  * kda_prefill_chunked_noalloc -- kda_prefill_chunked without a caller
  * workspace. It allocates no device memory, for callers that cannot call
  * cudaMalloc/cudaFree at call time: serving loops that forbid them because

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -65,6 +66,13 @@ int check_common(int dk, int dv, int dtype, int mode) {
 }
 
 }  // namespace
+
+namespace kda {
+namespace {
+std::atomic<int> g_chain_columns{0};
+}  // namespace
+int prefill_chain_columns() { return g_chain_columns.load(std::memory_order_relaxed); }
+}  // namespace kda
 
 extern "C" {
 
@@ -331,6 +339,12 @@ int kda_device_errors(int* flags) {
   int e = kda::read_and_clear_device_errors(flags);
   if (e == 0) e = kda::read_and_clear_prologue_errors(flags);
   if (e != 0) return cuda_status((cudaError_t)e, "kda_device_errors");
+  return ok();
+}
+
+int kda_set_prefill_chain_columns(int cols) {
+  if (cols != 0 && cols != 32 && cols != 64) return fail(KDA_ERR_ARG, "cols must be 0, 32 or 64");
+  kda::g_chain_columns.store(cols, std::memory_order_relaxed);
   return ok();
 }
 

@@ -117,6 +117,9 @@ int64_t prefill_tc_image_bytes(int dv);
 // into a.workspace, then the chain over `sched`'s (pseudo-)sequences.
 cudaError_t launch_prefill_tc_prep(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s);
 cudaError_t launch_prefill_tc_chain(const PrefillArgs& a, const PrefillSched& sched, cudaStream_t s);
+// State columns per chain CTA chosen by kda_set_prefill_chain_columns(): 0 (by
+// grid size), 32 or 64.
+int prefill_chain_columns();
 // Sequence-parallel prefill of one sequence (kda_scan.cu): the sequence cut into
 // about `segments` pieces of whole checkpoint strides (fewer than 3 runs the plain
 // chain); scratch of prefill_scan_scratch_bytes() for the same arguments.

@@ -566,33 +566,41 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 }
 
 // ---- chain kernel -------------------------------------------------------------
-// One CTA per (sequence, head, 64-column slice of dv), ten warps.  Warp 9
+// One CTA per (sequence, head, slice of DVS = 32 or 64 columns of dv), ten
+// warps: 32-column slices when 64-column ones would leave more than half of
+// the SMs idle (the chain is latency-bound, and an N = 32 product reads 5 KB
+// of operands instead of 6 KB while the per-row register work halves).  Warp 9
 // issues every tensor-core product and every image copy (it shares a
 // scheduler with warps 1 and 5, which wait on the products it issues); warp 8
 // writes checkpoint pages from a staging buffer the row warps fill, so no
 // global store precedes a hand-off on the critical path; warps 0-7 do the
 // per-row work, warps w and w + 4 sharing TMEM lane quadrant w % 4 and taking
-// the left and right 32 columns of its rows.  Hand-offs go through mbarriers
+// the left and right DVS / 2 columns of its rows.  Hand-offs go through mbarriers
 // only:  bar1 / bar3 / bar2 (product commits), dready (Delta' written by warps
 // 0, 1, 4, 5) and sready (chunk done by warps 0-7: state written, TMEM and
 // stage reads finished, the output rows of the chunk in registers).
-constexpr int DVS = 64;                            // state columns per CTA
 constexpr int CNT = 320;                           // chain threads: 8 row warps, 1 idle, 1 issuing
 constexpr int ISSUER = 9;                          // the issuing warp
 constexpr int CRW = 256;                           // row threads
 constexpr uint32_t S_WQ = 0, S_KB = 32768, S_PB = 49152, S_U = 65536, S_EG = 73728;
 constexpr uint32_t STAGE = 75776;                 // 74 KB, keeps every stage 1024-aligned
-constexpr uint32_t C_DELTA = 2 * STAGE;           // 8 KB  Delta' MN-major (mn = 64 cols, K = 64 tokens)
-constexpr uint32_t C_SB = C_DELTA + 8192;         // 16 KB S bf16 MN-major (mn = 64 cols, K = 128)
+constexpr uint32_t C_DELTA = 2 * STAGE;           // 8 KB  Delta' MN-major (mn = DVS cols, K = 64 tokens)
+constexpr uint32_t C_SB = C_DELTA + 8192;         // 16 KB S bf16 MN-major (mn = DVS cols, K = 128)
 constexpr uint32_t C_MISC = C_SB + 16384;
-constexpr uint32_t C_CK = C_MISC + 128;           // 34 KB checkpoint staging: fp32 [128 rows][64], rows 272 B apart
+constexpr uint32_t C_CK = C_MISC + 128;           // 34 KB checkpoint staging: fp32 [128 rows][DVS], rows 272 B apart
 constexpr uint32_t CK_ROW = 272;
 constexpr uint32_t C_SMEM = C_CK + 128 * CK_ROW + 1024;
 constexpr uint32_t CHUNK_TX = 32768 + 16384 + 8192 + 8192 + 512;
 
-template <int DV>
+// TMEM -> registers, 16 or 32 consecutive columns of this warp's 32 lanes
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
+
+template <int DV, int DVS>
 __global__ void __launch_bounds__(CNT, 1)
 kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned char* __restrict__ ws) {
+  static_assert(DVS == 32 || DVS == 64, "a chain CTA owns 32 or 64 state columns");
+  constexpr int NC = DVS / 2;                          // state columns per row thread
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t full0 = smem_u32(sm + C_MISC);         // two image stages
@@ -616,7 +624,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   const int64_t ib = img_bytes(DV);
   const unsigned char* img0 = ws + ((int64_t)sched.chunk_base[n] * H + h) * ib;
   const int col0 = sl * DVS;
-  const int jc = 32 * hh;                              // this thread's first column inside the slice
+  const int jc = NC * hh;                              // this thread's first column inside the slice
 
   if (tid == 0) {
     mbar_init(full0, 1);
@@ -637,18 +645,18 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     const int s = e >> 9, o = e & 511;
     reinterpret_cast<uint4*>(sm + s * STAGE + S_PB)[o] = make_uint4(0, 0, 0, 0);
   }
-  // row warps: state row i, columns col0 + jc .. col0 + jc + 31
+  // row warps: state row i, columns col0 + jc .. col0 + jc + NC - 1
   const int i = 32 * qd + lane;
-  float S[32];
+  float S[NC];
   if (warp < 8) {
     const int64_t srow = (((int64_t)n * H + h) * DKT + i) * DV + col0 + jc;
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
+    for (int j = 0; j < NC; j += 4) {
       float4 x = a.S0 ? *reinterpret_cast<const float4*>(a.S0 + srow + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
     }
 #pragma unroll
-    for (int cch = 0; cch < 4; ++cch)
+    for (int cch = 0; cch < NC / 8; ++cch)
       *reinterpret_cast<uint4*>(sm + C_SB + off_mn(jc + 8 * cch, i, 128)) = pack8(S + 8 * cch);
   }
   fence_async_smem();
@@ -673,7 +681,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       bulk_g2s(dst + S_WQ, src + IMG_WQ, 32768, fb);
       bulk_g2s(dst + S_KB, src + IMG_KB, 16384, fb);
       bulk_g2s(dst + S_PB + 8192, src + IMG_P, 8192, fb);
-      bulk_g2s(dst + S_U, src + IMG_U + sl * 8192, 8192, fb);
+      bulk_g2s(dst + S_U, src + IMG_U + (col0 >> 6) * 8192, 8192, fb);   // the 64-column block of the slice
       bulk_g2s(dst + S_EG, src + img_eg(DV), 512, fb);
     };
     // operand descriptors, computed once: k-step j only moves the start address
@@ -803,15 +811,16 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
         if (!__all_sync(0xffffffffu, mbar_wait(bar1, ph))) return false;
         fence_after();
         const int r = i;
-        float v[32];
-        tmem_ld32(d1 + lane_off + jc, v);
+        float v[NC];
+        tmem_ld_cols(d1 + lane_off + jc, v);
         const uint4* urow = reinterpret_cast<const uint4*>(st + S_U + r * 128);
-        uint4 u[4];
+        const int cb0 = ((col0 & 63) + jc) >> 3;           // first 16-byte chunk of this thread's columns
+        uint4 u[NC / 8];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)                     // all loads before any store
-          u[cc] = use_u ? urow[(4 * hh + cc) ^ (r & 7)] : make_uint4(0u, 0u, 0u, 0u);
+        for (int cc = 0; cc < NC / 8; ++cc)                // all loads before any store
+          u[cc] = use_u ? urow[(cb0 + cc) ^ (r & 7)] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < NC / 8; ++cc) {
           const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u[cc]);
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
@@ -821,7 +830,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
           }
         }
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
+        for (int cc = 0; cc < NC / 8; ++cc)
           *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(jc + 8 * cc, r, 64)) = pack8(v + 8 * cc);
         fence_async_smem();
         fence_before();
@@ -834,12 +843,12 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
       {
         const float eg = reinterpret_cast<const float*>(st + S_EG)[i];
-        float v[32];
-        tmem_ld32(d2 + lane_off + jc, v);
+        float v[NC];
+        tmem_ld_cols(d2 + lane_off + jc, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[j] = fmaf(eg, S[j], v[j]);
+        for (int j = 0; j < NC; ++j) S[j] = fmaf(eg, S[j], v[j]);
 #pragma unroll
-        for (int cch = 0; cch < 4; ++cch)
+        for (int cch = 0; cch < NC / 8; ++cch)
           *reinterpret_cast<uint4*>(sm + C_SB + off_mn(jc + 8 * cch, i, 128)) = pack8(S + 8 * cch);
       }
       const int L = min(C, len - c * C);
@@ -855,7 +864,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
           if (n_ck > 0 && !__all_sync(0xffffffffu, mbar_wait(ckfree, (uint32_t)((n_ck - 1) & 1)))) return false;
           float4* srow = reinterpret_cast<float4*>(sm + C_CK + i * CK_ROW + jc * 4);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) srow[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+          for (int j = 0; j < NC / 4; ++j) srow[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
           fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(ckfull);
@@ -868,12 +877,12 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
           }
         }
       }
-      float ov[32];
+      float ov[NC];
       if (qd >= 2) {                        // outputs of chunk c: rows 64-127 of d1[c&1]
         if (*s_abort) return false;
         if (!__all_sync(0xffffffffu, mbar_wait(bar2, ph))) return false;
         fence_after();
-        tmem_ld32(d1 + lane_off + jc, ov);
+        tmem_ld_cols(d1 + lane_off + jc, ov);
       }
       fence_async_smem();
       fence_before();
@@ -884,7 +893,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
         if (emit && r < L) {
           __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0 + jc;
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(ov + 8 * cc);
+          for (int cc = 0; cc < NC / 8; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(ov + 8 * cc);
         }
       }
       return true;
@@ -906,7 +915,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   if (warp < 8 && *s_abort == 0) {
     float* dst = a.S_final + (((int64_t)n * H + h) * DKT + i) * DV + col0 + jc;
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    for (int j = 0; j < NC; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
   }
   if (warp == ISSUER) tmem_dealloc(tmem, 256);
 }
@@ -933,13 +942,28 @@ cudaError_t launch_prep_dv(const PrefillArgs& a, const PrefillSched& sched, unsi
   return cudaGetLastError();
 }
 
-template <int DV>
-cudaError_t launch_chain_dv(const PrefillArgs& a, const PrefillSched& sched, const unsigned char* ws, cudaStream_t s) {
-  auto chain = kda_chain_kernel<DV>;
+template <int DV, int DVS>
+cudaError_t launch_chain_cols(const PrefillArgs& a, const PrefillSched& sched, const unsigned char* ws,
+                              cudaStream_t s) {
+  auto chain = kda_chain_kernel<DV, DVS>;
   cudaError_t e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
   chain<<<dim3(DV / DVS, a.H, sched.n_seqs), CNT, C_SMEM, s>>>(a, sched, ws);
   return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t launch_chain_dv(const PrefillArgs& a, const PrefillSched& sched, const unsigned char* ws, cudaStream_t s) {
+  int cols = prefill_chain_columns();
+  if (cols == 0) {
+    // one CTA per SM at most: 32-column slices while twice the 64-column grid still fits
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cols = 2 * (int64_t)(DV / 64) * a.H * sched.n_seqs <= sms ? 32 : 64;
+  }
+  return cols == 32 ? launch_chain_cols<DV, 32>(a, sched, ws, s) : launch_chain_cols<DV, 64>(a, sched, ws, s);
 }
 
 template <int DV>

@@ -59,6 +59,7 @@ def _load():
         "kda_prefill_chunked_host": ([P, P, P, P, P, P, P, I, L, I, I, I, I, I, I, P, P, P, L, P, P, L, P, L, L, I, P],
                                      I),
         "kda_device_errors": ([ctypes.POINTER(ctypes.c_int)], I),
+        "kda_set_prefill_chain_columns": ([I], I),
         "kda_pack_heads": ([P, L, L, P, L, I, I, I, I, P], I),
         "kda_unpack_heads": ([P, P, L, L, I, I, I, I, P], I),
         "kda_pool_create": ([P, L, L, ctypes.POINTER(P)], I),
@@ -363,6 +364,11 @@ def kda_device_errors() -> int:
     flags = ctypes.c_int(0)
     _check(_lib.kda_device_errors(ctypes.byref(flags)), "kda_device_errors")
     return int(flags.value)
+
+
+def kda_set_prefill_chain_columns(cols: int) -> None:
+    """State columns per chain CTA of the tensor-core prefill: 32, 64, or 0 (chosen per call)."""
+    _check(_lib.kda_set_prefill_chain_columns(int(cols)), "kda_set_prefill_chain_columns")
 
 
 def kda_input_prep(mixed, conv_weight, g_logits, beta_logits, cu_seqlens=None, window_in=None,

@@ -49,6 +49,17 @@ def test_status_strings(K):
     assert K._lib.kda_version() >= 1
 
 
+def test_chain_columns_knob(K):
+    f = K._lib.kda_set_prefill_chain_columns
+    for bad in (-1, 1, 16, 48, 128):
+        assert f(bad) == -1
+    for good in (32, 64, 0):
+        assert f(good) == 0
+    with pytest.raises(K.KdaError):
+        K.kda_set_prefill_chain_columns(96)
+    K.kda_set_prefill_chain_columns(0)
+
+
 def test_snapshot_cost_ratio_matches_pages(K):
     assert round(K.kda_snapshot_cost_ratio(2, 8, 8), 2) == 1.94
     assert round(K.kda_snapshot_cost_ratio(1, 16, 16), 2) == 3.94

@@ -115,8 +115,17 @@ def test_resume_from_checkpoint_page(K):
     assert rel(o_tail, o_all[512:]) < TOL_F32
 
 
-def test_long_prefill_sampled_heads(K):
-    """B=1, H=32, dk=dv=128, T=8192, bf16, 16 checkpoints; heads 0, 13, 31 checked."""
+@pytest.fixture
+def chain_cols(K):
+    yield K.kda_set_prefill_chain_columns
+    K.kda_set_prefill_chain_columns(0)
+
+
+@pytest.mark.parametrize("cols", [0, 64])
+def test_long_prefill_sampled_heads(K, cols, chain_cols):
+    """B=1, H=32, dk=dv=128, T=8192, bf16, 16 checkpoints; heads 0, 13, 31 checked (chain CTA
+    width chosen per call, which takes 32-column slices here, and forced to 64)."""
+    chain_cols(cols)
     H, d, T, stride = 32, 128, 8192, 512
     S0, p, cu = I.prefill_inputs([T], H, d, d, dtype=torch.bfloat16, seed=0, device="cuda")
     n_ck = K.kda_num_checkpoints(cu, T, stride)
@@ -219,6 +228,30 @@ def test_tc_weak_decay_long_memory(K, mode):
     chunks), so the bf16 operand copies of S feed 32 chained updates; outputs, final state
     and every checkpoint page must still meet the bf16 tolerances."""
     _tc_case(K, [2048], 128, mode=mode, seed=9, stride=512, g_min=-0.01)
+
+
+@pytest.mark.parametrize("cols", [32, 64])
+@pytest.mark.parametrize("dv", [64, 128])
+def test_tc_chain_column_slices(K, dv, cols, chain_cols):
+    """Both chain CTA widths, forced, on ragged sequences in both modes."""
+    chain_cols(cols)
+    _tc_case(K, [1, 63, 65, 130, 0, 200, 128, 320], dv, mode=0, seed=11, pad_bytes=64)
+    _tc_case(K, [300, 64], dv, mode=1, seed=12, stride=64)
+
+
+def test_tc_chain_widths_agree(K, chain_cols):
+    """32- and 64-column chain CTAs compute every state column the same way."""
+    H, d = 4, 128
+    S0, p, cu = I.prefill_inputs([900, 77, 256], H, d, d, dtype=torch.bfloat16, seed=13, device="cuda")
+    res = []
+    for cols in (32, 64):
+        chain_cols(cols)
+        res.append(K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
+                                         ckpt_stride=0))
+    torch.cuda.synchronize()
+    assert K.kda_device_errors() == 0
+    (o32, s32), (o64, s64) = res
+    assert rel(o32, o64) < 1e-5 and rel(s32, s64) < 1e-5
 
 
 def test_tc_cold_start_and_single_chunk(K):
