@@ -43,6 +43,7 @@ from kda_delta_rule_gb300 import dist as D           # noqa: E402
 from kda_delta_rule_gb300 import inputs as I         # noqa: E402
 
 H, DK, DV, T, STRIDE, CHUNK = 32, 128, 128, 8192, 512, 64
+PREFILL_KERNELS_PER_CALL = 2           # chunk prep + chain, the only launches of a timed step
 E2E_SEGMENT = 1024                      # tokens per copy/compute segment of the end-to-end call
 DEC_B, DEC_STEPS = 256, 256
 REP_B, REP_H, REP_D, REP_DRAFT, REP_SETS = 32, 16, 32, 8, 64
@@ -658,7 +659,7 @@ def main():
                          "tc_frac": flops / (kern_avg_ms / 1e3) / 1e12 / tf},
             "e2e": {"value": T * world * args.steps / (e2e_max / 1e3), "unit": "tokens/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": args.steps,
+            "gpu_launches": PREFILL_KERNELS_PER_CALL * args.steps,
             "clocks": r["clocks"],
             "cpu_baseline": cpu,
             **extras,
