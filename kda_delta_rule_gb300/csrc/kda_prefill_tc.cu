@@ -17,7 +17,7 @@
 //    A and P on tcgen05, the UT solve in shared memory, W and U on tcgen05.
 //    It writes, per chunk and head, a pre-swizzled image of every operand the
 //    state recurrence needs (the "chunk image") into the caller's workspace.
-//  * chain, one CTA per (sequence, head, 64-column slice of dv), walking the
+//  * chain, one CTA per (sequence, head, 32- or 64-column slice of dv), walking the
 //    chunks in order: bulk-async (TMA) copies of the chunk images into a
 //    two-stage ring, three tcgen05 contractions per chunk with the fp32 state
 //    in registers, outputs and chunk-aligned checkpoints straight to memory
