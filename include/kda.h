@@ -306,7 +306,9 @@ int64_t kda_num_checkpoints(const int32_t* cu_seqlens, int n_seqs, int64_t T,
  * Kernels: bf16 projections with dk = 128 and dv in {64, 128} run on tcgen05
  * tensor cores (bf16 operands, fp32 accumulation and state) when a workspace
  * is given; every other case, and a NULL workspace, runs the fp32 CUDA-core
- * kernel. The workspace is only touched during the call's kernels (stream
+ * kernel. Both take g in [-10, 0]: a gate outside that range (or NaN) is not
+ * rejected on the host (it is device data) but raises KDA_DEVERR_GATE in
+ * kda_device_errors(), and the call's results are then not to be trusted. The workspace is only touched during the call's kernels (stream
  * order); calls sharing one workspace must be ordered on one stream.
  */
 int kda_prefill_chunked(const float* S0, const void* q, const void* k,
@@ -362,10 +364,19 @@ int64_t kda_prefill_workspace_bytes(const int32_t* cu_seqlens, int n_seqs, int64
 
 /*
  * kda_device_errors -- read and clear the library's device error word.
- * Bit 0: a kernel gave up waiting on an mbarrier (about one second) and
- * returned early, so that call's outputs are invalid. Synchronises the
- * device. *flags receives the word; returns KDA_OK or KDA_ERR_CUDA.
+ * Bit 0 (KDA_DEVERR_WAIT): a kernel gave up waiting on an mbarrier (about
+ * one second) and returned early, so that call's outputs are invalid.
+ * Bit 1 (KDA_DEVERR_GATE): a chunked prefill (kda_prefill_chunked and the
+ * calls built on it) read a gate g outside [-10, 0] or a NaN gate. Its
+ * kernels split each pairwise decay at a reference token per 16-token block,
+ * so a factor can reach e^(8 |g|): finite for g >= -10, not beyond. The
+ * call's outputs may then hold inf or NaN. ([SERVE] §1.3 draws
+ * g = g_min sigmoid(.) in [g_min, 0]; the pages use g_min = -5.)
+ * Synchronises the device. *flags receives the word; returns KDA_OK or
+ * KDA_ERR_CUDA.
  */
+#define KDA_DEVERR_WAIT  1
+#define KDA_DEVERR_GATE  2
 int kda_device_errors(int* flags);
 
 /*
@@ -398,6 +409,10 @@ int kda_set_prefill_chain_columns(int cols);
  * kernel as kda_prefill_chunked does with a NULL workspace.
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
+ * The address is kept per device ordinal for the life of the process: it
+ * assumes the runtime's primary context on each device, with no
+ * cudaDeviceReset in between (after a reset, or under a context the caller
+ * created through the driver API, the kept address would be stale).
  * All calls share the one array: calls whose kernels overlap on the GPU (on
  * different streams, or from different threads) race on it and must be
  * ordered by the caller. Nothing in it needs clearing between calls: every

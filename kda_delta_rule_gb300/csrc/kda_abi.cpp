@@ -338,6 +338,7 @@ int kda_device_errors(int* flags) {
   if (!flags) return fail(KDA_ERR_ARG, "flags is NULL");
   int e = kda::read_and_clear_device_errors(flags);
   if (e == 0) e = kda::read_and_clear_prologue_errors(flags);
+  if (e == 0) e = kda::read_and_clear_simt_errors(flags);
   if (e != 0) return cuda_status((cudaError_t)e, "kda_device_errors");
   return ok();
 }
@@ -780,6 +781,18 @@ double kda_snapshot_cost_ratio(int H, int dk, int dv) {
 }
 
 }  // extern "C"
+
+namespace kda {
+int validate_prefill(const float* S0, const void* q, const void* k, const void* v, const void* g, const void* beta,
+                     const int32_t* cu_seqlens, int n_seqs, int64_t T, int H, int dk, int dv, int dtype, int chunk,
+                     int ckpt_stride, const void* o, const float* S_final, const void* page_pool, int64_t page_bytes,
+                     const int32_t* ckpt_page_ids, int64_t num_ckpt, int mode) {
+  int64_t need = 0;
+  bool done = false;
+  return check_prefill(S0, q, k, v, g, beta, cu_seqlens, n_seqs, T, H, dk, dv, dtype, chunk, ckpt_stride, o, S_final,
+                       page_pool, page_bytes, ckpt_page_ids, num_ckpt, mode, &need, &done);
+}
+}  // namespace kda
 
 namespace kda {
 int set_error(int status, const char* msg) { return fail(status, "%s", msg); }

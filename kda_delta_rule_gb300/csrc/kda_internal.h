@@ -128,8 +128,16 @@ int64_t prefill_scan_scratch_bytes(int64_t len, int H, int dk, int dv, int ckpt_
 cudaError_t launch_prefill_tc_scan(const PrefillArgs& a, int64_t len, int segments, void* scratch, cudaStream_t s);
 // Copy the device error word to *flags and clear it (synchronises the device).
 int read_and_clear_device_errors(int* flags);
+// OR the CUDA-core prefill kernel's error word into *flags and clear it.
+int read_and_clear_simt_errors(int* flags);
 // Record a failure message for kda_last_error() and return `status`.
 int set_error(int status, const char* msg);
+// The host-side argument checks of kda_prefill_chunked (everything but the
+// workspace): KDA_OK or the status (and message) that call would return.
+int validate_prefill(const float* S0, const void* q, const void* k, const void* v, const void* g, const void* beta,
+                     const int32_t* cu_seqlens, int n_seqs, int64_t T, int H, int dk, int dv, int dtype, int chunk,
+                     int ckpt_stride, const void* o, const float* S_final, const void* page_pool, int64_t page_bytes,
+                     const int32_t* ckpt_page_ids, int64_t num_ckpt, int mode);
 
 // Flat <-> strided (B,H,dk,dv) copies.  pack zero-fills flat past B*H*dk*dv.
 cudaError_t launch_pack(const float* S, int64_t stride_b, int64_t stride_h, float* flat,

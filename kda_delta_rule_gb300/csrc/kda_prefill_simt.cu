@@ -27,6 +27,20 @@
 #include "../../include/kda.h"
 
 namespace kda {
+
+// Device error word of this translation unit (same bits as kda_device_errors):
+// bit 1 = a gate outside [-10, 0] (or NaN) was read, beyond the range where the
+// factor split below stays finite.
+static __device__ int g_simt_error = 0;
+
+int read_and_clear_simt_errors(int* flags) {
+  int word = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&word, g_simt_error, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_simt_error, &zero, sizeof(int));
+  *flags |= word;
+  return (int)e;
+}
+
 namespace {
 
 constexpr int C = 64;        // chunk length
@@ -81,6 +95,7 @@ kda_prefill_simt_kernel(const PrefillArgs a, const PrefillSched sched) {
   }
 
   int ck = 0;   // checkpoints emitted so far by this sequence
+  bool gate_bad = false;
   for (int c0 = 0; c0 < len; c0 += C) {
     const int L = min(C, len - c0);
     const int64_t t0 = start + c0;
@@ -92,6 +107,7 @@ kda_prefill_simt_kernel(const PrefillArgs a, const PrefillSched sched) {
       if (r < L) {
         const int64_t off = ((t0 + r) * H + h) * DK + i;
         kv = to_f32(k[off]); qv = to_f32(q[off]); gv = to_f32(g[off]);
+        gate_bad |= !(gv >= -10.f && gv <= 0.f);
       }
       sm.Kr[r * KS + i] = kv; sm.Qr[r * KS + i] = qv; sm.Gm[r * KS + i] = gv;
     }
@@ -243,6 +259,7 @@ kda_prefill_simt_kernel(const PrefillArgs a, const PrefillSched sched) {
     const int i = e / DVS, j = e % DVS;
     a.S_final[sbase + (int64_t)i * DV + j] = sm.S[e];
   }
+  if (gate_bad) atomicOr(&g_simt_error, 2);
 }
 
 template <int DK, typename T>

@@ -34,6 +34,8 @@
 #include "kda_tmap.h"
 #include "../../include/kda.h"
 
+#include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <mutex>
 #include <type_traits>
@@ -187,16 +189,21 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   float2 gl[16];
   {
     float a0 = 0.f, a1 = 0.f, p0 = 0.f, p1 = 0.f;
+    bool bad = false;
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
       const int r = 16 * qb + rr;
       const float2 gv = r < L ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
+      bad |= !(gv.x >= -10.f && gv.x <= 0.f && gv.y >= -10.f && gv.y <= 0.f);
       gl[rr] = make_float2(gv.x * kLog2e, gv.y * kLog2e);
       a0 += gl[rr].x;
       a1 += gl[rr].y;
       if (rr == 7) { p0 = a0; p1 = a1; }
     }
     part[qb * 64 + pch] = make_float4(p0, p1, a0, a1);
+    // the factor bounds below hold for g in [-10, 0]; anything else (or NaN)
+    // raises the gate bit of the error word
+    if (bad) atomicOr(&g_kda_device_error, kDevErrGate);
   }
   __syncthreads();
   float gm[4][2], GC[2] = {0.f, 0.f}, acc0[2] = {0.f, 0.f};
@@ -774,9 +781,13 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
         const int64_t idx = (int64_t)sched.ckpt_base[n] + (c * C + L) / a.ckpt_stride - 1;
         if (idx >= a.num_ckpt) break;
         const int32_t page_id = a.ckpt_page_ids[idx];
-        bool w = false;
-        while (!w && !*s_abort) w = __all_sync(0xffffffffu, mbar_wait(ckfull, (uint32_t)(k & 1)));
-        if (!w) break;
+        // one bounded wait: it ends when the rows are staged, when another warp
+        // aborts, or after about a second (error word raised); either failure
+        // ends this warp's loop and aborts the CTA
+        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(ckfull, (uint32_t)(k & 1), s_abort))) {
+          *s_abort = 1;
+          break;
+        }
         char* page = a.page_pool + (int64_t)page_id * a.page_bytes;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
@@ -920,6 +931,19 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   if (warp == ISSUER) tmem_dealloc(tmem, 256);
 }
 
+// SM count of the current device, looked up once per device.
+cudaError_t device_sms(int* sms) {
+  static std::atomic<int> cache[64];            // 0 = not looked up yet
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && (*sms = cache[dev].load(std::memory_order_relaxed)) > 0) return cudaSuccess;
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && cached) cache[dev].store(*sms, std::memory_order_relaxed);
+  return e;
+}
+
 // [T][cols] bf16 tensor map with a box of box_x columns x 64 rows
 bool make_map(CUtensorMap* m, const void* base, int64_t T, int64_t cols, int box_x, bool swizzle128) {
   return make_map_2d(m, base, T, cols, 2, box_x, 64, swizzle128);
@@ -938,7 +962,9 @@ cudaError_t launch_prep_dv(const PrefillArgs& a, const PrefillSched& sched, unsi
   auto prep = a.mode == KDA_MODE_DECAY_FIRST ? kda_chunk_prep_kernel<DV, true> : kda_chunk_prep_kernel<DV, false>;
   cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM);
   if (e != cudaSuccess) return e;
-  prep<<<(unsigned)((int64_t)a.H * total_chunks), PNT, P_SMEM, s>>>(a, sched, ws, maps);
+  const int64_t items = (int64_t)a.H * total_chunks;
+  if (items > INT32_MAX) return cudaErrorInvalidValue;
+  prep<<<(unsigned)items, PNT, P_SMEM, s>>>(a, sched, ws, maps);
   return cudaGetLastError();
 }
 
@@ -957,9 +983,8 @@ cudaError_t launch_chain_dv(const PrefillArgs& a, const PrefillSched& sched, con
   int cols = prefill_chain_columns();
   if (cols == 0) {
     // one CTA per SM at most: 32-column slices while twice the 64-column grid still fits
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int sms = 0;
+    cudaError_t e = device_sms(&sms);
     if (e != cudaSuccess) return e;
     cols = 2 * (int64_t)(DV / 64) * a.H * sched.n_seqs <= sms ? 32 : 64;
   }
@@ -1060,6 +1085,10 @@ extern "C" int kda_prefill_chunked_noalloc(const float* S0, const void* q, const
                                            void* page_pool, int64_t page_bytes,
                                            const int32_t* ckpt_page_ids, int32_t* ckpt_pos,
                                            int64_t num_ckpt, int mode, kda_stream_t stream) {
+  // the same argument checks (and errors) as kda_prefill_chunked come first
+  if (int st = kda::validate_prefill(S0, q, k, v, g, beta, cu_seqlens, n_seqs, T, H, dk, dv, dtype, chunk,
+                                     ckpt_stride, o, S_final, page_pool, page_bytes, ckpt_page_ids, num_ckpt, mode))
+    return st;
   const int64_t need = kda_prefill_workspace_bytes(cu_seqlens, n_seqs, T, H, dk, dv, dtype);
   if (need < 0) return (int)need;
   void* ws = nullptr;

@@ -161,9 +161,12 @@ __device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity) {
   return done != 0;
 }
 
-// Device-side error word: bit 0 = an mbarrier wait gave up.  Read and cleared
-// by the host through kda_device_errors(); one copy per translation unit that
-// includes this header (the tensor-core kernels live in one).
+// Device-side error word: bit 0 = an mbarrier wait gave up; bit 1 = a gate
+// outside the chunked prefill's range [-10, 0] (or NaN) was read.  Read and
+// cleared by the host through kda_device_errors(); one copy per translation
+// unit that includes this header (the tensor-core kernels live in one).
+constexpr int kDevErrWait = 1;
+constexpr int kDevErrGate = 2;
 static __device__ int g_kda_device_error = 0;
 
 // Wait for phase `parity` of an mbarrier, giving up after about one second
@@ -173,7 +176,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_test(mbar, parity)) {
     if (clock64() - t0 > (1LL << 31)) {
-      atomicOr(&g_kda_device_error, 1);
+      atomicOr(&g_kda_device_error, kDevErrWait);
       return false;
     }
   }
@@ -193,6 +196,28 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(mbar) : "memory");
+}
+
+// 2-D tile of a tensor map fetched into L2 only (no shared memory, no
+// completion to wait for): a later tma_load_2d of the same box hits L2.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               :: "l"(map), "r"(x), "r"(y) : "memory");
+}
+
+// Wait for phase `parity` of an mbarrier unless `abort_flag` becomes nonzero,
+// giving up after about one second (2^31 SM clocks, which raises the error
+// word).  Returns true only when the phase completed.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t mbar, uint32_t parity, volatile int* abort_flag) {
+  const long long t0 = clock64();
+  while (!mbar_test(mbar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > (1LL << 31)) {
+      atomicOr(&g_kda_device_error, kDevErrWait);
+      return false;
+    }
+  }
+  return true;
 }
 
 // shared -> global bulk copy tracked by bulk groups (16-byte aligned ends, size a multiple of 16)

@@ -23,6 +23,7 @@ PAGE_FREE, PAGE_KDA_STATE, PAGE_MLA_KV = 0, 1, 2
 LAYOUT_KV, LAYOUT_VK = 0, 1
 ACT_NONE, ACT_SILU = 0, 1
 MAX_DRAFT = 16
+DEVERR_WAIT, DEVERR_GATE = 1, 2
 
 
 class KdaError(RuntimeError):
@@ -360,7 +361,8 @@ def kda_prefill_workspace_bytes(cu_seqlens, T, H, dk, dv, dtype) -> int:
 
 
 def kda_device_errors() -> int:
-    """Read and clear the device error word (bit 0: an mbarrier wait timed out)."""
+    """Read and clear the device error word (DEVERR_WAIT: an mbarrier wait timed out;
+    DEVERR_GATE: a chunked prefill read a gate outside [-10, 0] or a NaN gate)."""
     flags = ctypes.c_int(0)
     _check(_lib.kda_device_errors(ctypes.byref(flags)), "kda_device_errors")
     return int(flags.value)

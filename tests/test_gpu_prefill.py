@@ -280,3 +280,29 @@ def test_tc_workspace_too_small_is_rejected(K):
         K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
                               ckpt_stride=0, workspace=ws)
     assert e.value.status == -2
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [(torch.bfloat16, 128, 128), (torch.float32, 64, 64)])
+def test_gate_outside_contract_is_flagged(K, dtype, dk, dv):
+    """The chunked kernels take g in [-10, 0] ([SERVE] §1.3 draws g = g_min sigmoid(.) in
+    [g_min, 0]; the block-reference factors reach e^(8 |g|)).  Gates drawn with g_min = -20
+    (about half of them below -10), or one NaN gate, raise DEVERR_GATE; gates drawn with
+    g_min = -10 raise nothing.  Both the tensor-core (bf16, dk = 128) and the CUDA-core
+    kernels are checked."""
+    H = 2
+    K.kda_device_errors()                                    # start from a clear word
+
+    def run(g_min, nan=False):
+        S0, p, cu = I.prefill_inputs([192], H, dk, dv, dtype=dtype, seed=5, g_min=g_min, device="cuda")
+        if nan:
+            p["g"][100, 1, 7] = float("nan")
+        K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu, ckpt_stride=0)
+        torch.cuda.synchronize()
+        return p, K.kda_device_errors()
+
+    p, flags = run(-10.0)
+    assert float(p["g"].min()) >= -10.0 and flags == 0
+    p, flags = run(-20.0)
+    assert bool((p["g"] < -10).any()) and flags & K.DEVERR_GATE
+    _, flags = run(-5.0, nan=True)
+    assert flags & K.DEVERR_GATE

@@ -34,61 +34,73 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _noalloc_call(K, S0, p, cu, H, dk, dv, stride, pool, ids, pos, o, S_fin):
+def _noalloc_call(K, S0, p, cu, H, dk, dv, stride, pool, ids, pos, o, S_fin, dtype=None):
     T = cu[-1]
     arr = (ctypes.c_int32 * len(cu))(*cu)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return K._lib.kda_prefill_chunked_noalloc(
         _ptr(S0), _ptr(p["q"]), _ptr(p["k"]), _ptr(p["v"]), _ptr(p["g"]), _ptr(p["beta"]),
-        arr, len(cu) - 1, T, H, dk, dv, K.KDA_BF16, 64, stride, _ptr(o), _ptr(S_fin),
-        ctypes.c_void_p(pool.arena.data_ptr()), pool.page_bytes, _ptr(ids), _ptr(pos), ids.numel(),
-        K.DECAY_FIRST, stream)
+        arr, len(cu) - 1, T, H, dk, dv, K.KDA_BF16 if dtype is None else dtype, 64, stride, _ptr(o),
+        _ptr(S_fin), ctypes.c_void_p(pool.arena.data_ptr()), pool.page_bytes, _ptr(ids), _ptr(pos),
+        ids.numel(), K.DECAY_FIRST, stream)
 
 
-def _one_call(K, lengths, seed, H=4, d=128, stride=128):
-    S0, p, cu = I.prefill_inputs(lengths, H, d, d, dtype=torch.bfloat16, seed=seed, device="cuda")
+def _one_call(K, lengths, seed, H=4, dk=128, dv=128, dtype=torch.bfloat16, stride=128):
+    S0, p, cu = I.prefill_inputs(lengths, H, dk, dv, dtype=dtype, seed=seed, device="cuda")
     T = cu[-1]
-    need = K.kda_prefill_workspace_bytes(cu, T, H, d, d, torch.bfloat16)
-    assert 0 < need <= (64 << 20)                 # fits the built-in scratch
+    need = K.kda_prefill_workspace_bytes(cu, T, H, dk, dv, dtype)
+    assert need <= (64 << 20)                     # fits the built-in scratch (0: CUDA-core kernel)
     n_ck = K.kda_num_checkpoints(cu, T, stride)
-    page_bytes = H * d * d * 4 + 256
+    page_bytes = H * dk * dv * 4 + 256
     pools, outs = [], []
     for _ in range(2):
         pool = K.PagePool(page_bytes, n_ck)
         pool.arena.fill_(0x5A)
         ids = torch.tensor(pool.alloc(n_ck), dtype=torch.int32, device="cuda")
         pos = torch.full((n_ck,), -1, dtype=torch.int32, device="cuda")
-        o = torch.empty(T, H, d, dtype=torch.bfloat16, device="cuda")
+        o = torch.empty(T, H, dv, dtype=dtype, device="cuda")
         S_fin = torch.empty_like(S0)
         pools.append((pool, ids, pos))
         outs.append((o, S_fin))
-    # regular entry point with a caller workspace
+    # regular entry point: with a caller workspace where the shape takes one, else without
     pool, ids, pos = pools[0]
     K.kda_prefill_chunked(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], cu_seqlens=cu,
                           ckpt_stride=stride, page_pool=pool, ckpt_page_ids=ids, ckpt_pos=pos,
-                          o=outs[0][0], S_final=outs[0][1], workspace="auto")
+                          o=outs[0][0], S_final=outs[0][1], workspace="auto" if need > 0 else None)
     # allocation-free entry point, straight through the C ABI
     pool, ids, pos = pools[1]
-    st = _noalloc_call(K, S0, p, cu, H, d, d, stride, pool, ids, pos, *outs[1])
+    code = K.KDA_BF16 if dtype == torch.bfloat16 else K.KDA_F32
+    st = _noalloc_call(K, S0, p, cu, H, dk, dv, stride, pool, ids, pos, *outs[1], dtype=code)
     assert st == 0, K._lib.kda_last_error()
     torch.cuda.synchronize()
     assert K.kda_device_errors() == 0
     (o_ref, S_ref), (o_na, S_na) = outs
-    assert rel(o_na, o_ref) < TOL_BF16_OUT
-    assert rel(S_na, S_ref) < TOL_BF16_STATE
+    # both calls run the same kernels on the same inputs: the results agree bit for bit
+    # (a stale or partly overwritten scratch would show here); the tolerances only
+    # describe the size of a difference if there is one
+    assert torch.equal(o_na, o_ref), f"outputs differ, rel {rel(o_na, o_ref):.3g} (bf16 bound {TOL_BF16_OUT})"
+    assert torch.equal(S_na, S_ref), f"final states differ, rel {rel(S_na, S_ref):.3g} (bound {TOL_BF16_STATE})"
     assert torch.equal(pools[1][2], pools[0][2])                 # checkpoint positions
-    n_state = H * d * d
+    n_state = H * dk * dv
     for c in range(n_ck):
         a = pools[0][0].page(int(pools[0][1][c]))
         b = pools[1][0].page(int(pools[1][1][c]))
-        assert rel(b[:n_state], a[:n_state]) < TOL_BF16_STATE
+        assert torch.equal(b[:n_state], a[:n_state]), f"checkpoint {c} differs"
         assert torch.all(b[n_state:] == 0)
+    return need
 
 
 def test_noalloc_matches_workspace_entry_point_twice(K):
     # two calls in a row: the second reuses the scratch the first one left behind
-    _one_call(K, [200, 64, 130], seed=21)
-    _one_call(K, [320, 5, 0, 257], seed=22)
+    assert _one_call(K, [200, 64, 130], seed=21) > 0
+    assert _one_call(K, [320, 5, 0, 257], seed=22) > 0
+
+
+def test_noalloc_without_scratch_runs_the_cuda_core_kernel(K):
+    # fp32 projections and a dk other than 128 need no scratch: the call runs the fp32
+    # CUDA-core kernel, exactly as kda_prefill_chunked does with a NULL workspace
+    assert _one_call(K, [130, 64], seed=23, H=2, dk=64, dv=64, dtype=torch.float32, stride=64) == 0
+    assert _one_call(K, [100], seed=24, H=2, dk=32, dv=128, dtype=torch.bfloat16, stride=64) == 0
 
 
 def test_noalloc_refuses_calls_larger_than_its_scratch(K):
