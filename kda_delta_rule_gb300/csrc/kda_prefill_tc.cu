@@ -576,18 +576,24 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 // One CTA per (sequence, head, slice of DVS = 32 or 64 columns of dv), ten
 // warps: 32-column slices when 64-column ones would leave more than half of
 // the SMs idle (the chain is latency-bound, and an N = 32 product reads 5 KB
-// of operands instead of 6 KB while the per-row register work halves).  Warp 9
-// issues every tensor-core product and every image copy (it shares a
-// scheduler with warps 1 and 5, which wait on the products it issues); warp 8
-// writes checkpoint pages from a staging buffer the row warps fill, so no
-// global store precedes a hand-off on the critical path; warps 0-7 do the
-// per-row work, warps w and w + 4 sharing TMEM lane quadrant w % 4 and taking
-// the left and right DVS / 2 columns of its rows.  Hand-offs go through mbarriers
-// only:  bar1 / bar3 / bar2 (product commits), dready (Delta' written by warps
-// 0, 1, 4, 5) and sready (chunk done by warps 0-7: state written, TMEM and
-// stage reads finished, the output rows of the chunk in registers).
-constexpr int CNT = 320;                           // chain threads: 8 row warps, 1 idle, 1 issuing
-constexpr int ISSUER = 9;                          // the issuing warp
+// of operands instead of 6 KB while the per-row register work halves).  Warps
+// 0-7 own the state rows, warps w and w + 4 sharing TMEM lane quadrant w % 4
+// and taking the left and right DVS / 2 columns of its rows; warp 8 writes
+// checkpoint pages from a staging buffer the row warps fill, so no global
+// store precedes a hand-off on the critical path; warp 9 streams the chunk
+// images into a two-stage ring.  Each product is issued by warp 0 right after
+// a named barrier of the warps that wrote its operand: Kbar^T Delta' (MMA3)
+// and P Delta' (MMA2) after the four Delta' warps (0, 1, 4, 5), [-bW; Qt] S
+// (MMA1) of the next chunk after all eight row warps have staged the state.
+// The output rows of a chunk are read back by warps 2, 3, 6, 7 while the next
+// chunk's Delta' is formed, when the tensor pipe is idle and they would only
+// wait.  Products report completion on mbarriers (bar1, bar3, bar2); a commit
+// after the eight-warp barrier hands a ring stage back to warp 9.
+// Both named barriers OR an error flag over their warps, so the row warps
+// leave the loop together; every mbarrier wait is bounded and watches the
+// abort flag.
+constexpr int CNT = 320;                           // chain threads: 8 row warps, writer, producer
+constexpr int PRODUCER = 9;                        // the image-copy warp
 constexpr int CRW = 256;                           // row threads
 constexpr uint32_t S_WQ = 0, S_KB = 32768, S_PB = 49152, S_U = 65536, S_EG = 73728;
 constexpr uint32_t STAGE = 75776;                 // 74 KB, keeps every stage 1024-aligned
@@ -603,6 +609,20 @@ constexpr uint32_t CHUNK_TX = 32768 + 16384 + 8192 + 8192 + 512;
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[32]) { tmem_ld32(taddr, v); }
 
+// Named barrier over `nthreads` threads that also ORs a predicate over them:
+// every participant gets the same answer.
+__device__ __forceinline__ bool bar_sync_or(int id, int nthreads, bool pred) {
+  int r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.s32 p, %1, 0; barrier.cta.red.or.pred q, %2, %3, p; selp.s32 %0, 1, 0, q; }"
+      : "=r"(r) : "r"((int)pred), "r"(id), "r"(nthreads) : "memory");
+  return r != 0;
+}
+// A whole warp waits on an mbarrier phase (bounded, abort-aware); the result is warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_test(mbar, parity) || mbar_wait_or_abort(mbar, parity, abort_flag));
+}
+
 template <int DV, int DVS>
 __global__ void __launch_bounds__(CNT, 1)
 kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned char* __restrict__ ws) {
@@ -610,12 +630,11 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   constexpr int NC = DVS / 2;                          // state columns per row thread
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const uint32_t full0 = smem_u32(sm + C_MISC);         // two image stages
+  const uint32_t full0 = smem_u32(sm + C_MISC);         // two image stages landed
   const uint32_t bar1 = smem_u32(sm + C_MISC + 16);     // [-bW; Qt] S done
   const uint32_t bar3 = smem_u32(sm + C_MISC + 24);     // Kbar^T Delta' done
   const uint32_t bar2 = smem_u32(sm + C_MISC + 32);     // P Delta' done
-  const uint32_t dready = smem_u32(sm + C_MISC + 40);   // Delta' in shared memory (4 warps)
-  const uint32_t sready = smem_u32(sm + C_MISC + 48);   // chunk finished by the row warps (8 warps)
+  const uint32_t free0 = smem_u32(sm + C_MISC + 40);    // two image stages released
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + C_MISC + 64);
   const uint32_t ckfull = smem_u32(sm + C_MISC + 88);   // staging filled (8 row warps)
   const uint32_t ckfree = smem_u32(sm + C_MISC + 96);   // staging written out (warp 8)
@@ -639,14 +658,14 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     mbar_init(bar1, 1);
     mbar_init(bar3, 1);
     mbar_init(bar2, 1);
-    mbar_init(dready, 4);
-    mbar_init(sready, 8);
+    mbar_init(free0, 1);
+    mbar_init(free0 + 8, 1);
     mbar_init(ckfull, 8);
     mbar_init(ckfree, 1);
     *s_abort = 0;
     mbar_init_fence();
   }
-  if (warp == ISSUER) tmem_alloc(smem_u32(tslot), 256);
+  if (warp == PRODUCER) tmem_alloc(smem_u32(tslot), 256);
   // zero rows 0-63 of both [0; P] buffers (never written by the copies)
   for (int e = tid; e < 2 * 512; e += CNT) {
     const int s = e >> 9, o = e & 511;
@@ -677,99 +696,36 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
   constexpr uint32_t ID_1 = idesc_bf16(128, DVS, false, true);   // [-bW; Qt] (K-major) x S (MN-major)
   constexpr uint32_t ID_3 = idesc_bf16(128, DVS, true, true);    // Kbar^T (MN-major) x Delta' (MN-major)
 
-  if (warp == ISSUER) {
-    // ---- issuing warp ----------------------------------------------------------
-    auto copy = [&](int cidx) {                                    // lane 0 only
-      const int s = cidx & 1;
-      const unsigned char* src = img0 + (int64_t)cidx * H * ib;
-      const uint32_t dst = smem_u32(sm + s * STAGE);
-      const uint32_t fb = full0 + 8 * s;
-      mbar_expect_tx(fb, CHUNK_TX);
-      bulk_g2s(dst + S_WQ, src + IMG_WQ, 32768, fb);
-      bulk_g2s(dst + S_KB, src + IMG_KB, 16384, fb);
-      bulk_g2s(dst + S_PB + 8192, src + IMG_P, 8192, fb);
-      bulk_g2s(dst + S_U, src + IMG_U + (col0 >> 6) * 8192, 8192, fb);   // the 64-column block of the slice
-      bulk_g2s(dst + S_EG, src + img_eg(DV), 512, fb);
-    };
-    // operand descriptors, computed once: k-step j only moves the start address
-    // (16-byte units in the low bits): +2 j within a 128-byte swizzle row and
-    // +8 * R per 64-element K block (K-major, R rows), +128 j (MN-major)
-    const uint64_t dS = desc_mn(sb, 128, 0), dD = desc_mn(delta, 64, 0);
-    const uint64_t dW0 = desc_k(smem_u32(sm + S_WQ), 128, 0), dW1 = desc_k(smem_u32(sm + STAGE + S_WQ), 128, 0);
-    const uint64_t dK0 = desc_mn(smem_u32(sm + S_KB), 64, 0), dK1 = desc_mn(smem_u32(sm + STAGE + S_KB), 64, 0);
-    const uint64_t dP0 = desc_k(smem_u32(sm + S_PB), 128, 0), dP1 = desc_k(smem_u32(sm + STAGE + S_PB), 128, 0);
-    auto mma1 = [&](auto stage_tag) {
-      constexpr int s = decltype(stage_tag)::value;
-      const uint64_t dW = s ? dW1 : dW0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma_w(tmem + 64u * s, dW + (uint64_t)((j >> 2) * 1024 + (j & 3) * 2), dS + (uint64_t)(128 * j), ID_1, j > 0);
-      mma_commit_w(bar1);
-    };
-    auto mma32 = [&](auto stage_tag) {
-      constexpr int s = decltype(stage_tag)::value;
-      const uint64_t dK = s ? dK1 : dK0, dP = s ? dP1 : dP0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma_w(d2, dK + (uint64_t)(128 * j), dD + (uint64_t)(128 * j), ID_3, j > 0);
-      mma_commit_w(bar3);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mma_w(tmem + 64u * s, dP + (uint64_t)(2 * j), dD + (uint64_t)(128 * j), ID_1, 1);
-      mma_commit_w(bar2);
-    };
-    int issued = 0;                        // image copies issued
-    int last1 = -1, last2 = -1;            // last chunk whose MMA1 / MMA3+MMA2 were issued
-    bool ok = nch > 0;
-    if (ok) {
-      if (lane == 0) {
-        copy(0);
-        if (nch > 1) copy(1);
-      }
-      issued = min(nch, 2);
-      __syncwarp();
-      ok = __all_sync(0xffffffffu, mbar_wait(full0, 0));
-      if (ok) { mma1(std::integral_constant<int, 0>{}); last1 = 0; }
-    }
-    // chunk c: MMA3/MMA2 once Delta' is in; MMA1(c+1) once the row warps are
-    // through chunk c and its images are in; then stage c & 1 is free for c + 2
-    auto step = [&](auto stage_tag, int c) -> bool {
-      constexpr int s = decltype(stage_tag)::value;
-      const uint32_t ph = (uint32_t)(c & 1);
-      if (*s_abort) return false;
-      if (!__all_sync(0xffffffffu, mbar_wait(dready, ph))) return false;
-      fence_after();
-      mma32(stage_tag);
-      last2 = c;
-      if (c + 1 < nch) {
-        if (*s_abort) return false;
-        bool w = mbar_wait(sready, ph);
-        w = w && mbar_wait(full0 + 8 * (s ^ 1), ((c + 1) >> 1) & 1);
-        if (!__all_sync(0xffffffffu, w)) return false;
-        fence_after();
-        mma1(std::integral_constant<int, s ^ 1>{});
-        last1 = c + 1;
-        if (c + 2 < nch) {
-          if (lane == 0) copy(c + 2);
-          issued = c + 3;
+  if (warp == PRODUCER) {
+    // ---- image copies: stage c & 1 of chunk c, once the products of chunk c - 2
+    // are complete and the row warps are through it (the free commit) ----------
+    if (lane == 0) {
+      auto copy = [&](int cidx) {
+        const int s = cidx & 1;
+        const unsigned char* src = img0 + (int64_t)cidx * H * ib;
+        const uint32_t dst = smem_u32(sm + s * STAGE);
+        const uint32_t fb = full0 + 8 * s;
+        mbar_expect_tx(fb, CHUNK_TX);
+        bulk_g2s(dst + S_WQ, src + IMG_WQ, 32768, fb);
+        bulk_g2s(dst + S_KB, src + IMG_KB, 16384, fb);
+        bulk_g2s(dst + S_PB + 8192, src + IMG_P, 8192, fb);
+        bulk_g2s(dst + S_U, src + IMG_U + (col0 >> 6) * 8192, 8192, fb);   // the 64-column block of the slice
+        bulk_g2s(dst + S_EG, src + img_eg(DV), 512, fb);
+      };
+      int issued = 0;
+      for (int c = 0; c < nch; ++c) {
+        if (c >= 2 && !mbar_wait_or_abort(free0 + 8 * (c & 1), (uint32_t)(((c - 2) >> 1) & 1), s_abort)) {
+          *s_abort = 1;
+          break;
         }
+        copy(c);
+        issued = c + 1;
       }
-      return true;
-    };
-    int c = 0;
-    while (ok && c < nch) {
-      ok = step(std::integral_constant<int, 0>{}, c);
-      if (!ok || ++c >= nch) break;
-      ok = step(std::integral_constant<int, 1>{}, c);
-      if (!ok) break;
-      ++c;
+      // leave no copy in flight into this CTA's shared memory (bounded waits; a
+      // phase that already completed returns at once)
+      for (int cc = max(0, issued - 2); cc < issued; ++cc) mbar_wait(full0 + 8 * (cc & 1), (uint32_t)((cc >> 1) & 1));
     }
-    if (!ok && nch > 0) {
-      *s_abort = 1;
-      // leave nothing in flight (bounded waits; a phase that already completed
-      // returns at once): the image copies issued and the last products
-      for (int cc = max(0, issued - 2); cc < issued; ++cc) mbar_wait(full0 + 8 * (cc & 1), (cc >> 1) & 1);
-      if (last1 >= 0) mbar_wait(bar1, (uint32_t)(last1 & 1));
-      if (last2 >= 0) { mbar_wait(bar3, (uint32_t)(last2 & 1)); mbar_wait(bar2, (uint32_t)(last2 & 1)); }
-    }
+    __syncwarp();
   } else if (warp == 8) {
     // ---- checkpoint writer: each staged checkpoint, 128 rows of 256 bytes --------
     const int ck_every = a.ckpt_stride > 0 && (sched.flags[n] & kSeqEmit) ? a.ckpt_stride / C : 0;
@@ -784,7 +740,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
         // one bounded wait: it ends when the rows are staged, when another warp
         // aborts, or after about a second (error word raised); either failure
         // ends this warp's loop and aborts the CTA
-        if (!__all_sync(0xffffffffu, mbar_wait_or_abort(ckfull, (uint32_t)(k & 1), s_abort))) {
+        if (!warp_wait(ckfull, (uint32_t)(k & 1), s_abort)) {
           *s_abort = 1;
           break;
         }
@@ -802,7 +758,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       }
     }
     bulk_wait_all();
-  } else if (warp < 8) {
+  } else {
     // ---- row warps -------------------------------------------------------------
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
     const uint32_t lane_off = (uint32_t)(32 * qd) << 16;
@@ -810,50 +766,117 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     const int ck_every = a.ckpt_stride > 0 && emit ? a.ckpt_stride / C : 0;
     int ck_left = ck_every;
     int n_ck = 0;                          // checkpoints staged so far
+    // operand descriptors, computed once: k-step j only moves the start address
+    // (16-byte units in the low bits): +2 j within a 128-byte swizzle row and
+    // +8 * R per 64-element K block (K-major, R rows), +128 j (MN-major)
+    const uint64_t dS = desc_mn(sb, 128, 0), dD = desc_mn(delta, 64, 0);
+    const uint64_t dW0 = desc_k(smem_u32(sm + S_WQ), 128, 0), dW1 = desc_k(smem_u32(sm + STAGE + S_WQ), 128, 0);
+    const uint64_t dK0 = desc_mn(smem_u32(sm + S_KB), 64, 0), dK1 = desc_mn(smem_u32(sm + STAGE + S_KB), 64, 0);
+    const uint64_t dP0 = desc_k(smem_u32(sm + S_PB), 128, 0), dP1 = desc_k(smem_u32(sm + STAGE + S_PB), 128, 0);
+    // products issued by warp 0 (all lanes run these; one elected lane issues)
+    int last1 = -1, last32 = -1;           // last chunk whose MMA1 / MMA3+MMA2 were issued (warp 0)
+    int last_free = -1;                    // last chunk whose stage-release commit was issued (warp 0)
+    auto mma1 = [&](auto stage_tag, int cidx) {
+      constexpr int s = decltype(stage_tag)::value;
+      const uint64_t dW = s ? dW1 : dW0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mma_w(tmem + 64u * s, dW + (uint64_t)((j >> 2) * 1024 + (j & 3) * 2), dS + (uint64_t)(128 * j), ID_1, j > 0);
+      mma_commit_w(bar1);
+      last1 = cidx;
+    };
+    auto mma32 = [&](auto stage_tag, int cidx) {
+      constexpr int s = decltype(stage_tag)::value;
+      const uint64_t dK = s ? dK1 : dK0, dP = s ? dP1 : dP0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_w(d2, dK + (uint64_t)(128 * j), dD + (uint64_t)(128 * j), ID_3, j > 0);
+      mma_commit_w(bar3);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_w(tmem + 64u * s, dP + (uint64_t)(2 * j), dD + (uint64_t)(128 * j), ID_1, 1);
+      mma_commit_w(bar2);
+      last32 = cidx;
+    };
+    // outputs of chunk cc: rows 64-127 of d1[cc & 1] (warps 2, 3, 6, 7); the buffer is
+    // next written by chunk cc + 2's MMA1, issued after these warps pass chunk cc + 1's
+    // eight-warp barrier.  Chunk cc's MMA2 is known complete once chunk cc + 1's bar1
+    // has been seen (warp 0 commits that after issuing the MMA2); only the last
+    // chunk waits on bar2 itself.
+    auto read_outputs = [&](int cc, bool wait_bar2) -> bool {
+      if (wait_bar2 && !warp_wait(bar2, (uint32_t)(cc & 1), s_abort)) return false;
+      fence_after();
+      float ov[NC];
+      tmem_ld_cols(tmem + 64u * (cc & 1) + lane_off + jc, ov);
+      const int r = i - 64;
+      if (emit && r < min(C, len - cc * C)) {
+        __nv_bfloat16* orow = o + ((start + (int64_t)cc * C + r) * H + h) * DV + col0 + jc;
+#pragma unroll
+        for (int q8 = 0; q8 < NC / 8; ++q8) *reinterpret_cast<uint4*>(orow + 8 * q8) = pack8(ov + 8 * q8);
+      }
+      return true;
+    };
+    if (nch > 0 && warp == 0) {
+      if (warp_wait(full0, 0, s_abort)) {
+        fence_after();
+        mma1(std::integral_constant<int, 0>{}, 0);
+      } else {
+        *s_abort = 1;
+      }
+    }
     auto row_step = [&](auto stage_tag, int c) -> bool {
       constexpr int s = decltype(stage_tag)::value;
       const uint32_t ph = (uint32_t)(c & 1);
       const unsigned char* st = sm + s * STAGE;
       const uint32_t d1 = tmem + 64u * s;
-      if (*s_abort) return false;
-      // the images of chunk c (complete long ago; acquires them for this thread)
-      if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (c >> 1) & 1))) return false;
+      // the images of chunk c (landed long ago; acquires them for this thread)
+      bool good = warp_wait(full0 + 8 * s, (uint32_t)((c >> 1) & 1), s_abort);
+      // shared-memory inputs of this chunk's row work, loaded before the waits
+      // on the products
+      const float eg = good ? reinterpret_cast<const float*>(st + S_EG)[i] : 0.f;
       if (qd < 2) {                         // Delta' = beta U - beta W S, token row r
-        if (!__all_sync(0xffffffffu, mbar_wait(bar1, ph))) return false;
-        fence_after();
         const int r = i;
-        float v[NC];
-        tmem_ld_cols(d1 + lane_off + jc, v);
         const uint4* urow = reinterpret_cast<const uint4*>(st + S_U + r * 128);
-        const int cb0 = ((col0 & 63) + jc) >> 3;           // first 16-byte chunk of this thread's columns
+        const int cb0 = ((col0 & 63) + jc) >> 3;             // first 16-byte chunk of this thread's columns
         uint4 u[NC / 8];
 #pragma unroll
-        for (int cc = 0; cc < NC / 8; ++cc)                // all loads before any store
-          u[cc] = use_u ? urow[(cb0 + cc) ^ (r & 7)] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int cc = 0; cc < NC / 8; ++cc) {
-          const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u[cc]);
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float2 x = __bfloat1622float2(pu[t]);
-            v[8 * cc + 2 * t] += x.x;
-            v[8 * cc + 2 * t + 1] += x.y;
-          }
-        }
-#pragma unroll
         for (int cc = 0; cc < NC / 8; ++cc)
-          *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(jc + 8 * cc, r, 64)) = pack8(v + 8 * cc);
-        fence_async_smem();
+          u[cc] = good && use_u ? urow[(cb0 + cc) ^ (r & 7)] : make_uint4(0u, 0u, 0u, 0u);
+        good = good && warp_wait(bar1, ph, s_abort);
+        if (good) {
+          fence_after();
+          float v[NC];
+          tmem_ld_cols(d1 + lane_off + jc, v);
+#pragma unroll
+          for (int cc = 0; cc < NC / 8; ++cc) {
+            const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u[cc]);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float2 x = __bfloat1622float2(pu[t]);
+              v[8 * cc + 2 * t] += x.x;
+              v[8 * cc + 2 * t + 1] += x.y;
+            }
+          }
+#pragma unroll
+          for (int cc = 0; cc < NC / 8; ++cc)
+            *reinterpret_cast<uint4*>(sm + C_DELTA + off_mn(jc + 8 * cc, r, 64)) = pack8(v + 8 * cc);
+          fence_async_smem();
+        }
         fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dready);
+        if (bar_sync_or(1, 128, !good)) {     // the four Delta' warps
+          *s_abort = 1;
+          good = false;
+        } else if (warp == 0) {
+          fence_after();
+          mma32(stage_tag, c);
+        }
+      } else if (c > 0) {
+        // the previous chunk's outputs, read while Delta' is formed: this chunk's
+        // MMA1 is complete first, so the tensor pipe is idle meanwhile
+        good = good && warp_wait(bar1, ph, s_abort) && read_outputs(c - 1, false);
       }
-      if (*s_abort) return false;
-      if (!__all_sync(0xffffffffu, mbar_wait(bar3, ph))) return false;
-      fence_after();
       // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
-      {
-        const float eg = reinterpret_cast<const float*>(st + S_EG)[i];
+      good = good && warp_wait(bar3, ph, s_abort);
+      if (good) {
+        fence_after();
         float v[NC];
         tmem_ld_cols(d2 + lane_off + jc, v);
 #pragma unroll
@@ -869,56 +892,69 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       // buffer once warp 8 has written out the previous checkpoint
       const bool ck = ck_every > 0 && --ck_left == 0;
       if (ck) ck_left = ck_every;
-      if (ck && L == C) {
+      if (good && ck && L == C) {
         const int64_t idx = (int64_t)sched.ckpt_base[n] + pos / a.ckpt_stride - 1;
         if (idx < a.num_ckpt) {
-          if (n_ck > 0 && !__all_sync(0xffffffffu, mbar_wait(ckfree, (uint32_t)((n_ck - 1) & 1)))) return false;
-          float4* srow = reinterpret_cast<float4*>(sm + C_CK + i * CK_ROW + jc * 4);
+          good = n_ck == 0 || warp_wait(ckfree, (uint32_t)((n_ck - 1) & 1), s_abort);
+          if (good) {
+            float4* srow = reinterpret_cast<float4*>(sm + C_CK + i * CK_ROW + jc * 4);
 #pragma unroll
-          for (int j = 0; j < NC / 4; ++j) srow[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ckfull);
-          ++n_ck;
-          if (h == 0 && sl == 0) {
-            float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
-            const int64_t used = (int64_t)H * DKT * DV, total = a.page_bytes / 4;
-            for (int64_t e = used + tid; e < total; e += CRW) page[e] = 0.f;   // pad past the state
-            if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = sched.pos_base[n] + pos;
+            for (int j = 0; j < NC / 4; ++j) srow[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ckfull);
+            ++n_ck;
+            if (h == 0 && sl == 0) {
+              float* page = reinterpret_cast<float*>(a.page_pool + (int64_t)a.ckpt_page_ids[idx] * a.page_bytes);
+              const int64_t used = (int64_t)H * DKT * DV, total = a.page_bytes / 4;
+              for (int64_t e = used + tid; e < total; e += CRW) page[e] = 0.f;   // pad past the state
+              if (tid == 0 && a.ckpt_pos) a.ckpt_pos[idx] = sched.pos_base[n] + pos;
+            }
           }
         }
       }
-      float ov[NC];
-      if (qd >= 2) {                        // outputs of chunk c: rows 64-127 of d1[c&1]
-        if (*s_abort) return false;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar2, ph))) return false;
-        fence_after();
-        tmem_ld_cols(d1 + lane_off + jc, ov);
-      }
       fence_async_smem();
       fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sready);
-      if (qd >= 2) {
-        const int r = i - 64;
-        if (emit && r < L) {
-          __nv_bfloat16* orow = o + ((start + (int64_t)c * C + r) * H + h) * DV + col0 + jc;
-#pragma unroll
-          for (int cc = 0; cc < NC / 8; ++cc) *reinterpret_cast<uint4*>(orow + 8 * cc) = pack8(ov + 8 * cc);
+      if (bar_sync_or(2, CRW, !good)) {       // all eight row warps
+        *s_abort = 1;
+        return false;
+      }
+      if (warp == 0) {
+        fence_after();
+        // every product reading stage s has been issued and the row warps are
+        // through it: the commit hands the stage back to the copy warp once the
+        // products are complete; then the next chunk's MMA1 goes in
+        mma_commit_w(free0 + 8 * s);
+        last_free = c;
+        if (c + 1 < nch) {
+          if (warp_wait(full0 + 8 * (s ^ 1), (uint32_t)(((c + 1) >> 1) & 1), s_abort)) {
+            fence_after();
+            mma1(std::integral_constant<int, s ^ 1>{}, c + 1);
+          } else {
+            *s_abort = 1;                   // the other warps see it at their next wait
+          }
         }
       }
       return true;
     };
-    bool ok = true;
     int c = 0;
-    while (ok && c < nch) {
-      ok = row_step(std::integral_constant<int, 0>{}, c);
-      if (!ok || ++c >= nch) break;
-      ok = row_step(std::integral_constant<int, 1>{}, c);
-      if (!ok) break;
+    // warp 0's failure before the loop reaches the other warps through the abort
+    // flag at their first wait, and every warp then leaves at the first barrier
+    bool ok = true;
+    while (c < nch) {
+      if (!(ok = row_step(std::integral_constant<int, 0>{}, c)) || ++c >= nch) break;
+      if (!(ok = row_step(std::integral_constant<int, 1>{}, c))) break;
       ++c;
     }
-    if (!ok) *s_abort = 1;
+    // the last chunk's outputs (no later chunk reads them back)
+    if (ok && nch > 0 && qd >= 2 && !read_outputs(nch - 1, true)) *s_abort = 1;
+    if (warp == 0 && *s_abort) {
+      // leave no product in flight (bounded waits; a phase that already completed
+      // returns at once)
+      if (last1 >= 0) mbar_wait(bar1, (uint32_t)(last1 & 1));
+      if (last32 >= 0) { mbar_wait(bar3, (uint32_t)(last32 & 1)); mbar_wait(bar2, (uint32_t)(last32 & 1)); }
+      if (last_free >= 0) mbar_wait(free0 + 8 * (last_free & 1), (uint32_t)((last_free >> 1) & 1));
+    }
   }
   fence_before();
   __syncthreads();
@@ -928,7 +964,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
 #pragma unroll
     for (int j = 0; j < NC; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
   }
-  if (warp == ISSUER) tmem_dealloc(tmem, 256);
+  if (warp == PRODUCER) tmem_dealloc(tmem, 256);
 }
 
 // SM count of the current device, looked up once per device.

@@ -76,6 +76,24 @@ __device__ __forceinline__ void mma_w(uint32_t d_tmem, uint64_t a, uint64_t b, u
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
       :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
+// A operand from TMEM (lanes = rows, K packed two bf16 per 32-bit column),
+// B from shared memory; issued by one elected lane of a converged warp.
+__device__ __forceinline__ void mma_tw(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p, e; .reg .b32 r; elect.sync r|e, 0xffffffff; setp.ne.b32 p, %4, 0; "
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// Shared memory -> TMEM copy of 128 rows x 32 bytes described by a matrix
+// descriptor (one 16-wide k-step of a K-major operand tile lands as 8 columns,
+// row r in lane r), issued by one elected lane; ordered before later products
+// of the same thread.
+__device__ __forceinline__ void tmem_cp_w(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{ .reg .pred e; .reg .b32 r; elect.sync r|e, 0xffffffff; "
+      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1; }"
+      :: "r"(taddr), "l"(sdesc) : "memory");
+}
 __device__ __forceinline__ void mma_commit_w(uint32_t mbar) {
   asm volatile(
       "{ .reg .pred e; .reg .b32 r; elect.sync r|e, 0xffffffff; "
