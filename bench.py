@@ -53,8 +53,8 @@ WORKLOAD = (f"kda_prefill_chunked long single sequence: B=1 H={H} dk=dv={DK} T={
 
 
 # DRAM bytes (read + write) of one prefill call measured by ncu on the T=8192 H=32 d=128
-# case (profiles/prefill_long_T8192_H32_d128_bf16.md), valid only for the kernel source it
-# was taken on: reported as null once kda_prefill_tc.cu changes.
+# case, keyed by the hash of the kernel source it was taken on: reported as null once
+# kda_prefill_tc.cu changes.
 PREFILL_TRAFFIC = {"3a56453556b31d49": 904_848_128}
 
 
@@ -258,8 +258,36 @@ def bench_prefill(K, dev, steps, warmup, rank):
     torch.cuda.synchronize(dev)
     D.barrier()
     e2e_ms = e0.elapsed_time(e1)
+
+    # the host link alone: the same bytes as one end-to-end step, one pinned-memory copy
+    # per tensor (cudaMemcpyAsync through torch), host-to-device and device-to-host each
+    # timed on its own with CUDA events; the two directions can run at the same time
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    dev_S0 = torch.empty_like(host_S0, device=dev)
+
+    def h2d_copies():
+        for n, t in host_in.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        dev_S0.copy_(host_S0, non_blocking=True)
+
+    def d2h_copies():
+        host_o.copy_(o, non_blocking=True)
+        host_S.copy_(S_fin, non_blocking=True)
+
+    link = {}
+    for name, fn in (("h2d", h2d_copies), ("d2h", d2h_copies)):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(steps):
+            fn()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        link[name] = c0.elapsed_time(c1) / steps
     return dict(total_ms=total_ms, kern_ms=kern_ms, bytes_step=bytes_step, clocks=clk.summary(),
-                n_ck=n_ck, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+                n_ck=n_ck, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, link=link)
 
 
 def bench_decode(K, dev, warmup=3, runs=3, layout=None):
@@ -658,7 +686,13 @@ def main():
                          "tc_tflops": flops / (kern_avg_ms / 1e3) / 1e12,
                          "tc_frac": flops / (kern_avg_ms / 1e3) / 1e12 / tf},
             "e2e": {"value": T * world * args.steps / (e2e_max / 1e3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                    "ms_per_step": e2e_max / args.steps,
+                    # plain pinned copies of the same bytes: the bound the host link sets on e2e
+                    "host_link": {"h2d_ms": r["link"]["h2d"], "d2h_ms": r["link"]["d2h"],
+                                  "h2d_GBps": r["h2d"] / (r["link"]["h2d"] / 1e3) / 1e9,
+                                  "d2h_GBps": r["d2h"] / (r["link"]["d2h"] / 1e3) / 1e9,
+                                  "bound_tokens_per_s": T / (max(r["link"]["h2d"], r["link"]["d2h"]) / 1e3)}},
             "gpu_launches": PREFILL_KERNELS_PER_CALL * args.steps,
             "clocks": r["clocks"],
             "cpu_baseline": cpu,

@@ -521,8 +521,167 @@ kda_step_kernel(const StepArgs a) {
   for (int m = 0; m < RPT; ++m) st_stream(Sout + (rg + RG * m) * ROWLEN + 4 * c4, S[m]);
 }
 
+// ---- 32 x 32 heads: one warp per head, one state column per lane ----------------
+// For the small heads of speculative replay ([SERVE] §1.2's demo shape, dk = dv = 32)
+// a warp holds a whole head with lane j owning column j of S (its 32 rows in
+// registers).  Both row reductions of a step are then the lane's own dot products
+// (a_j = sum_i w_i S_ij, b_j = sum_i e^{g_i} q_i S_ij) with no shuffles, and the
+// per-step row coefficients w_i, e^{g_i} q_i, e^{g_i}, beta k_i are shared-memory
+// broadcasts staged once per call.  Warps are independent: a CTA's four heads may
+// belong to different sequences and layers.
+constexpr int kSmallD = 32;
+constexpr int kSmallHPC = 4;          // heads (warps) per CTA
+
+template <typename T, bool TRANS, int MAXS>
+__global__ void __launch_bounds__(32 * kSmallHPC)
+kda_step_small_kernel(const StepArgs a) {
+  constexpr int D = kSmallD;
+  __shared__ float4 coef[kSmallHPC][MAXS][4][D / 4];   // per step: w, e^g q, e^g, beta k (rows 0..31)
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t nheads = (int64_t)a.B * a.H;
+  const int64_t head = (int64_t)blockIdx.x * kSmallHPC + w;   // over all stacked layers
+  if (head >= nheads * a.layers) return;                      // whole warps leave; no CTA barrier follows
+  const int64_t layer = head / nheads, hl = head - layer * nheads;
+  const int b = (int)(hl / a.H);
+  int n = a.steps;
+  if (a.n_accepted != nullptr) {
+    const int na = a.n_accepted[b];
+    n = na < 0 ? 0 : (na > a.steps ? a.steps : na);
+  }
+  int64_t srow_in = head, srow_out = head;
+  bool live_state = true;
+  if (a.slot_in != nullptr) {
+    const int32_t si = a.slot_in[b], so = a.slot_out[b];
+    live_state = si >= 0 && si < a.n_slots && so >= 0 && so < a.n_slots;
+    const int64_t h0 = layer * a.n_slots * a.H + (hl % a.H);
+    srow_in = live_state ? h0 + (int64_t)si * a.H : 0;
+    srow_out = live_state ? h0 + (int64_t)so * a.H : 0;
+  }
+  // ---- state: column `lane` (stored (dk, dv): one coalesced row per load;
+  // stored (dv, dk): the lane's own 128-byte row of S^T) ----
+  float S[D];
+  const float* Sin = a.S_in + srow_in * (int64_t)(D * D);
+  if (live_state) {
+    if constexpr (TRANS) {
+#pragma unroll
+      for (int i = 0; i < D; i += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(Sin + lane * D + i);
+        S[i] = x.x; S[i + 1] = x.y; S[i + 2] = x.z; S[i + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < D; ++i) S[i] = Sin[i * D + lane];
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < D; ++i) S[i] = 0.f;
+  }
+  // ---- projections of every step: lane i brings key channel i (and value channel i) ----
+  const T* q = reinterpret_cast<const T*>(a.q);
+  const T* k = reinterpret_cast<const T*>(a.k);
+  const T* v = reinterpret_cast<const T*>(a.v);
+  const T* g = reinterpret_cast<const T*>(a.g);
+  const T* beta = reinterpret_cast<const T*>(a.beta);
+  float rk[MAXS], rq[MAXS], rg[MAXS], rv[MAXS], rb[MAXS];
+#pragma unroll
+  for (int s = 0; s < MAXS; ++s) {
+    const bool live = s < n;
+    int slot = a.ring_start + s;                       // stored step of step s
+    if (slot >= a.proj_steps) slot -= a.proj_steps;
+    const int64_t hs = (layer * a.proj_steps + slot) * nheads + hl;   // (layer, step, b, h) flattened
+    rk[s] = live ? to_f32(k[hs * D + lane]) : 0.f;
+    rq[s] = live ? to_f32(q[hs * D + lane]) : 0.f;
+    rg[s] = live ? to_f32(g[hs * D + lane]) : 0.f;
+    rv[s] = live ? to_f32(v[hs * D + lane]) : 0.f;
+    rb[s] = live ? to_f32(beta[hs]) : 0.f;
+  }
+  // per-step row coefficients of the accepted steps
+  float kq[MAXS];
+  const bool df = a.mode == KDA_MODE_DECAY_FIRST;
+#pragma unroll
+  for (int s = 0; s < MAXS; ++s) {
+    if (s < n) {
+      const float e = expf(rg[s]);
+      float* c = reinterpret_cast<float*>(coef[w][s]);
+      c[lane] = df ? e * rk[s] : rk[s];
+      c[D + lane] = e * rq[s];
+      c[2 * D + lane] = e;
+      c[3 * D + lane] = rb[s] * rk[s];
+    }
+    kq[s] = rk[s] * rq[s];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {          // the steps' k.q butterflies, interleaved
+#pragma unroll
+    for (int s = 0; s < MAXS; ++s) kq[s] += __shfl_xor_sync(0xffffffffu, kq[s], off);
+  }
+  __syncwarp();
+  // ---- the accepted steps ----
+  T* out = reinterpret_cast<T*>(a.out);
+  T* orow = out + head * a.out_head_stride + lane;
+#pragma unroll
+  for (int s = 0; s < MAXS; ++s) {
+    if (s < n) {
+      const float4* cw = coef[w][s][0];
+      const float4* cq = coef[w][s][1];
+      const float4* ce = coef[w][s][2];
+      const float4* ck = coef[w][s][3];
+      // four independent chains per sum
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+#pragma unroll
+      for (int i4 = 0; i4 < D / 4; ++i4) {
+        const float4 x = cw[i4], y = cq[i4];
+        const int i = 4 * i4;
+        a0 = fmaf(x.x, S[i], a0); a1 = fmaf(x.y, S[i + 1], a1);
+        a2 = fmaf(x.z, S[i + 2], a2); a3 = fmaf(x.w, S[i + 3], a3);
+        b0 = fmaf(y.x, S[i], b0); b1 = fmaf(y.y, S[i + 1], b1);
+        b2 = fmaf(y.z, S[i + 2], b2); b3 = fmaf(y.w, S[i + 3], b3);
+      }
+      const float d = rv[s] - ((a0 + a1) + (a2 + a3));
+      const float o = fmaf(rb[s] * kq[s], d, (b0 + b1) + (b2 + b3));
+      orow[s * a.out_step_stride] = from_f32<T>(live_state ? o : 0.f);
+#pragma unroll
+      for (int i4 = 0; i4 < D / 4; ++i4) {
+        const float4 e4 = ce[i4], k4 = ck[i4];
+        const int i = 4 * i4;
+        S[i] = fmaf(e4.x, S[i], k4.x * d);
+        S[i + 1] = fmaf(e4.y, S[i + 1], k4.y * d);
+        S[i + 2] = fmaf(e4.z, S[i + 2], k4.z * d);
+        S[i + 3] = fmaf(e4.w, S[i + 3], k4.w * d);
+      }
+    }
+  }
+  // steps past the accepted prefix produce zero output rows
+  for (int s = n; s < a.steps; ++s) orow[s * a.out_step_stride] = from_f32<T>(0.f);
+  if (!live_state) return;
+  float* Sout = a.S_out + srow_out * (int64_t)(D * D);
+  if constexpr (TRANS) {
+#pragma unroll
+    for (int i = 0; i < D; i += 4)
+      *reinterpret_cast<float4*>(Sout + lane * D + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < D; ++i) Sout[i * D + lane] = S[i];
+  }
+}
+
+template <typename T, bool TRANS>
+cudaError_t launch_small(const StepArgs& a, cudaStream_t s) {
+  const int64_t heads = (int64_t)a.B * a.H * a.layers;
+  const unsigned grid = (unsigned)((heads + kSmallHPC - 1) / kSmallHPC);
+  if (a.steps <= 1) {
+    kda_step_small_kernel<T, TRANS, 1><<<grid, 32 * kSmallHPC, 0, s>>>(a);
+  } else if (a.steps <= 8) {
+    kda_step_small_kernel<T, TRANS, 8><<<grid, 32 * kSmallHPC, 0, s>>>(a);
+  } else {
+    kda_step_small_kernel<T, TRANS, KDA_MAX_DRAFT><<<grid, 32 * kSmallHPC, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
 template <int DK, int DV, typename T, bool TRANS, bool FUSED>
 cudaError_t launch_dims(const StepArgs& a, cudaStream_t s) {
+  if constexpr (DK == kSmallD && DV == kSmallD && !FUSED) return launch_small<T, TRANS>(a, s);
   // rows per thread 16 where the head is big enough; at least 128 threads per CTA
   constexpr int TPR = DV / 4;
   constexpr int NW0 = (DK * TPR) / (16 * 32);
