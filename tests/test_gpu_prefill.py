@@ -121,13 +121,30 @@ def chain_cols(K):
     K.kda_set_prefill_chain_columns(0)
 
 
-@pytest.mark.parametrize("cols", [0, 64])
-def test_long_prefill_sampled_heads(K, cols, chain_cols):
-    """B=1, H=32, dk=dv=128, T=8192, bf16, 16 checkpoints; heads 0, 13, 31 checked (chain CTA
-    width chosen per call, which takes 32-column slices here, and forced to 64)."""
-    chain_cols(cols)
+def _np(t):
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+@pytest.fixture(scope="module")
+def long_case():
+    """B=1, H=32, dk=dv=128, T=8192, bf16, checkpoints every 512 tokens: the inputs on the
+    device and the fp64 oracle of every head (one worker process per head)."""
+    from oracle_pool import prefill_chunked_per_head
     H, d, T, stride = 32, 128, 8192, 512
     S0, p, cu = I.prefill_inputs([T], H, d, d, dtype=torch.bfloat16, seed=0, device="cuda")
+    ref = prefill_chunked_per_head(_np(S0), *(_np(p[n]) for n in ("q", "k", "v", "g", "beta")), cu,
+                                   stride, range(H))
+    return S0, p, cu, ref
+
+
+@pytest.mark.parametrize("cols", [0, 64])
+def test_long_prefill_all_heads(K, cols, chain_cols, long_case):
+    """B=1, H=32, dk=dv=128, T=8192, bf16, 16 checkpoints: outputs, final state and all 16
+    checkpoint pages of every head against the fp64 oracle (chain CTA width chosen per call,
+    which takes 32-column slices here, and forced to 64)."""
+    chain_cols(cols)
+    S0, p, cu, ref = long_case
+    H, d, T, stride = 32, 128, 8192, 512
     n_ck = K.kda_num_checkpoints(cu, T, stride)
     assert n_ck == 16
     pool = K.PagePool(H * d * d * 4, n_ck)
@@ -137,21 +154,24 @@ def test_long_prefill_sampled_heads(K, cols, chain_cols):
                                      ckpt_stride=stride, page_pool=pool, ckpt_page_ids=ids,
                                      ckpt_pos=pos)
     torch.cuda.synchronize()
+    assert K.kda_device_errors() == 0
     assert pos.tolist() == [512 * j for j in range(1, 17)]
     assert torch.equal(pool.page(int(ids[-1])).reshape(1, H, d, d), S_fin)
-    for h in (0, 13, 31):
-        args = [f(S0[:, h:h + 1])] + [f(p[n][:, h:h + 1]) for n in ("q", "k", "v", "g", "beta")]
-        o_ref, S_ref, ck_ref = O.prefill_chunked(*args, cu_seqlens=cu, chunk=64, ckpt_stride=stride)
-        assert rel(o[:, h], o_ref[:, 0]) < TOL_BF16_OUT
-        assert rel(S_fin[0, h], S_ref[0, 0]) < TOL_BF16_STATE
-        for c in (0, 7, 15):
-            page = pool.page(int(ids[c])).reshape(H, d, d)
-            assert rel(page[h], ck_ref[c][2][0]) < TOL_BF16_STATE
+    pages = torch.stack([pool.page(int(ids[c])).reshape(H, d, d) for c in range(n_ck)])
+    for h in range(H):
+        o_ref, S_ref, ck_ref = ref[h]
+        assert rel(o[:, h], o_ref[:, 0]) < TOL_BF16_OUT, h
+        assert rel(S_fin[0, h], S_ref[0, 0]) < TOL_BF16_STATE, h
+        assert [t for _, t, _ in ck_ref] == pos.tolist()
+        for c in range(n_ck):
+            assert rel(pages[c, h], ck_ref[c][2][0]) < TOL_BF16_STATE, (h, c)
 
 
-def test_varlen_resume_sampled(K):
+def test_varlen_resume_longest_sequence_all_heads(K):
     """64 sequences, lengths log-uniform in [512, 32768] (multiples of 64), H=32, dk=dv=128, bf16,
-    S0 ~ N(0, 0.05), checkpoints every 512 tokens; three (sequence, head) pairs checked."""
+    S0 ~ N(0, 0.05), checkpoints every 512 tokens: every head of the longest sequence (outputs,
+    final state, every checkpoint page) and one head each of the shortest and the median."""
+    from oracle_pool import prefill_chunked_per_head
     H, d, stride = 32, 128, 512
     lengths = I.varlen_lengths(64, seed=0)
     S0, p, cu = I.prefill_inputs(lengths, H, d, d, dtype=torch.bfloat16, seed=0, device="cuda")
@@ -165,19 +185,28 @@ def test_varlen_resume_sampled(K):
                                      ckpt_stride=stride, page_pool=pool, ckpt_page_ids=ids,
                                      ckpt_pos=pos)
     torch.cuda.synchronize()
+    assert K.kda_device_errors() == 0
     expect = [t for L in lengths for t in O.checkpoint_positions(L, stride)]
     assert pos.tolist() == expect
     order = np.argsort(lengths)
     base = np.concatenate([[0], np.cumsum([L // stride for L in lengths])])
-    for n, h in ((int(order[0]), 5), (int(order[32]), 20), (int(order[-1]), 31)):
+
+    def check(n, heads):
         a, b = cu[n], cu[n + 1]
-        args = [f(S0[n:n + 1, h:h + 1])] + [f(p[x][a:b, h:h + 1]) for x in ("q", "k", "v", "g", "beta")]
-        o_ref, S_ref, ck_ref = O.prefill_chunked(*args, cu_seqlens=None, chunk=64, ckpt_stride=stride)
-        assert rel(o[a:b, h], o_ref[:, 0]) < TOL_BF16_OUT
-        assert rel(S_fin[n, h], S_ref[0, 0]) < TOL_BF16_STATE
-        for j in sorted({0, len(ck_ref) - 1}):
-            page = pool.page(int(ids[base[n] + j])).reshape(H, d, d)
-            assert rel(page[h], ck_ref[j][2][0]) < TOL_BF16_STATE
+        ins = [_np(S0[n:n + 1])] + [_np(p[x][a:b]) for x in ("q", "k", "v", "g", "beta")]
+        ref = prefill_chunked_per_head(*ins, None, stride, heads)
+        for h in heads:
+            o_ref, S_ref, ck_ref = ref[h]
+            assert rel(o[a:b, h], o_ref[:, 0]) < TOL_BF16_OUT, (n, h)
+            assert rel(S_fin[n, h], S_ref[0, 0]) < TOL_BF16_STATE, (n, h)
+            assert len(ck_ref) == lengths[n] // stride
+            for j in range(len(ck_ref)):
+                page = pool.page(int(ids[base[n] + j])).reshape(H, d, d)
+                assert rel(page[h], ck_ref[j][2][0]) < TOL_BF16_STATE, (n, h, j)
+
+    check(int(order[-1]), range(H))                       # the longest sequence, every head
+    check(int(order[0]), [5])
+    check(int(order[32]), [20])
 
 
 # ---------------------------------------------------------------------------
