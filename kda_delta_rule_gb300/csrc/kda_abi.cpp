@@ -339,6 +339,7 @@ int kda_device_errors(int* flags) {
   int e = kda::read_and_clear_device_errors(flags);
   if (e == 0) e = kda::read_and_clear_prologue_errors(flags);
   if (e == 0) e = kda::read_and_clear_simt_errors(flags);
+  if (e == 0) e = kda::read_and_clear_scan_errors(flags);
   if (e != 0) return cuda_status((cudaError_t)e, "kda_device_errors");
   return ok();
 }

@@ -130,6 +130,8 @@ cudaError_t launch_prefill_tc_scan(const PrefillArgs& a, int64_t len, int segmen
 int read_and_clear_device_errors(int* flags);
 // OR the CUDA-core prefill kernel's error word into *flags and clear it.
 int read_and_clear_simt_errors(int* flags);
+// OR the sequence-parallel scan kernel's error word into *flags and clear it.
+int read_and_clear_scan_errors(int* flags);
 // Record a failure message for kda_last_error() and return `status`.
 int set_error(int status, const char* msg);
 // The host-side argument checks of kda_prefill_chunked (everything but the

@@ -12,13 +12,17 @@
 //      1 .. P-2 its local state L_j (zero start) and its transition M_j, run as
 //      dk / dv pseudo-sequences with the beta U term dropped, each starting from a
 //      block of dv columns of the identity (their final states are M_j's columns).
-//   3. The scan X_{j+1} = M_j X_j + L_j in fp32 (one CTA per head and 32 columns).
+//   3. The scan X_{j+1} = M_j X_j + L_j on the tensor cores (tf32 products with X
+//      split into a tf32 part and its fp32 remainder, fp32 accumulation; one CTA per
+//      head and 32 columns).
 //   4. One chain launch over segments 1 .. P-1 from their starts X_j: outputs,
 //      checkpoints, and the last segment's final state.
 // Steps 2 and 4 each run a 1/P-long chain per (pseudo-)sequence in parallel, so a
 // sequence whose heads occupy few SMs finishes in about 2/P of the serial chain's
 // time; the prep is shared.
 #include "kda_internal.h"
+#include "kda_tc.cuh"
+#include "kda_tmap.h"
 #include "../../include/kda.h"
 
 #include <algorithm>
@@ -71,85 +75,179 @@ __global__ void scan_init_kernel(const float* __restrict__ S0, float* __restrict
   }
 }
 
-// X_1 = segment 0's final state; X_{j+1} = M_j X_j + L_j for j = 1 .. P-2.
-// One CTA of 256 threads per (head, 32 state columns); X block [DK][32] and M_j
-// transposed, [k][i], in shared memory; each thread a 4 x 4 block (rows 4 ti ..,
-// columns 4 tc ..): per k one 16-byte read of X's row k and one of M_j's column k
-// feed 16 FMAs.
-constexpr int SCAN_NT = 256;
+// X_1 = segment 0's final state; X_{j+1} = M_j X_j + L_j for j = 1 .. P-2, on the
+// tensor cores.  One CTA of 128 threads per (head, 32 state columns); thread i owns
+// row i.  M_j (fp32, DK x DK) is brought by TMA as the K-major A operand of a
+// kind::tf32 product (boxes of 32 columns x 128 rows, 128-byte swizzle), one step
+// ahead into a two-stage buffer.  X_j is the MN-major B operand (32 columns of
+// 128 bytes per K row) in two parts, X_hi = X rounded to tf32 and X_lo = X - X_hi,
+// so D = M_j X_hi + M_j X_lo keeps X at fp32 precision (M_j enters at tf32,
+// relative 2^-11); D accumulates in TMEM (128 lanes x 32 columns), and the
+// readback adds L_j.
+constexpr int SCAN_NT = 128;
+constexpr uint32_t SC_M = 0;                    // 2 x 64 KB: M_j, M_{j+1}
+constexpr uint32_t SC_XH = 131072;              // 16 KB: X_hi, MN-major (mn = 32 columns, K = 128 rows)
+constexpr uint32_t SC_XL = SC_XH + 16384;       // 16 KB: X_lo
+constexpr uint32_t SC_MISC = SC_XL + 16384;     // mbarriers, TMEM slot
+constexpr uint32_t SC_SMEM = SC_MISC + 64 + 1024;
+
+// tf32 x tf32 -> fp32, A K-major, B MN-major
+__host__ __device__ constexpr uint32_t scan_idesc(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (1u << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_tf32_w(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p, e; .reg .b32 r; elect.sync r|e, 0xffffffff; setp.ne.b32 p, %4, 0; "
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p; }"
+      :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ float tf32_round(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+// byte offset of (K row k, column c) in an MN-major 4-byte tile of 32 columns
+__device__ __forceinline__ uint32_t off_x(int k, int c) {
+  return (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((c >> 2) ^ (k & 7))) << 4) + (c & 3) * 4);
+}
+
 template <int DK>
-__global__ void __launch_bounds__(SCAN_NT) scan_kernel(const float* __restrict__ SfA, float* __restrict__ XC, int H,
-                                                       int dv, int P, int nb) {
-  static_assert(DK / 4 * 8 == SCAN_NT, "one thread per 4 x 4 block of a DK x 32 tile");
-  extern __shared__ float4 scan_smem4[];
-  float* Xs = reinterpret_cast<float*>(scan_smem4);        // [DK][32]
-  float* MT = Xs + DK * 32;                                // [DK (k)][DK (i)]
-  const int h = blockIdx.x, c0 = blockIdx.y * 32, tid = threadIdx.x;
-  const int tc = tid & 7, ti = tid >> 3;                   // column group, row group
+__global__ void __launch_bounds__(SCAN_NT, 1) scan_kernel(const __grid_constant__ CUtensorMap mmap,
+                                                          const float* __restrict__ SfA, float* __restrict__ XC,
+                                                          int H, int dv, int P, int nb) {
+  static_assert(DK == SCAN_NT, "one thread per state row");
+  using namespace tc;
+  extern __shared__ unsigned char scan_smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(((uintptr_t)scan_smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t mbar_m = smem_u32(sm + SC_MISC);          // two M stages landed
+  const uint32_t mbar_d = smem_u32(sm + SC_MISC + 16);     // product done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SC_MISC + 32);
+  const int h = blockIdx.x, c0 = blockIdx.y * 32, i = threadIdx.x, warp = i >> 5;
   const int64_t HS = (int64_t)H * DK * dv;
-  for (int e = tid; e < DK * 32; e += SCAN_NT) {
-    const int i = e >> 5, cc = e & 31;
-    const int64_t off = ((int64_t)h * DK + i) * dv + c0 + cc;
-    const float x = SfA[off];
-    Xs[e] = x;
-    XC[off] = x;
-  }
-  __syncthreads();
-  // M_j as float4s along k (row i, columns k .. k + 3), consecutive threads on
-  // consecutive rows so that the transposed stores hit distinct banks; the loads of
-  // M_{j+1} are in flight while step j computes
-  constexpr int NM = DK * DK / 4 / SCAN_NT;
-  float4 mv[NM];
-  auto load_m = [&](int j) {
+  constexpr uint32_t ID = scan_idesc(128, 32);
+
+  // the M_j boxes: K block kb (columns 32 kb ..) is column block b = 32 kb / dv of
+  // the transition's pseudo-sequences, at column 32 kb % dv
+  auto load_m = [&](int j, int st) {
     const int64_t ls = 1 + (int64_t)(j - 1) * (1 + nb);
+    const uint32_t mb = mbar_m + 8 * st;
+    mbar_expect_tx(mb, DK * DK * 4);
 #pragma unroll
-    for (int u = 0; u < NM; ++u) {
-      const int e = tid + SCAN_NT * u, i = e % DK, k = 4 * (e / DK), b = k / dv;
-      mv[u] = *reinterpret_cast<const float4*>(SfA + (ls + 1 + b) * HS + ((int64_t)h * DK + i) * dv + (k - b * dv));
+    for (int kb = 0; kb < DK / 32; ++kb) {
+      const int b = 32 * kb / dv, x = 32 * kb % dv;
+      tma_load_2d(smem_u32(sm + SC_M + st * 65536 + kb * 16384), &mmap, x, (int)((ls + 1 + b) * H + h) * DK, mb);
     }
   };
-  if (P >= 3) load_m(1);
-  for (int j = 1; j <= P - 2; ++j) {
-    const int64_t ls = 1 + (int64_t)(j - 1) * (1 + nb);    // slot of L_j; M_j's column blocks follow
+  auto put_x = [&](const float (&x)[32]) {
 #pragma unroll
-    for (int u = 0; u < NM; ++u) {
-      const int e = tid + SCAN_NT * u, i = e % DK, k = 4 * (e / DK);
-      MT[(k + 0) * DK + i] = mv[u].x;
-      MT[(k + 1) * DK + i] = mv[u].y;
-      MT[(k + 2) * DK + i] = mv[u].z;
-      MT[(k + 3) * DK + i] = mv[u].w;
+    for (int q = 0; q < 8; ++q) {
+      float hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hi[e] = tf32_round(x[4 * q + e]);
+        lo[e] = x[4 * q + e] - hi[e];
+      }
+      *reinterpret_cast<float4*>(sm + SC_XH + off_x(i, 4 * q)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<float4*>(sm + SC_XL + off_x(i, 4 * q)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
     }
-    float acc[4][4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float4 l4 = *reinterpret_cast<const float4*>(SfA + ls * HS + ((int64_t)h * DK + 4 * ti + r) * dv + c0 +
-                                                         4 * tc);
-      acc[r][0] = l4.x; acc[r][1] = l4.y; acc[r][2] = l4.z; acc[r][3] = l4.w;
-    }
-    __syncthreads();
-    if (j + 1 <= P - 2) load_m(j + 1);
-#pragma unroll 8
-    for (int k = 0; k < DK; ++k) {
-      const float4 x4 = *reinterpret_cast<const float4*>(Xs + k * 32 + 4 * tc);
-      const float4 m4 = *reinterpret_cast<const float4*>(MT + k * DK + 4 * ti);
-      const float mr[4] = {m4.x, m4.y, m4.z, m4.w}, xc[4] = {x4.x, x4.y, x4.z, x4.w};
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(mr[r], xc[q], acc[r][q]);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float4 o4 = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      *reinterpret_cast<float4*>(Xs + (4 * ti + r) * 32 + 4 * tc) = o4;
-      *reinterpret_cast<float4*>(XC + (int64_t)j * HS + ((int64_t)h * DK + 4 * ti + r) * dv + c0 + 4 * tc) = o4;
-    }
-    __syncthreads();
+  };
+
+  if (i == 0) {
+    mbar_init(mbar_m, 1);
+    mbar_init(mbar_m + 8, 1);
+    mbar_init(mbar_d, 1);
+    mbar_init_fence();
   }
+  if (warp == 0) tmem_alloc(smem_u32(tslot), 32);
+  float x[32];
+  {
+    const int64_t off = ((int64_t)h * DK + i) * dv + c0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(SfA + off + 4 * q);
+      x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
+      *reinterpret_cast<float4*>(XC + off + 4 * q) = v;
+    }
+  }
+  put_x(x);
+  fence_async_smem();
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tslot;
+  int issued = 0;                                          // M loads issued (thread 0)
+  if (i == 0 && P >= 3) { load_m(1, 0); issued = 1; }
+  bool ok = true;
+  for (int j = 1; j <= P - 2 && ok; ++j) {
+    const int st = (j - 1) & 1;
+    const int64_t ls = 1 + (int64_t)(j - 1) * (1 + nb);
+    float l[32];
+    const int64_t lo_off = ls * HS + ((int64_t)h * DK + i) * dv + c0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(SfA + lo_off + 4 * q);
+      l[4 * q] = v.x; l[4 * q + 1] = v.y; l[4 * q + 2] = v.z; l[4 * q + 3] = v.w;
+    }
+    // the next transition into the other stage (its last reader, step j - 1's
+    // product, is complete)
+    if (i == 0 && j + 1 <= P - 2) { load_m(j + 1, st ^ 1); issued = j + 1; }
+    if (warp == 0) {
+      const bool landed = __all_sync(0xffffffffu, mbar_wait(mbar_m + 8 * st, (uint32_t)(((j - 1) >> 1) & 1)));
+      if (landed) {
+        fence_after();
+        const uint32_t mb = smem_u32(sm + SC_M + st * 65536);
+        const uint32_t xh = smem_u32(sm + SC_XH), xl = smem_u32(sm + SC_XL);
+#pragma unroll
+        for (int k = 0; k < DK / 8; ++k)
+          mma_tf32_w(tmem, desc_k(mb, 128, k), desc_sw128(xh + 1024 * k, DK * 128, 1024), ID, k > 0);
+#pragma unroll
+        for (int k = 0; k < DK / 8; ++k)
+          mma_tf32_w(tmem, desc_k(mb, 128, k), desc_sw128(xl + 1024 * k, DK * 128, 1024), ID, 1);
+        mma_commit_w(mbar_d);
+      }
+      ok = landed;
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) break;
+    ok = __syncthreads_and(mbar_wait(mbar_d, (uint32_t)((j - 1) & 1))) != 0;
+    if (!ok) break;
+    fence_after();
+    float d[32];
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), d);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[e] = d[e] + l[e];
+    const int64_t off = (int64_t)j * HS + ((int64_t)h * DK + i) * dv + c0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(XC + off + 4 * q) = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    put_x(x);
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+  }
+  if (i == 0 && !ok) {
+    // leave no copy in flight into this CTA's shared memory: the last load of each
+    // stage (bounded waits; a phase already seen returns at once)
+    for (int jj = max(1, issued - 1); jj <= issued; ++jj)
+      mbar_wait(mbar_m + 8 * ((jj - 1) & 1), (uint32_t)(((jj - 1) >> 1) & 1));
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 32);
 }
 
 }  // namespace
+
+// OR the scan kernel's device error word (its bounded waits) into *flags and clear it.
+int read_and_clear_scan_errors(int* flags) {
+  int word = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&word, tc::g_kda_device_error, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(tc::g_kda_device_error, &zero, sizeof(int));
+  *flags |= word;
+  return (int)e;
+}
 
 // The segment count asked of make_plan when the caller leaves it open: the most
 // segments whose first chain launch still fits one CTA per SM.
@@ -218,10 +316,11 @@ cudaError_t launch_prefill_tc_scan(const PrefillArgs& a, int64_t len, int segmen
 
   // ---- scan of the segment starts ----
   auto kern = scan_kernel<128>;                            // the tensor-core chain has dk = 128
-  const int smem = (a.dk * 32 + a.dk * a.dk) * 4;
-  if (smem > 48 * 1024 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+  CUtensorMap mmap;                                        // the transitions' states as [rows][dv] fp32
+  if (!make_map_2d(&mmap, SfA, (int64_t)p.nA * a.H * a.dk, a.dv, 4, 32, 128, true)) return cudaErrorInvalidValue;
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_SMEM)) != cudaSuccess)
     return e;
-  kern<<<dim3(a.H, a.dv / 32), SCAN_NT, smem, s>>>(SfA, XC, a.H, a.dv, p.P, p.nb);
+  kern<<<dim3(a.H, a.dv / 32), SCAN_NT, SC_SMEM, s>>>(mmap, SfA, XC, a.H, a.dv, p.P, p.nb);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // ---- second chain launch: segments 1 .. P-1 from their starts ----

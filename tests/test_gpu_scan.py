@@ -36,6 +36,7 @@ def _scan(K, T, H, dv, stride, segments, mode=0, seed=0, S0_none=False):
                                 page_pool=pool if n_ck else None, ckpt_page_ids=ids if n_ck else None,
                                 ckpt_pos=pos if n_ck else None, segments=segments, mode=mode)
     torch.cuda.synchronize()
+    assert K.kda_device_errors() == 0
     S0_ref = np.zeros((1, H, dk, dv)) if S0_none else f(S0)
     o_ref, S_ref, ck_ref = O.prefill_recurrent(S0_ref, *(f(p[n]) for n in ("q", "k", "v", "g", "beta")),
                                                ckpt_stride=stride, mode=mode)
@@ -89,3 +90,35 @@ def test_scan_long_sequence_sampled_against_plain_chain(K):
         hd = {n: f(p[n][:, h]) for n in ("q", "k", "v", "g", "beta")}
         _, S_ref = O.kda_recurrent(f(S0[0, h]), hd["q"], hd["k"], hd["v"], hd["g"], hd["beta"])
         assert rel(S1[0, h], S_ref) < TOL_BF16_STATE
+
+
+def test_scan_32_heads_every_head_against_oracle(K):
+    """H = 32, dk = dv = 128 (the long-prefill head count), T = 4096 cut into 4 pieces, checkpoints
+    every 512: outputs, final state and every checkpoint page of every head against the fp64
+    oracle, one worker process per head.  The first chain launch here has 5 pseudo-sequences x
+    32 heads of CTAs (several waves), the tensor-core scan 32 x 4 CTAs."""
+    from oracle_pool import prefill_chunked_per_head
+    T, H, d, stride = 4096, 32, 128, 512
+    S0, p, cu = I.prefill_inputs([T], H, d, d, dtype=torch.bfloat16, seed=31, device="cuda")
+    n_ck = K.kda_num_checkpoints(cu, T, stride)
+    pool = K.PagePool(H * d * d * 4, n_ck)
+    ids = torch.tensor(pool.alloc(n_ck), dtype=torch.int32, device="cuda")
+    pos = torch.full((n_ck,), -1, dtype=torch.int32, device="cuda")
+    o, S_f = K.kda_prefill_scan(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], ckpt_stride=stride, page_pool=pool,
+                                ckpt_page_ids=ids, ckpt_pos=pos, segments=4)
+    torch.cuda.synchronize()
+    assert K.kda_device_errors() == 0
+    assert pos.tolist() == [stride * j for j in range(1, n_ck + 1)]
+
+    def np32(t):
+        return t.detach().to("cpu", torch.float32).numpy()
+
+    ref = prefill_chunked_per_head(np32(S0), *(np32(p[n]) for n in ("q", "k", "v", "g", "beta")), cu, stride,
+                                   range(H))
+    pages = torch.stack([pool.page(int(ids[c])).reshape(H, d, d) for c in range(n_ck)])
+    for h in range(H):
+        o_ref, S_ref, ck_ref = ref[h]
+        assert rel(o[:, h], o_ref[:, 0]) < TOL_BF16_OUT, h
+        assert rel(S_f[0, h], S_ref[0, 0]) < TOL_BF16_STATE, h
+        for c in range(n_ck):
+            assert rel(pages[c, h], ck_ref[c][2][0]) < TOL_BF16_STATE, (h, c)
