@@ -10,6 +10,7 @@
     python -m kda_delta_rule_gb300.cases decode_vk    [--reps N]   # decode on 256 of 512 transposed pool slots
     python -m kda_delta_rule_gb300.cases decode_fused [--reps N]   # decode with the input prologue, B=256
     python -m kda_delta_rule_gb300.cases scan     [--reps N]   # sequence-parallel prefill, T=65536 H=4 d=128
+    python -m kda_delta_rule_gb300.cases scan32   [--reps N]   # the same at T=8192 H=32 d=128, 4 pieces
 
 Each case prints the mean device time per call measured with CUDA events.
 """
@@ -131,17 +132,22 @@ def case_decode_fused(reps, H=32, d=128, B=256, w=4):
                                                  raw["beta_logits"], o=o), reps)
 
 
-def case_scan(reps, T=65536, H=4, d=128):
+def case_scan(reps, T=65536, H=4, d=128, segments=0):
     S0, p, cu = I.prefill_inputs([T], H, d, d, dtype=torch.bfloat16, seed=0, device="cuda")
-    ws = torch.empty(K.kda_prefill_scan_workspace_bytes(T, H, d, d, torch.bfloat16, 0, 0), dtype=torch.uint8,
+    ws = torch.empty(K.kda_prefill_scan_workspace_bytes(T, H, d, d, torch.bfloat16, 0, segments), dtype=torch.uint8,
                      device="cuda")
     o = torch.empty(T, H, d, dtype=torch.bfloat16, device="cuda")
     Sf = torch.empty_like(S0)
     return _time(lambda: K.kda_prefill_scan(S0, p["q"], p["k"], p["v"], p["g"], p["beta"], ckpt_stride=0, o=o,
-                                            S_final=Sf, workspace=ws), reps)
+                                            S_final=Sf, segments=segments, workspace=ws), reps)
 
 
-CASES = {"scan": case_scan, "decode": case_decode, "replay": case_replay, "prefill": case_prefill,
+def case_scan32(reps):
+    """The sequence-parallel path at the long-prefill shape (T=8192, H=32), four pieces."""
+    return case_scan(reps, T=8192, H=32, segments=4)
+
+
+CASES = {"scan": case_scan, "scan32": case_scan32, "decode": case_decode, "replay": case_replay, "prefill": case_prefill,
          "varlen": case_varlen, "pack": case_pack, "layer": case_layer, "prologue": case_prologue, "decode_vk": case_decode_vk,
          "decode_fused": case_decode_fused}
 

@@ -152,6 +152,9 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   const __nv_bfloat16* bg = reinterpret_cast<const __nv_bfloat16*>(a.beta);
 
   if (tid == 0) {
+    // the chain launch that follows may start its CTAs once every prep CTA has
+    // begun; it reads nothing of this grid before its grid-dependency wait
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     mbar_init(mbar, 1);
     mbar_init(mbar_in, 1);
     mbar_init(mbar_v, 1);
@@ -666,6 +669,9 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     mbar_init_fence();
   }
   if (warp == PRODUCER) tmem_alloc(smem_u32(tslot), 256);
+  // launched as a programmatic dependent of the preceding kernel (the prep, or the
+  // scan kernel that makes S0): everything below may read what it wrote
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // zero rows 0-63 of both [0; P] buffers (never written by the copies)
   for (int e = tid; e < 2 * 512; e += CNT) {
     const int s = e >> 9, o = e & 511;
@@ -1010,7 +1016,21 @@ cudaError_t launch_chain_cols(const PrefillArgs& a, const PrefillSched& sched, c
   auto chain = kda_chain_kernel<DV, DVS>;
   cudaError_t e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C_SMEM);
   if (e != cudaSuccess) return e;
-  chain<<<dim3(DV / DVS, a.H, sched.n_seqs), CNT, C_SMEM, s>>>(a, sched, ws);
+  // programmatic dependent launch: the chain's CTAs may be scheduled while the
+  // preceding kernel's last CTAs run; each waits (griddepcontrol.wait) before it
+  // reads any memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(DV / DVS, a.H, sched.n_seqs);
+  cfg.blockDim = dim3(CNT);
+  cfg.dynamicSmemBytes = C_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, chain, a, sched, ws);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
