@@ -81,13 +81,13 @@ __global__ void scan_init_kernel(const float* __restrict__ S0, float* __restrict
 // kind::tf32 product (boxes of 32 columns x 128 rows, 128-byte swizzle), one step
 // ahead into a two-stage buffer.  X_j is the MN-major B operand (32 columns of
 // 128 bytes per K row) in two parts, X_hi = X rounded to tf32 and X_lo = X - X_hi,
-// so D = M_j X_hi + M_j X_lo keeps X at fp32 precision (M_j enters at tf32,
-// relative 2^-11); D accumulates in TMEM (128 lanes x 32 columns), and the
-// readback adds L_j.
+// side by side as one N = 64 operand (two 128-byte atoms), so one product gives
+// M_j X_hi and M_j X_lo in TMEM columns 0-31 and 32-63 and their sum keeps X at
+// fp32 precision (M_j enters at tf32, relative 2^-11); the readback adds L_j.
 constexpr int SCAN_NT = 128;
 constexpr uint32_t SC_M = 0;                    // 2 x 64 KB: M_j, M_{j+1}
 constexpr uint32_t SC_XH = 131072;              // 16 KB: X_hi, MN-major (mn = 32 columns, K = 128 rows)
-constexpr uint32_t SC_XL = SC_XH + 16384;       // 16 KB: X_lo
+constexpr uint32_t SC_XL = SC_XH + 16384;       // 16 KB: X_lo, the operand's second MN atom
 constexpr uint32_t SC_MISC = SC_XL + 16384;     // mbarriers, TMEM slot
 constexpr uint32_t SC_SMEM = SC_MISC + 64 + 1024;
 
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(SCAN_NT, 1) scan_kernel(const __grid_constant_
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SC_MISC + 32);
   const int h = blockIdx.x, c0 = blockIdx.y * 32, i = threadIdx.x, warp = i >> 5;
   const int64_t HS = (int64_t)H * DK * dv;
-  constexpr uint32_t ID = scan_idesc(128, 32);
+  constexpr uint32_t ID = scan_idesc(128, 64);
 
   // the M_j boxes: K block kb (columns 32 kb ..) is column block b = 32 kb / dv of
   // the transition's pseudo-sequences, at column 32 kb % dv
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(SCAN_NT, 1) scan_kernel(const __grid_constant_
     mbar_init(mbar_d, 1);
     mbar_init_fence();
   }
-  if (warp == 0) tmem_alloc(smem_u32(tslot), 32);
+  if (warp == 0) tmem_alloc(smem_u32(tslot), 64);
   float x[32];
   {
     const int64_t off = ((int64_t)h * DK + i) * dv + c0;
@@ -196,13 +196,11 @@ __global__ void __launch_bounds__(SCAN_NT, 1) scan_kernel(const __grid_constant_
       if (landed) {
         fence_after();
         const uint32_t mb = smem_u32(sm + SC_M + st * 65536);
-        const uint32_t xh = smem_u32(sm + SC_XH), xl = smem_u32(sm + SC_XL);
+        const uint32_t xh = smem_u32(sm + SC_XH);
+        // B: [X_hi | X_lo], the second 128-byte MN atom LBO = SC_XL - SC_XH bytes on
 #pragma unroll
         for (int k = 0; k < DK / 8; ++k)
-          mma_tf32_w(tmem, desc_k(mb, 128, k), desc_sw128(xh + 1024 * k, DK * 128, 1024), ID, k > 0);
-#pragma unroll
-        for (int k = 0; k < DK / 8; ++k)
-          mma_tf32_w(tmem, desc_k(mb, 128, k), desc_sw128(xl + 1024 * k, DK * 128, 1024), ID, 1);
+          mma_tf32_w(tmem, desc_k(mb, 128, k), desc_sw128(xh + 1024 * k, SC_XL - SC_XH, 1024), ID, k > 0);
         mma_commit_w(mbar_d);
       }
       ok = landed;
@@ -212,10 +210,11 @@ __global__ void __launch_bounds__(SCAN_NT, 1) scan_kernel(const __grid_constant_
     ok = __syncthreads_and(mbar_wait(mbar_d, (uint32_t)((j - 1) & 1))) != 0;
     if (!ok) break;
     fence_after();
-    float d[32];
+    float d[32], dl[32];
     tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), d);
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32, dl);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) x[e] = d[e] + l[e];
+    for (int e = 0; e < 32; ++e) x[e] = (d[e] + dl[e]) + l[e];
     const int64_t off = (int64_t)j * HS + ((int64_t)h * DK + i) * dv + c0;
 #pragma unroll
     for (int q = 0; q < 8; ++q)
@@ -235,7 +234,7 @@ __global__ void __launch_bounds__(SCAN_NT, 1) scan_kernel(const __grid_constant_
   fence_before();
   __syncthreads();
   fence_after();
-  if (warp == 0) tmem_dealloc(tmem, 32);
+  if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 }  // namespace
