@@ -661,8 +661,8 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     mbar_init(bar1, 1);
     mbar_init(bar3, 1);
     mbar_init(bar2, 1);
-    mbar_init(free0, 1);
-    mbar_init(free0 + 8, 1);
+    mbar_init(free0, 9);                 // the products' commit and the eight row warps
+    mbar_init(free0 + 8, 9);
     mbar_init(ckfull, 8);
     mbar_init(ckfree, 1);
     *s_abort = 0;
@@ -781,7 +781,6 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
     const uint64_t dP0 = desc_k(smem_u32(sm + S_PB), 128, 0), dP1 = desc_k(smem_u32(sm + STAGE + S_PB), 128, 0);
     // products issued by warp 0 (all lanes run these; one elected lane issues)
     int last1 = -1, last32 = -1;           // last chunk whose MMA1 / MMA3+MMA2 were issued (warp 0)
-    int last_free = -1;                    // last chunk whose stage-release commit was issued (warp 0)
     auto mma1 = [&](auto stage_tag, int cidx) {
       constexpr int s = decltype(stage_tag)::value;
       const uint64_t dW = s ? dW1 : dW0;
@@ -800,6 +799,9 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
 #pragma unroll
       for (int j = 0; j < 4; ++j) mma_w(tmem + 64u * s, dP + (uint64_t)(2 * j), dD + (uint64_t)(128 * j), ID_1, 1);
       mma_commit_w(bar2);
+      // every product reading this stage is issued: their completion is the first
+      // release arrival of the stage (the row warps give the other eight)
+      mma_commit_w(free0 + 8 * s);
       last32 = cidx;
     };
     // outputs of chunk cc: rows 64-127 of d1[cc & 1] (warps 2, 3, 6, 7); the buffer is
@@ -838,6 +840,12 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       // shared-memory inputs of this chunk's row work, loaded before the waits
       // on the products
       const float eg = good ? reinterpret_cast<const float*>(st + S_EG)[i] : 0.f;
+      // this warp's last read of the stage: its release arrival, so the copy of
+      // chunk c + 2 can start once the products are done as well
+      auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(free0 + 8 * s);
+      };
       if (qd < 2) {                         // Delta' = beta U - beta W S, token row r
         const int r = i;
         const uint4* urow = reinterpret_cast<const uint4*>(st + S_U + r * 128);
@@ -846,6 +854,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
 #pragma unroll
         for (int cc = 0; cc < NC / 8; ++cc)
           u[cc] = good && use_u ? urow[(cb0 + cc) ^ (r & 7)] : make_uint4(0u, 0u, 0u, 0u);
+        release();
         good = good && warp_wait(bar1, ph, s_abort);
         if (good) {
           fence_after();
@@ -874,10 +883,11 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
           fence_after();
           mma32(stage_tag, c);
         }
-      } else if (c > 0) {
+      } else {
+        release();
         // the previous chunk's outputs, read while Delta' is formed: this chunk's
         // MMA1 is complete first, so the tensor pipe is idle meanwhile
-        good = good && warp_wait(bar1, ph, s_abort) && read_outputs(c - 1, false);
+        if (c > 0) good = good && warp_wait(bar1, ph, s_abort) && read_outputs(c - 1, false);
       }
       // state update: S_i <- e^{Gamma_C,i} S_i + (Kbar^T Delta')_i
       good = good && warp_wait(bar3, ph, s_abort);
@@ -927,11 +937,7 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       }
       if (warp == 0) {
         fence_after();
-        // every product reading stage s has been issued and the row warps are
-        // through it: the commit hands the stage back to the copy warp once the
-        // products are complete; then the next chunk's MMA1 goes in
-        mma_commit_w(free0 + 8 * s);
-        last_free = c;
+        // the next chunk's MMA1
         if (c + 1 < nch) {
           if (warp_wait(full0 + 8 * (s ^ 1), (uint32_t)(((c + 1) >> 1) & 1), s_abort)) {
             fence_after();
@@ -959,7 +965,6 @@ kda_chain_kernel(const PrefillArgs a, const PrefillSched sched, const unsigned c
       // returns at once)
       if (last1 >= 0) mbar_wait(bar1, (uint32_t)(last1 & 1));
       if (last32 >= 0) { mbar_wait(bar3, (uint32_t)(last32 & 1)); mbar_wait(bar2, (uint32_t)(last32 & 1)); }
-      if (last_free >= 0) mbar_wait(free0 + 8 * (last_free & 1), (uint32_t)((last_free >> 1) & 1));
     }
   }
   fence_before();
