@@ -537,6 +537,11 @@ __global__ void __launch_bounds__(32 * kSmallHPC)
 kda_step_small_kernel(const StepArgs a) {
   constexpr int D = kSmallD;
   __shared__ float4 coef[kSmallHPC][MAXS][4][D / 4];   // per step: w, e^g q, e^g, beta k (rows 0..31)
+  // launched as a programmatic dependent of the preceding kernel: the next launch
+  // may be placed at once, and nothing is read before the preceding kernel's
+  // writes are complete and visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t nheads = (int64_t)a.B * a.H;
   const int64_t head = (int64_t)blockIdx.x * kSmallHPC + w;   // over all stacked layers
@@ -668,14 +673,33 @@ kda_step_small_kernel(const StepArgs a) {
 template <typename T, bool TRANS>
 cudaError_t launch_small(const StepArgs& a, cudaStream_t s) {
   const int64_t heads = (int64_t)a.B * a.H * a.layers;
-  const unsigned grid = (unsigned)((heads + kSmallHPC - 1) / kSmallHPC);
-  if (a.steps <= 1) {
-    kda_step_small_kernel<T, TRANS, 1><<<grid, 32 * kSmallHPC, 0, s>>>(a);
-  } else if (a.steps <= 8) {
-    kda_step_small_kernel<T, TRANS, 8><<<grid, 32 * kSmallHPC, 0, s>>>(a);
-  } else {
-    kda_step_small_kernel<T, TRANS, KDA_MAX_DRAFT><<<grid, 32 * kSmallHPC, 0, s>>>(a);
+  // programmatic dependent launch on an eager stream: back-to-back calls overlap
+  // one kernel's launch with the previous one's run (each waits on the grid
+  // dependency before its first read).  Inside a stream capture the plain launch
+  // is kept: replayed graphs pipeline their kernel nodes better without it.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    cap = cudaStreamCaptureStatusActive;
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((heads + kSmallHPC - 1) / kSmallHPC));
+  cfg.blockDim = dim3(32 * kSmallHPC);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cap == cudaStreamCaptureStatusNone ? 1 : 0;
+  cudaError_t e;
+  if (a.steps <= 1) {
+    e = cudaLaunchKernelEx(&cfg, kda_step_small_kernel<T, TRANS, 1>, a);
+  } else if (a.steps <= 8) {
+    e = cudaLaunchKernelEx(&cfg, kda_step_small_kernel<T, TRANS, 8>, a);
+  } else {
+    e = cudaLaunchKernelEx(&cfg, kda_step_small_kernel<T, TRANS, KDA_MAX_DRAFT>, a);
+  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
