@@ -238,6 +238,9 @@ __device__ __forceinline__ void fused_compute(const StepArgs& a, const FusedIn<D
 template <int DK, int DV, int NW, int HPC, int MAXS, typename T, bool TRANS, bool FUSED>
 __global__ void __launch_bounds__(32 * NW * HPC, (step_min_blocks<32 * NW * HPC, MAXS, DK * DV>()))
 kda_step_kernel(const StepArgs a) {
+  // programmatic dependent of the preceding kernel (see launch_pdl)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   using C = StepCfg<DK, DV, NW>;
   using CT = StepCfgT<DK, DV, NW>;
   constexpr int NT = C::NT;
@@ -670,37 +673,40 @@ kda_step_small_kernel(const StepArgs a) {
   }
 }
 
-template <typename T, bool TRANS>
-cudaError_t launch_small(const StepArgs& a, cudaStream_t s) {
-  const int64_t heads = (int64_t)a.B * a.H * a.layers;
-  // programmatic dependent launch on an eager stream: back-to-back calls overlap
-  // one kernel's launch with the previous one's run (each waits on the grid
-  // dependency before its first read).  Inside a stream capture the plain launch
-  // is kept: replayed graphs pipeline their kernel nodes better without it.
+// Launch a step kernel as a programmatic dependent of the preceding kernel on an
+// eager stream: back-to-back calls overlap one kernel's launch with the previous
+// one's run (each kernel waits on the grid dependency before its first read).
+// Inside a stream capture the plain launch is kept: replayed graphs pipeline
+// their kernel nodes better without it.
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const StepArgs& a) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
     cudaGetLastError();
     cap = cudaStreamCaptureStatusActive;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((heads + kSmallHPC - 1) / kSmallHPC));
-  cfg.blockDim = dim3(32 * kSmallHPC);
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = cap == cudaStreamCaptureStatusNone ? 1 : 0;
-  cudaError_t e;
-  if (a.steps <= 1) {
-    e = cudaLaunchKernelEx(&cfg, kda_step_small_kernel<T, TRANS, 1>, a);
-  } else if (a.steps <= 8) {
-    e = cudaLaunchKernelEx(&cfg, kda_step_small_kernel<T, TRANS, 8>, a);
-  } else {
-    e = cudaLaunchKernelEx(&cfg, kda_step_small_kernel<T, TRANS, KDA_MAX_DRAFT>, a);
-  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <typename T, bool TRANS>
+cudaError_t launch_small(const StepArgs& a, cudaStream_t s) {
+  const int64_t heads = (int64_t)a.B * a.H * a.layers;
+  const dim3 grid((unsigned)((heads + kSmallHPC - 1) / kSmallHPC)), block(32 * kSmallHPC);
+  if (a.steps <= 1) return launch_pdl(kda_step_small_kernel<T, TRANS, 1>, grid, block, 0, s, a);
+  if (a.steps <= 8) return launch_pdl(kda_step_small_kernel<T, TRANS, 8>, grid, block, 0, s, a);
+  return launch_pdl(kda_step_small_kernel<T, TRANS, KDA_MAX_DRAFT>, grid, block, 0, s, a);
 }
 
 template <int DK, int DV, typename T, bool TRANS, bool FUSED>
@@ -724,8 +730,7 @@ cudaError_t launch_dims(const StepArgs& a, cudaStream_t s) {
     }
     dim3 block(NT, HPCv);
     int64_t grid = (nheads * a.layers + HPCv - 1) / HPCv;
-    kern<<<(unsigned)grid, block, total, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), block, total, s, a);
   };
   if (FUSED || a.steps == 1) {
     if constexpr (HMAX >= 4) {
