@@ -76,24 +76,6 @@ __device__ __forceinline__ void mma_w(uint32_t d_tmem, uint64_t a, uint64_t b, u
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
       :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
-// A operand from TMEM (lanes = rows, K packed two bf16 per 32-bit column),
-// B from shared memory; issued by one elected lane of a converged warp.
-__device__ __forceinline__ void mma_tw(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{ .reg .pred p, e; .reg .b32 r; elect.sync r|e, 0xffffffff; setp.ne.b32 p, %4, 0; "
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
-      :: "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-// Shared memory -> TMEM copy of 128 rows x 32 bytes described by a matrix
-// descriptor (one 16-wide k-step of a K-major operand tile lands as 8 columns,
-// row r in lane r), issued by one elected lane; ordered before later products
-// of the same thread.
-__device__ __forceinline__ void tmem_cp_w(uint32_t taddr, uint64_t sdesc) {
-  asm volatile(
-      "{ .reg .pred e; .reg .b32 r; elect.sync r|e, 0xffffffff; "
-      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1; }"
-      :: "r"(taddr), "l"(sdesc) : "memory");
-}
 __device__ __forceinline__ void mma_commit_w(uint32_t mbar) {
   asm volatile(
       "{ .reg .pred e; .reg .b32 r; elect.sync r|e, 0xffffffff; "
@@ -131,16 +113,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "r"(taddr) : "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr) : "memory");
-#pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
@@ -214,13 +186,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       :: "r"(dst), "l"(map), "r"(x), "r"(y), "r"(mbar) : "memory");
-}
-
-// 2-D tile of a tensor map fetched into L2 only (no shared memory, no
-// completion to wait for): a later tma_load_2d of the same box hits L2.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
-               :: "l"(map), "r"(x), "r"(y) : "memory");
 }
 
 // Wait for phase `parity` of an mbarrier unless `abort_flag` becomes nonzero,
