@@ -245,9 +245,12 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     const float gmq1 = qb == 0 ? gm[0][1] : (qb == 1 ? gm[1][1] : (qb == 2 ? gm[2][1] : gm[3][1]));
     const float em0 = ex2(gmq0), em1 = ex2(gmq1);                    // e^{Gamma_m}
     const float ec0 = ex2(GC[0] - gmq0), ec1 = ex2(GC[1] - gmq1);    // e^{Gamma_C - Gamma_m}
+    // the two channels of a thread go through packed fp32 (two-lane) multiplies
+    // and adds: the same roundings as scalar ones, half the instructions
+    const float2 em = make_float2(em0, em1), ec = make_float2(ec0, ec1);
     auto rows = [&](auto full_tag) {
       constexpr bool FULL = decltype(full_tag)::value;              // no token past the end
-      float ac0 = acc0[0] - gmq0, ac1 = acc0[1] - gmq1;             // Gamma - Gamma_m, log2 units
+      float2 ac = make_float2(acc0[0] - gmq0, acc0[1] - gmq1);      // Gamma - Gamma_m, log2 units
 #pragma unroll
       for (int rr = 0; rr < 16; ++rr) {
         const int r = 16 * qb + rr;
@@ -257,20 +260,20 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
         __nv_bfloat162* yp = reinterpret_cast<__nv_bfloat162*>(sm + P_APB + oy);
         const float2 kv = in ? __bfloat1622float2(*xp) : make_float2(0.f, 0.f);
         const float2 qv = in ? __bfloat1622float2(*yp) : make_float2(0.f, 0.f);
-        const float p0 = ac0, p1 = ac1;             // Gamma_{r-1} - Gamma_m
-        ac0 += gl[rr].x;                            // Gamma_r - Gamma_m
-        ac1 += gl[rr].y;
-        const float E0 = ex2_normal(ac0), E1 = ex2_normal(ac1), Ei0 = ex2_normal(-ac0), Ei1 = ex2_normal(-ac1);
-        const float EG0 = decay_first ? E0 : ex2_normal(p0), EG1 = decay_first ? E1 : ex2_normal(p1);
-        const float Fq0 = E0 * em0, Fq1 = E1 * em1;       // e^{Gamma}
-        const float Fg0 = EG0 * em0, Fg1 = EG1 * em1;     // e^{G}
-        const float Fc0 = Ei0 * ec0, Fc1 = Ei1 * ec1;     // e^{Gamma_C - Gamma}
-        *reinterpret_cast<__nv_bfloat162*>(sm + P_KHAT + o64) = __floats2bfloat162_rn(kv.x * Ei0, kv.y * Ei1);
-        *reinterpret_cast<__nv_bfloat162*>(sm + P_KTIL + o64) = __floats2bfloat162_rn(kv.x * Fg0, kv.y * Fg1);
-        *reinterpret_cast<__nv_bfloat162*>(img + IMG_WQ + oy) = __floats2bfloat162_rn(qv.x * Fq0, qv.y * Fq1);
-        *reinterpret_cast<__nv_bfloat162*>(img + IMG_KB + o64) = __floats2bfloat162_rn(kv.x * Fc0, kv.y * Fc1);
-        *xp = __floats2bfloat162_rn(kv.x * EG0, kv.y * EG1);     // X = k e^{G - Gamma_m}
-        *yp = __floats2bfloat162_rn(qv.x * E0, qv.y * E1);       // Y = q e^{Gamma - Gamma_m}
+        const float2 p = ac;                        // Gamma_{r-1} - Gamma_m
+        ac = __fadd2_rn(ac, gl[rr]);                // Gamma_r - Gamma_m
+        const float2 E = make_float2(ex2_normal(ac.x), ex2_normal(ac.y));
+        const float2 Ei = make_float2(ex2_normal(-ac.x), ex2_normal(-ac.y));
+        const float2 EG = decay_first ? E : make_float2(ex2_normal(p.x), ex2_normal(p.y));
+        const float2 Fq = __fmul2_rn(E, em);        // e^{Gamma}
+        const float2 Fg = __fmul2_rn(EG, em);       // e^{G}
+        const float2 Fc = __fmul2_rn(Ei, ec);       // e^{Gamma_C - Gamma}
+        *reinterpret_cast<__nv_bfloat162*>(sm + P_KHAT + o64) = __float22bfloat162_rn(__fmul2_rn(kv, Ei));
+        *reinterpret_cast<__nv_bfloat162*>(sm + P_KTIL + o64) = __float22bfloat162_rn(__fmul2_rn(kv, Fg));
+        *reinterpret_cast<__nv_bfloat162*>(img + IMG_WQ + oy) = __float22bfloat162_rn(__fmul2_rn(qv, Fq));
+        *reinterpret_cast<__nv_bfloat162*>(img + IMG_KB + o64) = __float22bfloat162_rn(__fmul2_rn(kv, Fc));
+        *xp = __float22bfloat162_rn(__fmul2_rn(kv, EG));     // X = k e^{G - Gamma_m}
+        *yp = __float22bfloat162_rn(__fmul2_rn(qv, E));      // Y = q e^{Gamma - Gamma_m}
       }
     };
     if (L == C) rows(std::true_type{}); else rows(std::false_type{});
