@@ -44,7 +44,7 @@ from kda_delta_rule_gb300 import inputs as I         # noqa: E402
 
 H, DK, DV, T, STRIDE, CHUNK = 32, 128, 128, 8192, 512, 64
 PREFILL_KERNELS_PER_CALL = 2           # chunk prep + chain, the only launches of a timed step
-E2E_SEGMENT = 1024                      # tokens per copy/compute segment of the end-to-end call
+E2E_SEGMENT = 2048                      # tokens per copy/compute segment of the end-to-end call
 DEC_B, DEC_STEPS = 256, 256
 REP_B, REP_H, REP_D, REP_DRAFT, REP_SETS = 32, 16, 32, 8, 64
 CONV_W = 4                              # ShortConv kernel size of the input-prologue measurements

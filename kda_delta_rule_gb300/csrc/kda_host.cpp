@@ -1,7 +1,8 @@
 // Prefill from host-resident inputs to host-resident outputs, with the copies
 // overlapped with the computation.
 //
-// The token range is cut into segments of at most `segment_tokens` tokens and
+// The token range is cut into segments of at most `segment_tokens` tokens (the
+// first one half that, since its copy-in is not overlapped with anything) and
 // kHostPieces sequence pieces.  A sequence longer than the room left in a
 // segment is cut at a multiple of the checkpoint stride (of the 64-token chunk
 // when there are no checkpoints) counted from its own start, so every piece
@@ -48,6 +49,8 @@ int64_t round_segment(int64_t segment_tokens, int ckpt_stride) {
 
 std::vector<Segment> plan(const int32_t* cu, int N, int64_t T, int64_t seg, int ckpt_stride) {
   const int al = align_of(ckpt_stride);
+  // the first segment is half as long: its copy-in is the only one nothing hides
+  const int64_t first = std::max<int64_t>(al, seg / 2 / al * al);
   std::vector<Segment> out;
   Segment cur{0, 0, {}};
   auto close = [&]() {
@@ -59,7 +62,7 @@ std::vector<Segment> plan(const int32_t* cu, int N, int64_t T, int64_t seg, int 
     int32_t pos = 0;
     do {
       if ((int)cur.pieces.size() == kHostPieces) close();
-      const int64_t room = seg - (cur.t1 - cur.t0);
+      const int64_t room = (out.empty() ? first : seg) - (cur.t1 - cur.t0);
       if (L - pos <= room) {
         cur.pieces.push_back({n, pos, L, L});
         cur.t1 += L - pos;
