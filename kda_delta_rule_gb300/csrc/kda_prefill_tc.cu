@@ -593,8 +593,10 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
 // (MMA1) of the next chunk after all eight row warps have staged the state.
 // The output rows of a chunk are read back by warps 2, 3, 6, 7 while the next
 // chunk's Delta' is formed, when the tensor pipe is idle and they would only
-// wait.  Products report completion on mbarriers (bar1, bar3, bar2); a commit
-// after the eight-warp barrier hands a ring stage back to warp 9.
+// wait.  Products report completion on mbarriers (bar1, bar3, bar2).  A ring
+// stage goes back to warp 9 after nine arrivals: the commit issued after MMA2
+// (every product reading the stage is then done) and one per row warp after
+// its last read of the stage, at the top of the step.
 // Both named barriers OR an error flag over their warps, so the row warps
 // leave the loop together; every mbarrier wait is bounded and watches the
 // abort flag.
