@@ -191,22 +191,28 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   // cumsums are kept in log2 units (g log2(e)), so every factor is one ex2.
   float2 gl[16];
   {
-    float a0 = 0.f, a1 = 0.f, p0 = 0.f, p1 = 0.f;
-    bool bad = false;
+    // both channels in packed form: bf16 min / max of the gates (a NaN carries
+    // through), packed fp32 scaling and sums (the roundings of scalar ones)
+    const __nv_bfloat162 z2 = __float2bfloat162_rn(0.f);
+    __nv_bfloat162 lo = z2, hi = z2;
+    const float2 l2e = make_float2(kLog2e, kLog2e);
+    float2 acc = make_float2(0.f, 0.f), half = acc;
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
       const int r = 16 * qb + rr;
-      const float2 gv = r < L ? __bfloat1622float2(g2[r * 64 + pch]) : make_float2(0.f, 0.f);
-      bad |= !(gv.x >= -10.f && gv.x <= 0.f && gv.y >= -10.f && gv.y <= 0.f);
-      gl[rr] = make_float2(gv.x * kLog2e, gv.y * kLog2e);
-      a0 += gl[rr].x;
-      a1 += gl[rr].y;
-      if (rr == 7) { p0 = a0; p1 = a1; }
+      const __nv_bfloat162 graw = r < L ? g2[r * 64 + pch] : z2;
+      lo = __hmin2_nan(lo, graw);
+      hi = __hmax2_nan(hi, graw);
+      gl[rr] = __fmul2_rn(__bfloat1622float2(graw), l2e);
+      acc = __fadd2_rn(acc, gl[rr]);
+      if (rr == 7) half = acc;
     }
-    part[qb * 64 + pch] = make_float4(p0, p1, a0, a1);
+    part[qb * 64 + pch] = make_float4(half.x, half.y, acc.x, acc.y);
     // the factor bounds below hold for g in [-10, 0]; anything else (or NaN)
     // raises the gate bit of the error word
-    if (bad) atomicOr(&g_kda_device_error, kDevErrGate);
+    const float2 lof = __bfloat1622float2(lo), hif = __bfloat1622float2(hi);
+    if (!(lof.x >= -10.f && lof.y >= -10.f && hif.x <= 0.f && hif.y <= 0.f))
+      atomicOr(&g_kda_device_error, kDevErrGate);
   }
   __syncthreads();
   float gm[4][2], GC[2] = {0.f, 0.f}, acc0[2] = {0.f, 0.f};
