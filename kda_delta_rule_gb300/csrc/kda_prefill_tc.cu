@@ -108,9 +108,12 @@ __device__ __forceinline__ int find_seq(const PrefillSched& s, int chunk) {
   return lo;
 }
 
-// All threads wait on an mbarrier; the outcome is made uniform across the CTA.
+// The CTA waits on an mbarrier: warp 0 polls it while the other warps sleep in
+// the block barrier (no issue slots taken from the co-resident CTA); the barrier
+// passes warp 0's acquire on to every thread and makes the outcome uniform.
 __device__ __forceinline__ bool cta_wait(uint32_t mbar, uint32_t parity) {
-  const bool ok = mbar_wait(mbar, parity);
+  bool ok = true;
+  if ((threadIdx.x >> 5) == 0) ok = mbar_wait(mbar, parity);
   return __syncthreads_and(ok) != 0;
 }
 
