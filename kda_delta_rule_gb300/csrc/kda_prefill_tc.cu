@@ -396,10 +396,16 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       nv = 32;
     }
     if (qd < 2) {
+      // entries with s >= r are never read; two columns per packed fp32 multiply
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int s = s0 + e;
-        if (e < nv) AF[r * 65 + s] = s_beta[s] * v[e];   // entries with s >= r are never read
+      for (int e = 0; e < 32; e += 2) {
+        if (e < nv) {
+          const int s = s0 + e;
+          const float2 b2 = *reinterpret_cast<const float2*>(s_beta + s);
+          const float2 x = __fmul2_rn(make_float2(v[e], v[e + 1]), b2);
+          AF[r * 65 + s] = x.x;
+          AF[r * 65 + s + 1] = x.y;
+        }
       }
     } else {
 #pragma unroll
@@ -418,7 +424,7 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       }
     }
   }
-  for (int e = tid; e < 64 * TS / 4; e += PNT) reinterpret_cast<float4*>(TF)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // (T's blocks above the diagonal are never stored: the [T; T] build writes their zeros)
   fence_before();
   __syncthreads();
   fence_after();
@@ -433,12 +439,13 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
       float arow[16];
 #pragma unroll
       for (int s2 = 0; s2 < j; ++s2) arow[s2] = AF[(b0 + j) * 65 + b0 + s2];
-      float e0 = 0.f, e1 = 0.f;
+      // even and odd terms in the two lanes of one packed fp32 accumulator
+      float2 e = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int s2 = 0; s2 < j; ++s2) {
-        if (s2 & 1) e1 = fmaf(arow[s2], x[s2], e1); else e0 = fmaf(arow[s2], x[s2], e0);
-      }
-      x[j] = j == cc ? 1.f : (j < cc ? 0.f : -(e0 + e1));
+      for (int s2 = 0; s2 + 1 < j; s2 += 2)
+        e = __ffma2_rn(make_float2(arow[s2], arow[s2 + 1]), make_float2(x[s2], x[s2 + 1]), e);
+      if (j & 1) e.x = fmaf(arow[j - 1], x[j - 1], e.x);
+      x[j] = j == cc ? 1.f : (j < cc ? 0.f : -(e.x + e.y));
     }
 #pragma unroll
     for (int j = 0; j < 16; ++j) TF[(b0 + j) * TS + b0 + cc] = x[j];
@@ -522,10 +529,14 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     const int r = tid & 127, c32 = 32 * (tid >> 7);
 #pragma unroll
     for (int cch = 0; cch < 4; ++cch) {
-      const float4 lo = *reinterpret_cast<const float4*>(TF + (r & 63) * TS + c32 + 8 * cch);
-      const float4 hi = *reinterpret_cast<const float4*>(TF + (r & 63) * TS + c32 + 8 * cch + 4);
-      const float t8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-      *reinterpret_cast<uint4*>(sm + P_TOP + off_k(r, c32 + 8 * cch, 128)) = pack8(t8);
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);              // zero above the diagonal blocks
+      if ((c32 + 8 * cch) >> 4 <= (r & 63) >> 4) {
+        const float4 lo = *reinterpret_cast<const float4*>(TF + (r & 63) * TS + c32 + 8 * cch);
+        const float4 hi = *reinterpret_cast<const float4*>(TF + (r & 63) * TS + c32 + 8 * cch + 4);
+        const float t8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        w = pack8(t8);
+      }
+      *reinterpret_cast<uint4*>(sm + P_TOP + off_k(r, c32 + 8 * cch, 128)) = w;
     }
   }
   fence_async_smem();
