@@ -456,13 +456,18 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
   // XT slots [6][16][16]: 0 A10 T00, 1 A32 T22, 2 A21 T11, 3 A31 T11, 4 A20 T00
   // (+ A21 T10), 5 A30 T00 (+ A31 T10).  One thread per row and 4 columns.
   float* XT = reinterpret_cast<float*>(sm + P_XT);
+  // the strip's four columns as two packed fp32 fused multiply-adds (fmaf's rounding)
+  auto fma4 = [](float a, float4 b, float4 acc) {
+    const float2 aa = make_float2(a, a);
+    const float2 lo = __ffma2_rn(aa, make_float2(b.x, b.y), make_float2(acc.x, acc.y));
+    const float2 hi = __ffma2_rn(aa, make_float2(b.z, b.w), make_float2(acc.z, acc.w));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  };
   auto a_t = [&](int I, int K, int J, int ar, int bq, float4 acc) {   // acc += A_IK T_KJ (row ar, cols 4bq..)
 #pragma unroll
     for (int s2 = 0; s2 < 16; ++s2) {
       const float av = AF[(16 * I + ar) * 65 + 16 * K + s2];
-      const float4 t4 = *reinterpret_cast<const float4*>(TF + (16 * K + s2) * TS + 16 * J + 4 * bq);
-      acc.x = fmaf(av, t4.x, acc.x); acc.y = fmaf(av, t4.y, acc.y);
-      acc.z = fmaf(av, t4.z, acc.z); acc.w = fmaf(av, t4.w, acc.w);
+      acc = fma4(av, *reinterpret_cast<const float4*>(TF + (16 * K + s2) * TS + 16 * J + 4 * bq), acc);
     }
     return acc;
   };
@@ -471,9 +476,7 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
     for (int s2 = 0; s2 < 16; ++s2) {
       if (!tri || s2 <= ar) {
         const float tv = TF[(16 * I + ar) * TS + 16 * L + s2];
-        const float4 x4 = *reinterpret_cast<const float4*>(XT + slot * 256 + s2 * 16 + 4 * bq);
-        acc.x = fmaf(tv, x4.x, acc.x); acc.y = fmaf(tv, x4.y, acc.y);
-        acc.z = fmaf(tv, x4.z, acc.z); acc.w = fmaf(tv, x4.w, acc.w);
+        acc = fma4(tv, *reinterpret_cast<const float4*>(XT + slot * 256 + s2 * 16 + 4 * bq), acc);
       }
     }
     return acc;
@@ -565,8 +568,13 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
         const int j = 64 * hw + 16 * cb;
         float v[16];
         tmem_ld16(la + j, v);
+        const float2 nb = make_float2(-br, -br);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] *= -br;
+        for (int e = 0; e < 16; e += 2) {
+          const float2 x = __fmul2_rn(make_float2(v[e], v[e + 1]), nb);
+          v[e] = x.x;
+          v[e + 1] = x.y;
+        }
         *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, j, 128)) = pack8(v);
         *reinterpret_cast<uint4*>(img + IMG_WQ + off_k(r, j + 8, 128)) = pack8(v + 8);
       }
@@ -576,8 +584,13 @@ kda_chunk_prep_kernel(const PrefillArgs a, const PrefillSched sched, unsigned ch
         const int j = (DV / 2) * hw + 16 * cb;
         float v[16];
         tmem_ld16(la + 128 + j, v);
+        const float2 pb = make_float2(br, br);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] *= br;
+        for (int e = 0; e < 16; e += 2) {
+          const float2 x = __fmul2_rn(make_float2(v[e], v[e + 1]), pb);
+          v[e] = x.x;
+          v[e + 1] = x.y;
+        }
         // row r of each 64-column block: 16-byte chunk c at position c ^ (r % 8), so the
         // chain's row-per-thread reads hit distinct banks
         unsigned char* blk = img + IMG_U + (j >> 6) * 8192 + r * 128;
