@@ -239,13 +239,32 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant
       float y[VEC], xs[VEC];
       if (role < 4) load8(tile_s + (row0 + t) * width, xs);
       if (conv_lane) {
+        // channel pairs through packed fp32 multiplies and fused multiply-adds
+        // (the roundings of the scalar ones)
+        float2 acc2[VEC / 2];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          float acc = tap[0][e] * xs[e];
+        for (int e = 0; e < VEC; e += 2)
+          acc2[e / 2] = __fmul2_rn(make_float2(tap[0][e], tap[0][e + 1]), make_float2(xs[e], xs[e + 1]));
 #pragma unroll
-          for (int d = 1; d < W; ++d) acc = fmaf(tap[d][e], ring[((u - d) % R + R) % R][e], acc);
-          if constexpr (HALF_TAPS) y[e] = fmaf(acc, tanh_hw(acc), acc);   // acc = x / 2
-          else y[e] = SILU ? silu_out<T>(acc) : acc;
+        for (int d = 1; d < W; ++d) {
+          const int sl = ((u - d) % R + R) % R;
+#pragma unroll
+          for (int e = 0; e < VEC; e += 2)
+            acc2[e / 2] = __ffma2_rn(make_float2(tap[d][e], tap[d][e + 1]),
+                                     make_float2(ring[sl][e], ring[sl][e + 1]), acc2[e / 2]);
+        }
+#pragma unroll
+        for (int e = 0; e < VEC; e += 2) {
+          const float2 acc = acc2[e / 2];
+          if constexpr (HALF_TAPS) {                           // acc = x / 2
+            const float2 th = make_float2(tanh_hw(acc.x), tanh_hw(acc.y));
+            const float2 r2 = __ffma2_rn(acc, th, acc);
+            y[e] = r2.x;
+            y[e + 1] = r2.y;
+          } else {
+            y[e] = SILU ? silu_out<T>(acc.x) : acc.x;
+            y[e + 1] = SILU ? silu_out<T>(acc.y) : acc.y;
+          }
         }
 #pragma unroll
         for (int e = 0; e < VEC; ++e) ring[u][e] = xs[e];   // the oldest row leaves, token t enters
@@ -253,8 +272,14 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant
         if constexpr (sizeof(T) == 2) {
           // g_min sigmoid(x) = g_min/2 + g_min/2 tanh(x/2) in one rounding
           const float hg = 0.5f * a.g_min;
+          const float2 hg2 = make_float2(hg, hg), h2 = make_float2(0.5f, 0.5f);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) y[e] = fmaf(hg, tanh_hw(0.5f * xs[e]), hg);
+          for (int e = 0; e < VEC; e += 2) {
+            const float2 x2 = __fmul2_rn(h2, make_float2(xs[e], xs[e + 1]));
+            const float2 r2 = __ffma2_rn(hg2, make_float2(tanh_hw(x2.x), tanh_hw(x2.y)), hg2);
+            y[e] = r2.x;
+            y[e + 1] = r2.y;
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < VEC; ++e) y[e] = a.g_min * sigm_out<T>(xs[e]);
@@ -270,8 +295,13 @@ kda_prologue_kernel(const ProArgs a, const ProSched sched, const __grid_constant
         for (int off = NQ / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         if (role < 2) {
           const float inv = rsqrtf(ss + a.eps);
+          const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) y[e] *= inv;
+          for (int e = 0; e < VEC; e += 2) {
+            const float2 r2 = __fmul2_rn(make_float2(y[e], y[e + 1]), inv2);
+            y[e] = r2.x;
+            y[e + 1] = r2.y;
+          }
         }
       }
       if (role < 4) store8(dptr, y);
