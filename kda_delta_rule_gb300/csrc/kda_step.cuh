@@ -634,28 +634,35 @@ kda_step_small_kernel(const StepArgs a) {
       const float4* cq = coef[w][s][1];
       const float4* ce = coef[w][s][2];
       const float4* ck = coef[w][s][3];
-      // four independent chains per sum
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
+      // four independent chains per sum, two per packed fp32 (two-lane) fused
+      // multiply-add: the roundings of scalar ones in half the instructions
+      float2 a01 = make_float2(0.f, 0.f), a23 = a01, b01 = a01, b23 = a01;
 #pragma unroll
       for (int i4 = 0; i4 < D / 4; ++i4) {
         const float4 x = cw[i4], y = cq[i4];
         const int i = 4 * i4;
-        a0 = fmaf(x.x, S[i], a0); a1 = fmaf(x.y, S[i + 1], a1);
-        a2 = fmaf(x.z, S[i + 2], a2); a3 = fmaf(x.w, S[i + 3], a3);
-        b0 = fmaf(y.x, S[i], b0); b1 = fmaf(y.y, S[i + 1], b1);
-        b2 = fmaf(y.z, S[i + 2], b2); b3 = fmaf(y.w, S[i + 3], b3);
+        const float2 s01 = make_float2(S[i], S[i + 1]), s23 = make_float2(S[i + 2], S[i + 3]);
+        a01 = __ffma2_rn(make_float2(x.x, x.y), s01, a01);
+        a23 = __ffma2_rn(make_float2(x.z, x.w), s23, a23);
+        b01 = __ffma2_rn(make_float2(y.x, y.y), s01, b01);
+        b23 = __ffma2_rn(make_float2(y.z, y.w), s23, b23);
       }
-      const float d = rv[s] - ((a0 + a1) + (a2 + a3));
-      const float o = fmaf(rb[s] * kq[s], d, (b0 + b1) + (b2 + b3));
+      const float d = rv[s] - ((a01.x + a01.y) + (a23.x + a23.y));
+      const float o = fmaf(rb[s] * kq[s], d, (b01.x + b01.y) + (b23.x + b23.y));
       orow[s * a.out_step_stride] = from_f32<T>(live_state ? o : 0.f);
+      const float2 d2 = make_float2(d, d);
 #pragma unroll
       for (int i4 = 0; i4 < D / 4; ++i4) {
         const float4 e4 = ce[i4], k4 = ck[i4];
         const int i = 4 * i4;
-        S[i] = fmaf(e4.x, S[i], k4.x * d);
-        S[i + 1] = fmaf(e4.y, S[i + 1], k4.y * d);
-        S[i + 2] = fmaf(e4.z, S[i + 2], k4.z * d);
-        S[i + 3] = fmaf(e4.w, S[i + 3], k4.w * d);
+        const float2 lo = __ffma2_rn(make_float2(e4.x, e4.y), make_float2(S[i], S[i + 1]),
+                                     __fmul2_rn(make_float2(k4.x, k4.y), d2));
+        const float2 hi = __ffma2_rn(make_float2(e4.z, e4.w), make_float2(S[i + 2], S[i + 3]),
+                                     __fmul2_rn(make_float2(k4.z, k4.w), d2));
+        S[i] = lo.x;
+        S[i + 1] = lo.y;
+        S[i + 2] = hi.x;
+        S[i + 3] = hi.y;
       }
     }
   }
