@@ -2,6 +2,7 @@
 
     python -m kda_delta_rule_gb300.cases decode   [--reps N]   # B=256 H=32 d=128, bf16 projections
     python -m kda_delta_rule_gb300.cases replay   [--reps N]   # B=32 H=16 d=32 draft 8, fp32
+    python -m kda_delta_rule_gb300.cases replay_layers [--reps N]   # the same for 64 stacked layers, one launch
     python -m kda_delta_rule_gb300.cases prefill  [--reps N]   # T=8192 H=32 d=128 bf16, 16 checkpoints
     python -m kda_delta_rule_gb300.cases varlen   [--reps N]   # 64 seqs, ~0.5M tokens, H=32 d=128 bf16
     python -m kda_delta_rule_gb300.cases pack     [--reps N]   # pack+unpack of a (256,32,128,128) state
@@ -51,6 +52,20 @@ def case_replay(reps):
     out = torch.empty(32, 16, 8, 32, device="cuda")
     return _time(lambda: K.kda_verify_replay(S, pr.q, pr.k, pr.v, pr.g, pr.beta, n, S_new=S_new, out=out),
                  reps)
+
+
+def case_replay_layers(reps, layers=64):
+    """64 stacked KDA layers of the replay shape, each with its own state and draft
+    projections and the accepted counts shared, in one kda_verify_replay_layers launch."""
+    sets = [I.replay_inputs(32, 16, 32, 32, 8, dtype=torch.float32, seed=i, device="cuda") for i in range(layers)]
+    n = sets[0][2].to("cuda")
+    S = torch.stack([x[0] for x in sets])
+    pj = {nm: torch.stack([getattr(x[1], nm) for x in sets]) for nm in ("q", "k", "v", "g", "beta")}
+    del sets
+    S_new = torch.empty_like(S)
+    out = torch.empty(layers, 32, 16, 8, 32, device="cuda")
+    return _time(lambda: K.kda_verify_replay_layers(S, pj["q"], pj["k"], pj["v"], pj["g"], pj["beta"], n,
+                                                    S_new=S_new, out=out), reps)
 
 
 def _prefill(lengths, reps, H=32, d=128, stride=512):
@@ -147,7 +162,8 @@ def case_scan32(reps):
     return case_scan(reps, T=8192, H=32, segments=4)
 
 
-CASES = {"scan": case_scan, "scan32": case_scan32, "decode": case_decode, "replay": case_replay, "prefill": case_prefill,
+CASES = {"scan": case_scan, "scan32": case_scan32, "decode": case_decode, "replay": case_replay,
+         "replay_layers": case_replay_layers, "prefill": case_prefill,
          "varlen": case_varlen, "pack": case_pack, "layer": case_layer, "prologue": case_prologue, "decode_vk": case_decode_vk,
          "decode_fused": case_decode_fused}
 
