@@ -530,10 +530,11 @@ kda_step_kernel(const StepArgs a) {
 // registers).  Both row reductions of a step are then the lane's own dot products
 // (a_j = sum_i w_i S_ij, b_j = sum_i e^{g_i} q_i S_ij) with no shuffles, and the
 // per-step row coefficients w_i, e^{g_i} q_i, e^{g_i}, beta k_i are shared-memory
-// broadcasts staged once per call.  One warp per CTA: at ~106 registers a thread an
-// SM then holds 18 of them (four-warp CTAs fit 16), and a single call's heads spread
-// over every SM (64 stacked layers 70.0 -> 68.7 us, one call in a CUDA graph 5.32 ->
-// 5.19 us, against four heads per CTA).
+// broadcasts staged once per call.  One warp per CTA: heads of different sequences
+// run different accepted counts, and a CTA's registers come back only when its last
+// warp ends, so one-warp CTAs hand each slot on as soon as its head is done; a single
+// call's heads also spread over every SM (64 stacked layers 70.0 -> 68.7 us, one call
+// in a CUDA graph 5.32 -> 5.19 us, against four heads per CTA).
 constexpr int kSmallD = 32;
 constexpr int kSmallHPC = 1;          // heads (warps) per CTA
 
