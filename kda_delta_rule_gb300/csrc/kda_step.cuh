@@ -35,6 +35,8 @@
 // This header holds the kernel and its launch templates; kda_step_{kv,vk}_{f32,bf16}.cu
 // instantiate one state layout and projection dtype each, kda_step.cu dispatches.
 #pragma once
+#include <atomic>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "../../include/kda.h"
@@ -535,13 +537,20 @@ kda_step_kernel(const StepArgs a) {
 // warp ends, so one-warp CTAs hand each slot on as soon as its head is done; a single
 // call's heads also spread over every SM (64 stacked layers 70.0 -> 68.7 us, one call
 // in a CUDA graph 5.32 -> 5.19 us, against four heads per CTA).
+// SPLIT = 2 gives each head two warps, 16 columns each, lane pairs (l, l + 16)
+// sharing a column and taking its upper and lower 16 rows: half the dependent
+// work per lane and one shuffle per sum, for calls whose heads would leave most
+// warp slots of the GPU empty (a single call's latency is then the point).
 constexpr int kSmallD = 32;
 constexpr int kSmallHPC = 1;          // heads (warps) per CTA
 
-template <typename T, bool TRANS, int MAXS>
+template <typename T, bool TRANS, int MAXS, int SPLIT>
 __global__ void __launch_bounds__(32 * kSmallHPC)
 kda_step_small_kernel(const StepArgs a) {
   constexpr int D = kSmallD;
+  constexpr int NCOL = D / SPLIT;                      // state columns of one warp
+  constexpr int RW = D * NCOL / 32;                    // state rows of one lane
+  static_assert(SPLIT == 1 || SPLIT == 2, "one or two warps per head");
   __shared__ float4 coef[kSmallHPC][MAXS][4][D / 4];   // per step: w, e^g q, e^g, beta k (rows 0..31)
   // launched as a programmatic dependent of the preceding kernel: the next launch
   // may be placed at once, and nothing is read before the preceding kernel's
@@ -550,8 +559,11 @@ kda_step_small_kernel(const StepArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t nheads = (int64_t)a.B * a.H;
-  const int64_t head = (int64_t)blockIdx.x * kSmallHPC + w;   // over all stacked layers
+  const int64_t unit = (int64_t)blockIdx.x * kSmallHPC + w;   // (head, column part)
+  const int64_t head = unit / SPLIT;                          // over all stacked layers
   if (head >= nheads * a.layers) return;                      // whole warps leave; no CTA barrier follows
+  const int j = (int)(unit % SPLIT) * NCOL + lane % NCOL;     // this lane's state column
+  const int r0 = (lane / NCOL) * RW;                          // and its first row
   const int64_t layer = head / nheads, hl = head - layer * nheads;
   const int b = (int)(hl / a.H);
   int n = a.steps;
@@ -568,26 +580,26 @@ kda_step_small_kernel(const StepArgs a) {
     srow_in = live_state ? h0 + (int64_t)si * a.H : 0;
     srow_out = live_state ? h0 + (int64_t)so * a.H : 0;
   }
-  // ---- state: column `lane` (stored (dk, dv): one coalesced row per load;
-  // stored (dv, dk): the lane's own 128-byte row of S^T) ----
-  float S[D];
+  // ---- state: rows r0 .. r0 + RW - 1 of column j (stored (dk, dv): coalesced
+  // row segments; stored (dv, dk): a contiguous piece of row j of S^T) ----
+  float S[RW];
   const float* Sin = a.S_in + srow_in * (int64_t)(D * D);
   if (live_state) {
     if constexpr (TRANS) {
 #pragma unroll
-      for (int i = 0; i < D; i += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(Sin + lane * D + i);
+      for (int i = 0; i < RW; i += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(Sin + j * D + r0 + i);
         S[i] = x.x; S[i + 1] = x.y; S[i + 2] = x.z; S[i + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < D; ++i) S[i] = Sin[i * D + lane];
+      for (int i = 0; i < RW; ++i) S[i] = Sin[(r0 + i) * D + j];
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < D; ++i) S[i] = 0.f;
+    for (int i = 0; i < RW; ++i) S[i] = 0.f;
   }
-  // ---- projections of every step: lane i brings key channel i (and value channel i) ----
+  // ---- projections of every step: lane i brings key channel i, and value channel j ----
   const T* q = reinterpret_cast<const T*>(a.q);
   const T* k = reinterpret_cast<const T*>(a.k);
   const T* v = reinterpret_cast<const T*>(a.v);
@@ -603,7 +615,7 @@ kda_step_small_kernel(const StepArgs a) {
     rk[s] = live ? to_f32(k[hs * D + lane]) : 0.f;
     rq[s] = live ? to_f32(q[hs * D + lane]) : 0.f;
     rg[s] = live ? to_f32(g[hs * D + lane]) : 0.f;
-    rv[s] = live ? to_f32(v[hs * D + lane]) : 0.f;
+    rv[s] = live ? to_f32(v[hs * D + j]) : 0.f;
     rb[s] = live ? to_f32(beta[hs]) : 0.f;
   }
   // per-step row coefficients of the accepted steps
@@ -629,7 +641,8 @@ kda_step_small_kernel(const StepArgs a) {
   __syncwarp();
   // ---- the accepted steps ----
   T* out = reinterpret_cast<T*>(a.out);
-  T* orow = out + head * a.out_head_stride + lane;
+  T* orow = out + head * a.out_head_stride + j;
+  const bool writer = r0 == 0;                         // one lane per column writes the outputs
 #pragma unroll
   for (int s = 0; s < MAXS; ++s) {
     if (s < n) {
@@ -637,12 +650,14 @@ kda_step_small_kernel(const StepArgs a) {
       const float4* cq = coef[w][s][1];
       const float4* ce = coef[w][s][2];
       const float4* ck = coef[w][s][3];
-      // four independent chains per sum, two per packed fp32 (two-lane) fused
-      // multiply-add: the roundings of scalar ones in half the instructions
+      // four independent chains per sum over the lane's rows, two per packed fp32
+      // (two-lane) fused multiply-add: the roundings of scalar ones in half the
+      // instructions; at SPLIT = 2 the partner lane's sum over the other 16 rows of
+      // the column is added last (so the two forms differ in the last bits)
       float2 a01 = make_float2(0.f, 0.f), a23 = a01, b01 = a01, b23 = a01;
 #pragma unroll
-      for (int i4 = 0; i4 < D / 4; ++i4) {
-        const float4 x = cw[i4], y = cq[i4];
+      for (int i4 = 0; i4 < RW / 4; ++i4) {
+        const float4 x = cw[r0 / 4 + i4], y = cq[r0 / 4 + i4];
         const int i = 4 * i4;
         const float2 s01 = make_float2(S[i], S[i + 1]), s23 = make_float2(S[i + 2], S[i + 3]);
         a01 = __ffma2_rn(make_float2(x.x, x.y), s01, a01);
@@ -650,13 +665,18 @@ kda_step_small_kernel(const StepArgs a) {
         b01 = __ffma2_rn(make_float2(y.x, y.y), s01, b01);
         b23 = __ffma2_rn(make_float2(y.z, y.w), s23, b23);
       }
-      const float d = rv[s] - ((a01.x + a01.y) + (a23.x + a23.y));
-      const float o = fmaf(rb[s] * kq[s], d, (b01.x + b01.y) + (b23.x + b23.y));
-      orow[s * a.out_step_stride] = from_f32<T>(live_state ? o : 0.f);
+      float sa = (a01.x + a01.y) + (a23.x + a23.y), sb = (b01.x + b01.y) + (b23.x + b23.y);
+      if constexpr (SPLIT == 2) {         // lanes l and l ^ 16 add the same two terms
+        sa += __shfl_xor_sync(0xffffffffu, sa, 16);
+        sb += __shfl_xor_sync(0xffffffffu, sb, 16);
+      }
+      const float d = rv[s] - sa;
+      const float o = fmaf(rb[s] * kq[s], d, sb);
+      if (writer) orow[s * a.out_step_stride] = from_f32<T>(live_state ? o : 0.f);
       const float2 d2 = make_float2(d, d);
 #pragma unroll
-      for (int i4 = 0; i4 < D / 4; ++i4) {
-        const float4 e4 = ce[i4], k4 = ck[i4];
+      for (int i4 = 0; i4 < RW / 4; ++i4) {
+        const float4 e4 = ce[r0 / 4 + i4], k4 = ck[r0 / 4 + i4];
         const int i = 4 * i4;
         const float2 lo = __ffma2_rn(make_float2(e4.x, e4.y), make_float2(S[i], S[i + 1]),
                                      __fmul2_rn(make_float2(k4.x, k4.y), d2));
@@ -670,16 +690,17 @@ kda_step_small_kernel(const StepArgs a) {
     }
   }
   // steps past the accepted prefix produce zero output rows
-  for (int s = n; s < a.steps; ++s) orow[s * a.out_step_stride] = from_f32<T>(0.f);
+  if (writer)
+    for (int s = n; s < a.steps; ++s) orow[s * a.out_step_stride] = from_f32<T>(0.f);
   if (!live_state) return;
   float* Sout = a.S_out + srow_out * (int64_t)(D * D);
   if constexpr (TRANS) {
 #pragma unroll
-    for (int i = 0; i < D; i += 4)
-      *reinterpret_cast<float4*>(Sout + lane * D + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+    for (int i = 0; i < RW; i += 4)
+      *reinterpret_cast<float4*>(Sout + j * D + r0 + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
   } else {
 #pragma unroll
-    for (int i = 0; i < D; ++i) Sout[i * D + lane] = S[i];
+    for (int i = 0; i < RW; ++i) Sout[(r0 + i) * D + j] = S[i];
   }
 }
 
@@ -710,13 +731,36 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   return cudaGetLastError();
 }
 
+// SM count of the current device, looked up once per device.
+inline cudaError_t step_device_sms(int* sms) {
+  static std::atomic<int> cache[64];            // 0 = not looked up yet
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && (*sms = cache[dev].load(std::memory_order_relaxed)) > 0) return cudaSuccess;
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess && cached) cache[dev].store(*sms, std::memory_order_relaxed);
+  return e;
+}
+
+template <typename T, bool TRANS, int SPLIT>
+cudaError_t launch_small_split(const StepArgs& a, cudaStream_t s) {
+  const int64_t units = (int64_t)a.B * a.H * a.layers * SPLIT;
+  const dim3 grid((unsigned)((units + kSmallHPC - 1) / kSmallHPC)), block(32 * kSmallHPC);
+  if (a.steps <= 1) return launch_pdl(kda_step_small_kernel<T, TRANS, 1, SPLIT>, grid, block, 0, s, a);
+  if (a.steps <= 8) return launch_pdl(kda_step_small_kernel<T, TRANS, 8, SPLIT>, grid, block, 0, s, a);
+  return launch_pdl(kda_step_small_kernel<T, TRANS, KDA_MAX_DRAFT, SPLIT>, grid, block, 0, s, a);
+}
+
 template <typename T, bool TRANS>
 cudaError_t launch_small(const StepArgs& a, cudaStream_t s) {
+  // two warps per head while the doubled grid stays within 16 warps per SM
+  int sms = 0;
+  cudaError_t e = step_device_sms(&sms);
+  if (e != cudaSuccess) return e;
   const int64_t heads = (int64_t)a.B * a.H * a.layers;
-  const dim3 grid((unsigned)((heads + kSmallHPC - 1) / kSmallHPC)), block(32 * kSmallHPC);
-  if (a.steps <= 1) return launch_pdl(kda_step_small_kernel<T, TRANS, 1>, grid, block, 0, s, a);
-  if (a.steps <= 8) return launch_pdl(kda_step_small_kernel<T, TRANS, 8>, grid, block, 0, s, a);
-  return launch_pdl(kda_step_small_kernel<T, TRANS, KDA_MAX_DRAFT>, grid, block, 0, s, a);
+  return 2 * heads <= 16 * (int64_t)sms ? launch_small_split<T, TRANS, 2>(a, s) : launch_small_split<T, TRANS, 1>(a, s);
 }
 
 template <int DK, int DV, typename T, bool TRANS, bool FUSED>

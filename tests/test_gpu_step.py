@@ -130,6 +130,45 @@ def test_replay_refuses_in_place(K):
     assert e.value.status == -7
 
 
+@pytest.mark.parametrize("trans", [False, True])
+def test_small_head_replay_forms_agree(K, trans):
+    """32 x 32 heads run one warp per head when the heads fill the GPU and two warps per
+    head (16 columns each) when they would not: 4,096 stacked heads take the first form,
+    each 512-head layer alone the second.  The two agree to fp32 rounding (their sums
+    associate differently) and each stays within tolerance of the oracle; a transposed
+    slot pool gives the same bits as the (dk, dv) states in either form."""
+    Lr, B, H, D, draft = 8, 32, 16, 32, 8
+    sets = [I.replay_inputs(B, H, D, D, draft, dtype=torch.float32, seed=90 + l) for l in range(Lr)]
+    n_acc = sets[0][2].cuda()
+    S = torch.stack([s_[0] for s_ in sets]).cuda()
+    cat = lambda name: torch.stack([getattr(s_[1], name) for s_ in sets]).cuda()
+    q, k, v, g, beta = (cat(nm) for nm in ("q", "k", "v", "g", "beta"))
+    S_new, out = K.kda_verify_replay_layers(S, q, k, v, g, beta, n_acc)
+    torch.cuda.synchronize()
+    singles = []
+    for l in range(Lr):
+        S1, o1 = K.kda_verify_replay(S[l], q[l], k[l], v[l], g[l], beta[l], n_acc)
+        torch.cuda.synchronize()
+        singles.append((S1, o1))
+        assert rel(S1, S_new[l]) < 1e-5 and rel(o1, out[l]) < 1e-5, f"layer {l}"
+    for l in (0, Lr - 1):
+        S_ref, out_ref = O.verify_and_replay_batched(f(S[l]), f(q[l]), f(k[l]), f(v[l]), f(g[l]), f(beta[l]),
+                                                     n_acc.cpu().numpy())
+        assert rel(S_new[l], S_ref) < TOL_F32 and rel(out[l], out_ref) < TOL_F32
+        assert rel(singles[l][0], S_ref) < TOL_F32 and rel(singles[l][1], out_ref) < TOL_F32
+    if trans:
+        # the same layers from transposed pools of B slots each (identity slot ids):
+        # the stacked call, then layer 0 alone (the other form)
+        pool = S.transpose(-1, -2).contiguous()
+        ids = torch.arange(B, dtype=torch.int32, device="cuda")
+        pool_new, o_t = K.kda_verify_replay_slots(pool, q, k, v, g, beta, n_acc, ids, layout=K.LAYOUT_VK)
+        p0_new, o0 = K.kda_verify_replay_slots(pool[:1], q[:1], k[:1], v[:1], g[:1], beta[:1], n_acc, ids,
+                                               layout=K.LAYOUT_VK)
+        torch.cuda.synchronize()
+        assert torch.equal(o_t, out) and torch.equal(pool_new.transpose(-1, -2), S_new)
+        assert torch.equal(o0[0], singles[0][1]) and torch.equal(p0_new[0].transpose(-1, -2), singles[0][0])
+
+
 @pytest.mark.parametrize("dk,dv,dtype", [(32, 32, torch.float32), (128, 128, torch.bfloat16)])
 def test_replay_layers_match_single_calls_and_oracle(K, dk, dv, dtype):
     """Three stacked layers in one launch: bit-identical to three single-layer calls,
